@@ -1,0 +1,174 @@
+"""Seeded synthetic workloads for the routed-expert FFN (decode regime).
+
+This module is shared by the CUDA path's tests/bench and by the CPU oracle's
+tests. It holds only input generation: the expert shapes, the seeded draws and
+the offline INT8 weight quantiser that prepares the weights both sides consume.
+It holds none of the routed-expert FFN's arithmetic (routing, gather, FFN,
+combine).
+
+Expert shapes and routing top-k come from HiNa-MoE (arXiv 2610.05123),
+§8.1 Table 3 ("Expert weight matrix dimensions and routing strategies"):
+    Mixtral-8x7B   Gate/Up 4096x14336, Down 14336x4096, Top-2
+    Mixtral-8x22B  Gate/Up 6144x16384, Down 16384x6144, Top-2
+    DeepSeek-V3    Gate/Up 7168x2048,  Down 2048x7168,  Top-8
+    Qwen3-235B     Gate/Up 4096x1536,  Down 1536x4096,  Top-8
+Table 3 prints Gate/Up as (hidden x intermediate) in math order; the weights
+here are stored the way §2.2 (Figure 3, "general layout") and Algorithm 1's
+W(n:n+32, k:k+32) index them: one output row per line, reduction contiguous,
+i.e. W_gate/W_up[E, I, H] and W_down[E, H, I].
+
+Expert counts: Mixtral 8, DeepSeek-V3 256, Qwen3-235B 128 (RapidMoE,
+arXiv 2610.01265, "Models"). The per-expert token range 1-16 follows HiNa-MoE
+§7.3 / Figure 10.
+
+Draws: x ~ N(0,1) -> bf16, router logits ~ N(0,1) f32, weights ~ N(0, 0.02)
+-> bf16 (round to nearest even). The INT8 variant quantises those bf16 draws
+symmetrically per group of 128 along the reduction dimension (HiNa-MoE §8.1,
+"same symmetric group-wise quantization scheme"; group size, scale dtype and
+rounding are not printed there, so: scale = max|w|/127 in fp32, q =
+clamp(round_half_even(w/scale), -127, 127), and an all-zero group gets scale 1).
+
+Every weight tensor is drawn expert by expert from its own generator, seeded
+from (seed, tensor, expert), so one expert's weights never depend on how many
+other experts exist or on the device chunking. Draws on CPU and on CUDA use
+different torch generators and are not equal to each other: a test draws once
+and hands the same tensors to both sides.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional, Sequence, Tuple
+
+import torch
+
+GROUP = 128  # INT8 quantisation group along the reduction dimension
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEConfig:
+    name: str
+    H: int            # hidden size (gate/up reduction, down output rows)
+    I: int            # intermediate size (gate/up output rows, down reduction)
+    E: int            # routed experts
+    top_k: int
+    wtype: str        # "bf16" or "int8"
+    T: Tuple[int, ...]  # token counts the workload is run at
+    skew_experts: Tuple[int, ...] = ()
+    skew: float = 0.0
+    seed: int = 0
+
+    @property
+    def weight_bytes_per_expert(self) -> int:
+        """Algorithmic weight-stream bytes of one expert (3 matrices + scales)."""
+        per = 3 * self.H * self.I * (1 if self.wtype == "int8" else 2)
+        if self.wtype == "int8":
+            per += 4 * (2 * self.I * (self.H // GROUP) + self.H * (self.I // GROUP))
+        return per
+
+
+CONFIGS: Dict[str, MoEConfig] = {
+    c.name: c
+    for c in (
+        MoEConfig("tiny", 256, 512, 8, 2, "bf16", (8,)),
+        MoEConfig("mixtral8x7b", 4096, 14336, 8, 2, "bf16", (1, 2, 4, 8, 16, 32, 64)),
+        MoEConfig("mixtral8x22b", 6144, 16384, 8, 2, "bf16", (1, 4, 16, 64)),
+        # "a skewed variant adding +2.0 to two fixed experts' logits": the two
+        # experts are not named; this build takes experts 0 and 1.
+        MoEConfig("mixtral8x22b_skew", 6144, 16384, 8, 2, "bf16", (1, 4, 16, 64),
+                  skew_experts=(0, 1), skew=2.0),
+        MoEConfig("dsv3", 7168, 2048, 256, 8, "bf16", (1, 16, 128, 512)),
+        MoEConfig("qwen3_int8", 4096, 1536, 128, 8, "int8", (1, 8, 64, 256)),
+    )
+}
+
+# tensor ids for generator seeding
+_X, _LOGITS, _WG, _WU, _WD = 0, 1, 2, 3, 4
+
+
+def _gen(device, seed: int, tensor: int, expert: int = 0) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed((seed * 1_000_003 + tensor * 65_537 + expert * 7919 + 12345) % (2**63 - 1))
+    return g
+
+
+def draw_x(T: int, H: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    g = _gen(device, seed, _X)
+    return torch.randn(T, H, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def draw_logits(T: int, E: int, seed: int = 0, device="cpu",
+                skew_experts: Sequence[int] = (), skew: float = 0.0) -> torch.Tensor:
+    g = _gen(device, seed, _LOGITS)
+    lg = torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
+    for e in skew_experts:
+        lg[:, e] += skew
+    return lg
+
+
+def draw_expert_weight(rows: int, K: int, seed: int, tensor: int, expert: int,
+                       device="cpu", std: float = 0.02) -> torch.Tensor:
+    g = _gen(device, seed, tensor, expert)
+    w = torch.randn(rows, K, generator=g, device=device, dtype=torch.float32)
+    return (w * std).to(torch.bfloat16)
+
+
+def draw_weights(E: int, rows: int, K: int, seed: int, tensor: int, device="cpu",
+                 experts: Optional[Sequence[int]] = None) -> torch.Tensor:
+    """[len(experts) or E, rows, K] bf16, drawn expert by expert."""
+    ids = range(E) if experts is None else experts
+    out = torch.empty(len(ids), rows, K, device=device, dtype=torch.bfloat16)
+    for n, e in enumerate(ids):
+        out[n] = draw_expert_weight(rows, K, seed, tensor, e, device)
+    return out
+
+
+def quantize_int8_groupwise(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Offline weight preparation: bf16 [..., rows, K] -> (int8 q, fp32 scale[..., rows, K/128]).
+
+    Symmetric per-group quantisation along the last (reduction) axis.
+    """
+    K = w.shape[-1]
+    if K % GROUP:
+        raise ValueError(f"reduction length {K} is not a multiple of {GROUP}")
+    wf = w.float().reshape(*w.shape[:-1], K // GROUP, GROUP)
+    s = wf.abs().amax(dim=-1) / 127.0
+    zero = s == 0
+    s = torch.where(zero, torch.ones_like(s), s)
+    q = torch.round(wf / s.unsqueeze(-1)).clamp_(-127, 127)
+    q = torch.where(zero.unsqueeze(-1), torch.zeros_like(q), q)
+    return q.to(torch.int8).reshape(w.shape), s.contiguous()
+
+
+def make_layer(cfg: MoEConfig, seed: Optional[int] = None, device="cpu",
+               experts: Optional[Sequence[int]] = None) -> Dict[str, torch.Tensor]:
+    """Expert weights of one MoE layer: W_gate/W_up [E,I,H], W_down [E,H,I] (+ INT8 scales).
+
+    For INT8 the returned W_* are int8 and s_* hold the fp32 group scales
+    (s_gate/s_up [E,I,H/128], s_down [E,H,I/128]); for BF16 s_* are None.
+    """
+    seed = cfg.seed if seed is None else seed
+    wg = draw_weights(cfg.E, cfg.I, cfg.H, seed, _WG, device, experts)
+    wu = draw_weights(cfg.E, cfg.I, cfg.H, seed, _WU, device, experts)
+    wd = draw_weights(cfg.E, cfg.H, cfg.I, seed, _WD, device, experts)
+    if cfg.wtype == "bf16":
+        return dict(W_gate=wg, W_up=wu, W_down=wd, s_gate=None, s_up=None, s_down=None)
+    qg, sg = quantize_int8_groupwise(wg)
+    del wg
+    qu, su = quantize_int8_groupwise(wu)
+    del wu
+    qd, sd = quantize_int8_groupwise(wd)
+    del wd
+    return dict(W_gate=qg, W_up=qu, W_down=qd, s_gate=sg, s_up=su, s_down=sd)
+
+
+def make_tokens(cfg: MoEConfig, T: int, seed: Optional[int] = None, device="cpu"):
+    """(x [T,H] bf16, router logits [T,E] f32) for one decode step."""
+    seed = cfg.seed if seed is None else seed
+    x = draw_x(T, cfg.H, seed, device)
+    lg = draw_logits(T, cfg.E, seed, device, cfg.skew_experts, cfg.skew)
+    return x, lg
+
+
+def expected_active(cfg: MoEConfig, T: int) -> float:
+    """E[A] under uniform routing: E * (1 - (1 - k/E)^T)."""
+    return cfg.E * (1.0 - (1.0 - cfg.top_k / cfg.E) ** T)
