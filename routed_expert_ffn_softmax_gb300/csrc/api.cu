@@ -1,0 +1,266 @@
+// C ABI of the routed-expert FFN library (declared in include/moe.h).
+// Host-side argument checks, workspace layout and the launch sequence.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "../../include/moe.h"
+#include "expert_stream.cuh"
+#include "moe_launch.h"
+
+namespace {
+
+using moe::stream::kMaxCtas;
+using moe::stream::kPartialFloats;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Workspace layout, in order (each section 256-byte aligned):
+//   ctrl      status word (byte 0) + stream-K counters at byte 256
+//   partials  stream-K partial slots
+//   h         [P, I] bf16 (gate+up output)
+//   --- moe_ffn_forward only ---
+//   ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg [P,H] bf16, Y [P,H] f32
+constexpr size_t kCtrlBytes = 2048;
+constexpr size_t kCountersOffset = 256;
+constexpr int kZeroWords = static_cast<int>((kCountersOffset + 4 * kMaxCtas) / 4);
+
+struct Layout {
+  size_t ctrl, partials, h, ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg, Y, total;
+};
+
+Layout layout(int64_t P, int H, int I, int E) {
+  Layout L{};
+  size_t o = 0;
+  L.ctrl = o;
+  o += kCtrlBytes;
+  L.partials = o;
+  o = align_up(o + sizeof(float) * static_cast<size_t>(kMaxCtas) * 2 * kPartialFloats);
+  L.h = o;
+  o = align_up(o + 2 * static_cast<size_t>(P) * I);
+  L.ids = o;
+  o = align_up(o + 4 * static_cast<size_t>(P));
+  L.w = o;
+  o = align_up(o + 4 * static_cast<size_t>(P));
+  L.counts = o;
+  o = align_up(o + 4 * static_cast<size_t>(E));
+  L.offsets = o;
+  o = align_up(o + 4 * static_cast<size_t>(E + 1));
+  L.sorted_token = o;
+  o = align_up(o + 4 * static_cast<size_t>(P));
+  L.inv_pos = o;
+  o = align_up(o + 4 * static_cast<size_t>(P));
+  L.active = o;
+  o = align_up(o + 4 * static_cast<size_t>(E));
+  L.num_active = o;
+  o = align_up(o + 4);
+  L.xg = o;
+  o = align_up(o + 2 * static_cast<size_t>(P) * H);
+  L.Y = o;
+  o = align_up(o + 4 * static_cast<size_t>(P) * H);
+  L.total = o;
+  return L;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Size checks shared by the entry points. Returns MOE_OK or the error to report.
+moe_status_t check_sizes(int T, int H, int I, int E, int top_k, moe_wtype_t wtype) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || top_k < 1) return MOE_ERR_INVALID_ARG;
+  if (wtype != MOE_W_BF16 && wtype != MOE_W_INT8_G128) return MOE_ERR_INVALID_ARG;
+  if (top_k > E) return MOE_ERR_INVALID_ARG;
+  if (E > 256) return MOE_ERR_UNSUPPORTED;
+  const int m = wtype == MOE_W_INT8_G128 ? 128 : 8;
+  if (H % m || I % m) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * top_k > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev < kMaxDev) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return -1;
+  if (dev < kMaxDev) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const int32_t* active,
+                            const int32_t* num_active, const void* Wg, const void* Wu, const void* Wd,
+                            const float* sg, const float* su, const float* sd, moe_wtype_t wtype, int H, int I,
+                            int E, int P, float* Y, char* ws, cudaStream_t stream) {
+  const int sms = sm_count();
+  if (sms < 1) return MOE_ERR_CUDA;
+  const Layout L = layout(P, H, I, E);
+  moe::ExpertFfnPlan plan{};
+  plan.xg = xg;
+  plan.offsets = offsets;
+  plan.active = active;
+  plan.num_active = num_active;
+  plan.W_gate = Wg;
+  plan.W_up = Wu;
+  plan.W_down = Wd;
+  plan.s_gate = sg;
+  plan.s_up = su;
+  plan.s_down = sd;
+  plan.int8 = wtype == MOE_W_INT8_G128;
+  plan.H = H;
+  plan.I = I;
+  plan.E = E;
+  plan.P = P;
+  plan.h = reinterpret_cast<uint16_t*>(ws + L.h);
+  plan.Y = Y;
+  plan.partials = reinterpret_cast<float*>(ws + L.partials);
+  plan.counters = reinterpret_cast<int32_t*>(ws + L.ctrl + kCountersOffset);
+  plan.status = reinterpret_cast<int32_t*>(ws + L.ctrl);
+  plan.num_ctas = sms < kMaxCtas ? sms : kMaxCtas;
+  return cuda_status(moe::launch_expert_ffn(plan, stream));
+}
+
+bool weights_ok(const void* Wg, const void* Wu, const void* Wd, const float* sg, const float* su,
+                const float* sd, moe_wtype_t wtype) {
+  if (!Wg || !Wu || !Wd || !aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16)) return false;
+  if (wtype == MOE_W_INT8_G128 &&
+      (!sg || !su || !sd || !aligned(sg, 4) || !aligned(su, 4) || !aligned(sd, 4)))
+    return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: outside what this library implements";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA call or kernel launch failed";
+  }
+  return "unknown moe_status_t";
+}
+
+size_t moe_workspace_size(int T, int H, int I, int E, int top_k, moe_wtype_t wtype) {
+  if (check_sizes(T, H, I, E, top_k, wtype) != MOE_OK) return 0;
+  return layout(static_cast<int64_t>(T) * top_k, H, I, E).total;
+}
+
+moe_status_t moe_route_topk(const float* logits, int T, int E, int top_k, int32_t* topk_ids, float* topk_w,
+                            int32_t* expert_counts, int32_t* expert_offsets, int32_t* sorted_token,
+                            int32_t* inv_pos, int32_t* active_experts, int32_t* num_active,
+                            moe_stream_t stream) {
+  const moe_status_t sz = check_sizes(T, 8, 8, E, top_k, MOE_W_BF16);
+  if (sz != MOE_OK) return sz;
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {logits, topk_ids, topk_w, expert_counts, expert_offsets,
+                        sorted_token, inv_pos, active_experts, num_active};
+  for (const void* p : ptrs)
+    if (!p || !aligned(p, 4)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_route(logits, T, E, top_k, topk_ids, topk_w, expert_counts, expert_offsets,
+                                       sorted_token, inv_pos, active_experts, num_active, nullptr, 0,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_gather(const uint16_t* x, int T, int H, int top_k, const int32_t* sorted_token, uint16_t* xg,
+                        moe_stream_t stream) {
+  if (T < 0 || H < 8 || H % 8 || top_k < 1) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * top_k > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !sorted_token || !xg || !aligned(x, 16) || !aligned(xg, 16) || !aligned(sorted_token, 4))
+    return MOE_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms < 1) return MOE_ERR_CUDA;
+  return cuda_status(
+      moe::launch_gather(x, T, H, top_k, sorted_token, xg, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets, const int32_t* active_experts,
+                            const int32_t* num_active, const void* W_gate, const void* W_up, const void* W_down,
+                            const float* s_gate, const float* s_up, const float* s_down, moe_wtype_t wtype, int H,
+                            int I, int E, int P, float* Y, void* workspace, size_t ws_bytes,
+                            moe_stream_t stream) {
+  if (P < 0) return MOE_ERR_INVALID_ARG;
+  const moe_status_t sz = check_sizes(P, H, I, E, 1, wtype);
+  if (sz != MOE_OK) return sz;
+  if (P == 0) return MOE_OK;
+  if (!xg || !expert_offsets || !active_experts || !num_active || !Y || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(xg, 16) || !aligned(Y, 16) || !aligned(workspace, kAlign) || !aligned(expert_offsets, 4) ||
+      !aligned(active_experts, 4) || !aligned(num_active, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(W_gate, W_up, W_down, s_gate, s_up, s_down, wtype)) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(P, H, I, E);
+  if (ws_bytes < L.ids) return MOE_ERR_WORKSPACE;  // ctrl + partials + h
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws + L.ctrl, 0, kCountersOffset + 4 * kMaxCtas, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return run_expert_ffn(xg, expert_offsets, active_experts, num_active, W_gate, W_up, W_down, s_gate, s_up, s_down,
+                        wtype, H, I, E, P, Y, ws, s);
+}
+
+moe_status_t moe_combine(const float* Y, const int32_t* inv_pos, const float* topk_w, int T, int top_k, int H,
+                         uint16_t* out, moe_stream_t stream) {
+  if (T < 0 || H < 8 || H % 8 || top_k < 1) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * top_k > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!Y || !inv_pos || !topk_w || !out || !aligned(Y, 16) || !aligned(out, 16) || !aligned(inv_pos, 4) ||
+      !aligned(topk_w, 4))
+    return MOE_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms < 1) return MOE_ERR_CUDA;
+  return cuda_status(
+      moe::launch_combine(Y, inv_pos, topk_w, T, top_k, H, out, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void* W_gate, const void* W_up,
+                             const void* W_down, const float* s_gate, const float* s_up, const float* s_down,
+                             moe_wtype_t wtype, int T, int H, int I, int E, int top_k, uint16_t* out,
+                             void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  const moe_status_t sz = check_sizes(T, H, I, E, top_k, wtype);
+  if (sz != MOE_OK) return sz;
+  if (T == 0) return MOE_OK;
+  if (!x || !logits || !out || !workspace || !aligned(x, 16) || !aligned(out, 16) || !aligned(logits, 4) ||
+      !aligned(workspace, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(W_gate, W_up, W_down, s_gate, s_up, s_down, wtype)) return MOE_ERR_INVALID_ARG;
+  const int P = T * top_k;
+  const Layout L = layout(P, H, I, E);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const int sms = sm_count();
+  if (sms < 1) return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  int32_t* ids = I32(L.ids);
+  float* w = reinterpret_cast<float*>(ws + L.w);
+  int32_t* offsets = I32(L.offsets);
+  int32_t* sorted_token = I32(L.sorted_token);
+  int32_t* inv_pos = I32(L.inv_pos);
+  int32_t* active = I32(L.active);
+  int32_t* num_active = I32(L.num_active);
+  uint16_t* xg = reinterpret_cast<uint16_t*>(ws + L.xg);
+  float* Y = reinterpret_cast<float*>(ws + L.Y);
+
+  cudaError_t e = moe::launch_route(logits, T, E, top_k, ids, w, I32(L.counts), offsets, sorted_token, inv_pos,
+                                    active, num_active, I32(L.ctrl), kZeroWords, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = moe::launch_gather(x, T, H, top_k, sorted_token, xg, sms, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const moe_status_t st = run_expert_ffn(xg, offsets, active, num_active, W_gate, W_up, W_down, s_gate, s_up,
+                                         s_down, wtype, H, I, E, P, Y, ws, s);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_combine(Y, inv_pos, w, T, top_k, H, out, sms, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,480 @@
+// Weight-streaming grouped expert kernels (gate+up with fused SiLU*up, and down).
+//
+// What they compute (HiNa-MoE, arXiv 2610.05123, §4.1 FFN equation):
+//   gate+up: h[p, i] = bf16( SiLU(sum_c xg[p,c] Wg[e,i,c]) * sum_c xg[p,c] Wu[e,i,c] )
+//   down:    Y[p, r] = sum_i h[p,i] Wd[e,r,i]
+// for every row p of an active expert e's token block, fp32 accumulation (§4.2.1).
+//
+// How (GB300 design; the pages' AMX micro-kernel is prior art, not the blueprint):
+//  * The weights are the large operand and are read exactly once per 64 routed
+//    tokens, in their general row-major layout (§2.2; "transform I, not W", §4.1).
+//    They sit on the 16-row side of the MMA ("swap AB"), the few tokens on the
+//    8-wide side, so even one token per expert runs on the tensor cores (§4.2.1:
+//    the matrix engine is used for every row count, no vector-unit fallback).
+//  * One persistent CTA per SM. A producer warp streams 128 weight rows x 128 bytes
+//    per stage with TMA (cp.async.bulk.tensor, evict-first L2 policy: the weights
+//    have no reuse, the streaming analogue of tileloadt1 in §4.2.2) together with the
+//    stage's token tiles, through a ring of mbarrier-guarded stages. Eight consumer
+//    warps run mma.sync m16n8k16 out of shared memory.
+//  * Gate and up rows of the same intermediate index are paired inside one MMA tile
+//    (tile rows 0-7 gate, 8-15 up), so the SiLU(g)*u epilogue is register-local
+//    (the second layout transformation of §4.1 happens in this epilogue: h is
+//    written token-major, the layout the down kernel's token tiles load). The down
+//    kernel writes Y token-major (the third transformation).
+//  * Work = (active expert, pass of <= 64 tokens, block of output rows) x reduction
+//    stages. The flattened stage range is split evenly over the CTAs (stream-K), so
+//    every SM streams the same number of weight bytes whatever the routing. A unit
+//    cut by a CTA boundary is finished by whichever of its CTAs arrives last
+//    (atomic counter, no waiting), which sums the fp32 partials in a fixed order,
+//    so results are deterministic.
+//  * Shared-memory tiles use the 128-byte TMA swizzle; the MMA's row and column
+//    order is permuted (sigma below) so that every 16-byte shared load of a warp is
+//    bank-conflict free.
+#pragma once
+
+#include "moe_device.cuh"
+
+namespace moe {
+namespace stream {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kRowsA = 128;                      // weight rows per stage
+constexpr int kRowBytes = 128;                   // bytes of each weight row per stage
+constexpr int kABytes = kRowsA * kRowBytes;      // 16 KB
+constexpr int kNMax = 64;                        // tokens per pass
+constexpr int kNT = kNMax / 8;                   // n8 tiles per pass
+constexpr int kTable = 256;                      // max experts (routing limit)
+constexpr int kMaxCtas = 256;                    // partial-slot capacity of the workspace
+constexpr int kPartialFloats = kNT * 4 * kConsumerThreads;  // one CTA slot: 32 regs x 256 threads
+
+template <bool kInt8>
+struct Geometry {
+  static constexpr int kK = kInt8 ? 128 : 64;            // reduction elements per stage
+  static constexpr int kBTileBytes = kInt8 ? 2048 : 1024;  // one n8 token tile per stage
+  static constexpr int kBBytes = kNT * kBTileBytes;
+  static constexpr int kSBytes = kInt8 ? 1024 : 0;       // 128 fp32 scales, padded
+  static constexpr int kStage = kABytes + kBBytes + kSBytes;  // multiple of 1024
+  static constexpr int kStages = kInt8 ? 6 : 8;
+  static constexpr int kBarBytes = 2 * kStages * 8;
+  static constexpr int kTableBytes = (4 * kTable + 16) * 4;
+  static constexpr int kSmem = kStages * kStage + kBarBytes + kTableBytes;
+  static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment for the 128B swizzle");
+};
+
+struct Args {
+  const int32_t* offsets;     // [E+1]
+  const int32_t* active;      // [E]
+  const int32_t* num_active;  // [1]
+  const float* s0;            // int8 scales: gate (gate+up) or down
+  const float* s1;            // int8 scales: up (gate+up only)
+  void* out;                  // h bf16 [P, I] (gate+up) or Y f32 [P, H] (down)
+  int64_t out_ld;
+  float* partials;            // [kMaxCtas][2][kPartialFloats]
+  int32_t* counters;          // [kMaxCtas], zero on entry, left zero on exit
+  int32_t* status;            // workspace status word
+  int rows;                   // output rows per expert: I (gate+up) or H (down)
+  int K;                      // reduction length: H (gate+up) or I (down)
+  int E;
+  int P;                      // rows of the token block
+};
+
+// MMA row/column g (0..7) -> row within an 8-row swizzle atom. Lanes g and g^1 share a
+// quarter-warp; sigma puts them in rows whose swizzle keys differ in bit 2, so their
+// 64-byte halves land on disjoint banks.
+__device__ __forceinline__ int sigma(int g) { return ((g & 1) << 2) | (g >> 1); }
+
+// Byte offset of 16-byte chunk `c` of row `r` in a tile of 128-byte rows (128B swizzle).
+__device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+struct Unit {
+  int e, tok0, ntok, rb;
+};
+
+template <bool kInt8, bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_stream_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                         const __grid_constant__ CUtensorMap tmB, const Args args) {
+  using G = Geometry<kInt8>;
+  constexpr int kRowsPerUnit = kGateUp ? 64 : 128;  // output rows per unit
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStage);
+  uint64_t* empty = full + G::kStages;
+  int* t_e = reinterpret_cast<int*>(empty + G::kStages);
+  int* t_tok0 = t_e + kTable;
+  int* t_ntok = t_tok0 + kTable;
+  int* t_pp = t_ntok + kTable;        // pass prefix, kTable + 1 entries
+  int* s_misc = t_pp + kTable + 4;    // 8 warp sums + flags
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < G::kStages; ++s) {
+      mbar_init(&full[s], kInt8 ? 33 : 1);  // producer expect_tx (+ 32 cp.async arrivals)
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    if (kGateUp) tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB);
+  }
+  // Everything below reads what earlier kernels wrote.
+  pdl_wait_predecessor();
+  pdl_allow_successor();
+
+  // ---- per-CTA schedule tables: active experts, their token blocks, pass prefix
+  int A = *args.num_active;
+  A = A < 0 ? 0 : (A > args.E ? args.E : A);
+  int passes = 0;
+  if (tid < kTable && tid < A) {
+    const int e = args.active[tid];
+    int tok0 = 0, ntok = 0;
+    if (e >= 0 && e < args.E) {
+      tok0 = args.offsets[e];
+      ntok = args.offsets[e + 1] - tok0;
+    }
+    // an entry that does not describe rows of the token block is skipped
+    if (tok0 < 0 || ntok < 0 || static_cast<int64_t>(tok0) + ntok > args.P) ntok = 0;
+    t_e[tid] = e;
+    t_tok0[tid] = tok0;
+    t_ntok[tid] = ntok;
+    passes = (ntok + kNMax - 1) / kNMax;
+  }
+  int incl = passes;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (warp < kConsumerWarps && lane == 31) s_misc[warp] = incl;
+  __syncthreads();
+  if (warp < kConsumerWarps) {
+    int add = 0;
+    for (int w = 0; w < warp; ++w) add += s_misc[w];
+    t_pp[tid + 1] = incl + add;
+  }
+  if (tid == 0) t_pp[0] = 0;
+  __syncthreads();
+
+  const int RB = (args.rows + kRowsPerUnit - 1) / kRowsPerUnit;
+  const int KI = (args.K + G::kK - 1) / G::kK;
+  const int64_t W = static_cast<int64_t>(t_pp[A]) * RB * KI;  // total stages
+  // Only min(grid, W) CTAs take part, so each owns at least one stage and every CTA
+  // between a unit's first and last owner holds a piece of it.
+  const int64_t NC = W < static_cast<int64_t>(gridDim.x) ? W : static_cast<int64_t>(gridDim.x);
+  const int64_t cta = blockIdx.x;
+  const int64_t it_beg = cta < NC ? cta * W / NC : 0;
+  const int64_t it_end = cta < NC ? (cta + 1) * W / NC : 0;
+
+  auto decode = [&](int64_t u) -> Unit {
+    const int q = static_cast<int>(u / RB);
+    Unit r;
+    r.rb = static_cast<int>(u % RB);
+    int lo = 0, hi = A - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (t_pp[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    const int np = q - t_pp[lo];
+    r.e = t_e[lo];
+    r.tok0 = t_tok0[lo] + np * kNMax;
+    const int left = t_ntok[lo] - np * kNMax;
+    r.ntok = left < kNMax ? left : kNMax;
+    return r;
+  };
+
+  if (warp == kConsumerWarps) {
+    // =========================== producer warp ===========================
+    const uint64_t policy = l2_policy_evict_first();
+    const int KG = args.K / 128;  // scale groups per row (int8)
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    int64_t cur_u = -1;
+    Unit un{};
+    for (int64_t it = it_beg; it < it_end; ++it) {
+      const int64_t u = it / KI;
+      const int kk = static_cast<int>(it - u * KI);
+      if (u != cur_u) {
+        un = decode(u);
+        cur_u = u;
+      }
+      const int nt8 = (un.ntok + 7) >> 3;
+      bool drained = true;
+      if (lane == 0) drained = mbar_wait(&empty[stage], phase ^ 1);
+      drained = __shfl_sync(0xffffffffu, drained, 0);
+      if (!drained) {
+        ok = false;
+        break;
+      }
+      uint8_t* st = smem + stage * G::kStage;
+      const int k0 = kk * G::kK;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[stage], kABytes + nt8 * G::kBTileBytes);
+        if (kGateUp) {
+          tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 64, un.e, policy);
+          tma_load_3d(st + 64 * kRowBytes, &tmA1, &full[stage], k0, un.rb * 64, un.e, policy);
+        } else {
+          tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 128, un.e, policy);
+        }
+        uint8_t* sb = st + kABytes;
+        for (int j = 0; j < nt8; ++j) {
+          tma_load_2d(sb + j * G::kBTileBytes, &tmB, &full[stage], k0, un.tok0 + 8 * j);
+          if (kInt8) tma_load_2d(sb + j * G::kBTileBytes + 1024, &tmB, &full[stage], k0 + 64, un.tok0 + 8 * j);
+        }
+      }
+      if (kInt8) {
+        float* sdst = reinterpret_cast<float*>(st + kABytes + G::kBBytes);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int row = lane + 32 * q4;
+          const float* sbase;
+          int grow;
+          if (kGateUp) {
+            sbase = row < 64 ? args.s0 : args.s1;
+            grow = un.rb * 64 + (row & 63);
+          } else {
+            sbase = args.s0;
+            grow = un.rb * 128 + row;
+          }
+          grow = grow < args.rows ? grow : args.rows - 1;  // rows past the end are zero-filled by TMA
+          cp_async_4(sdst + row, sbase + (static_cast<int64_t>(un.e) * args.rows + grow) * KG + kk);
+        }
+        cp_async_arrive_noinc(&full[stage]);
+      }
+      ++issued;
+      if (++stage == G::kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    // Never leave with copies in flight: wait for the last phase issued on each stage.
+    if (lane == 0) {
+      const int64_t n = issued < G::kStages ? issued : G::kStages;
+      int s = stage;
+      uint32_t ph = phase;
+      for (int64_t i = 0; i < n; ++i) {
+        if (--s < 0) {
+          s = G::kStages - 1;
+          ph ^= 1;
+        }
+        if (!mbar_wait(&full[s], ph)) {
+          atomicExch(args.status, kStatusDrainTimeout);
+          break;
+        }
+      }
+      if (!ok) atomicExch(args.status, kStatusWaitEmptyTimeout);
+    }
+    return;
+  }
+
+  // ============================ consumer warps ============================
+  const int cw = warp;           // 0..7
+  const int ctid = tid;          // 0..255
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const int sg = sigma(g);
+  // weight rows of this warp's MMA tile (rows g / g+8 of the m16 tile)
+  const int rowLo = kGateUp ? cw * 8 + sg : cw * 16 + sg;
+  const int rowHi = kGateUp ? 64 + cw * 8 + sg : cw * 16 + 8 + sg;
+  // token row of this lane's B fragment inside each n8 tile (MMA column g)
+  const int brow = kInt8 ? g : sg;
+
+  float acc[kNT][4];
+  float accg[kInt8 ? kNT : 1][4];
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  int64_t cur_u = -1;
+  Unit un{};
+  const int64_t first_unit = it_beg / KI;
+
+#pragma unroll 1
+  for (int64_t it = it_beg; it < it_end; ++it) {
+    const int64_t u = it / KI;
+    const int kk = static_cast<int>(it - u * KI);
+    if (u != cur_u) {
+      un = decode(u);
+      cur_u = u;
+#pragma unroll
+      for (int j = 0; j < kNT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
+    }
+    const int nt8 = (un.ntok + 7) >> 3;
+
+    if (ok && !mbar_wait(&full[stage], phase)) {
+      ok = false;
+      atomicExch(args.status, kStatusWaitFullTimeout);
+    }
+    if (ok) {
+      const uint8_t* st = smem + stage * G::kStage;
+      const uint8_t* sb = st + kABytes;
+      if constexpr (!kInt8) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
+          const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
+#pragma unroll
+          for (int j = 0; j < kNT; ++j) {
+            if (j < nt8) {
+              const uint4 bv = *reinterpret_cast<const uint4*>(sb + j * G::kBTileBytes + swz(brow, 4 * b + t));
+              mma_16816_bf16(acc[j], alo.x, ahi.x, alo.y, ahi.y, bv.x, bv.y);
+              mma_16816_bf16(acc[j], alo.z, ahi.z, alo.w, ahi.w, bv.z, bv.w);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kNT; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) accg[j][q] = 0.0f;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          // 16 int8 weights per row: reduction index 64b + 16t + [0, 16)
+          const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
+          const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
+          const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
+          const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+          uint32_t a_lo_l[4], a_lo_h[4], a_hi_l[4], a_hi_h[4];
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            int8x4_to_bf16x2x2(aw_lo[s], a_lo_l[s], a_lo_h[s]);
+            int8x4_to_bf16x2x2(aw_hi[s], a_hi_l[s], a_hi_h[s]);
+          }
+#pragma unroll
+          for (int j = 0; j < kNT; ++j) {
+            if (j < nt8) {
+              // the same 16 reduction indices of the lane's token row: 32 bytes = chunks 2t, 2t+1
+              const uint8_t* tb = sb + j * G::kBTileBytes + b * 1024;
+              const uint4 b0 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t));
+              const uint4 b1 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t + 1));
+              mma_16816_bf16(accg[j], a_lo_l[0], a_hi_l[0], a_lo_h[0], a_hi_h[0], b0.x, b0.y);
+              mma_16816_bf16(accg[j], a_lo_l[1], a_hi_l[1], a_lo_h[1], a_hi_h[1], b0.z, b0.w);
+              mma_16816_bf16(accg[j], a_lo_l[2], a_hi_l[2], a_lo_h[2], a_hi_h[2], b1.x, b1.y);
+              mma_16816_bf16(accg[j], a_lo_l[3], a_hi_l[3], a_lo_h[3], a_hi_h[3], b1.z, b1.w);
+            }
+          }
+        }
+        const float* ss = reinterpret_cast<const float*>(sb + G::kBBytes);
+        const float slo = ss[rowLo];
+        const float shi = ss[rowHi];
+#pragma unroll
+        for (int j = 0; j < kNT; ++j) {
+          acc[j][0] = fmaf(slo, accg[j][0], acc[j][0]);
+          acc[j][1] = fmaf(slo, accg[j][1], acc[j][1]);
+          acc[j][2] = fmaf(shi, accg[j][2], acc[j][2]);
+          acc[j][3] = fmaf(shi, accg[j][3], acc[j][3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == G::kStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+
+    if (kk != KI - 1 && it != it_end - 1) continue;
+
+    // ---------------- end of this CTA's piece of unit u ----------------
+    const int64_t ub = u * KI;
+    const int64_t ue = ub + KI;
+    bool finish = true;
+    if (ub < it_beg || ue > it_end) {
+      // unit split across CTAs: publish the fp32 partial, last arriver reduces
+      auto cta_of = [&](int64_t i) -> int64_t { return ((i + 1) * NC - 1) / W; };
+      const int64_t c_first = cta_of(ub);
+      const int64_t c_last = cta_of(ue - 1);
+      const int slot = (u == first_unit) ? 0 : 1;
+      float* mine = args.partials + (cta * 2 + slot) * static_cast<int64_t>(kPartialFloats) + ctid;
+#pragma unroll
+      for (int j = 0; j < kNT; ++j)
+        if (j < nt8)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mine[(j * 4 + q) * kConsumerThreads] = acc[j][q];
+      __threadfence();
+      named_bar_sync(1, kConsumerThreads);
+      if (ctid == 0) {
+        const int old = atomicAdd(&args.counters[c_first], 1);
+        const int last = (old == static_cast<int>(c_last - c_first));
+        if (last) args.counters[c_first] = 0;  // leave the counter clean for the next launch
+        s_misc[8] = last;
+      }
+      named_bar_sync(1, kConsumerThreads);
+      finish = s_misc[8] != 0;
+      if (finish) {
+        __threadfence();
+#pragma unroll
+        for (int j = 0; j < kNT; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
+        for (int64_t c = c_first; c <= c_last; ++c) {
+          const int64_t c_first_unit = (c * W / NC) / KI;
+          const int cslot = (u == c_first_unit) ? 0 : 1;
+          const float* src = args.partials + (c * 2 + cslot) * static_cast<int64_t>(kPartialFloats) + ctid;
+#pragma unroll
+          for (int j = 0; j < kNT; ++j)
+            if (j < nt8)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[j][q] += __ldcg(src + (j * 4 + q) * kConsumerThreads);
+        }
+      }
+      named_bar_sync(1, kConsumerThreads);  // s_misc[8] is reused by the next piece
+    }
+    if (!finish) continue;
+
+    // ---------------- epilogue ----------------
+    if constexpr (kGateUp) {
+      const int i = un.rb * 64 + cw * 8 + sg;  // intermediate index of rows g (gate) / g+8 (up)
+      if (i < args.rows) {
+        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+        for (int j = 0; j < kNT; ++j) {
+          if (j < nt8) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int col = 2 * t + c;
+              const int n = 8 * j + (kInt8 ? col : sigma(col));
+              if (n < un.ntok) {
+                const float gv = acc[j][c];
+                const float uv = acc[j][2 + c];
+                const float silu = gv / (1.0f + expf(-gv));
+                h[static_cast<int64_t>(un.tok0 + n) * args.out_ld + i] = __float2bfloat16_rn(silu * uv);
+              }
+            }
+          }
+        }
+      }
+    } else {
+      const int r_lo = un.rb * 128 + cw * 16 + sg;
+      const int r_hi = r_lo + 8;
+      float* y = static_cast<float*>(args.out);
+#pragma unroll
+      for (int j = 0; j < kNT; ++j) {
+        if (j < nt8) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int col = 2 * t + c;
+            const int n = 8 * j + (kInt8 ? col : sigma(col));
+            if (n < un.ntok) {
+              float* yr = y + static_cast<int64_t>(un.tok0 + n) * args.out_ld;
+              if (r_lo < args.rows) yr[r_lo] = acc[j][c];
+              if (r_hi < args.rows) yr[r_hi] = acc[j][2 + c];
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace stream
+}  // namespace moe

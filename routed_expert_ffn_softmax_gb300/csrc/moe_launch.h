@@ -1,0 +1,70 @@
+// Host-side launch helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace moe {
+
+// Launch with programmatic dependent launch enabled: the kernel may begin while its
+// predecessor in the stream finishes; every kernel of this library waits for its
+// predecessor (griddepcontrol.wait) before touching data the predecessor wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
+                         int32_t* offsets, int32_t* sorted_token, int32_t* inv_pos, int32_t* active,
+                         int32_t* num_active, int32_t* zero_words, int n_zero, cudaStream_t stream);
+
+cudaError_t launch_gather(const uint16_t* x, int T, int H, int k, const int32_t* sorted_token, uint16_t* xg,
+                          int num_sms, cudaStream_t stream);
+
+cudaError_t launch_combine(const float* Y, const int32_t* inv_pos, const float* w, int T, int k, int H,
+                           uint16_t* out, int num_sms, cudaStream_t stream);
+
+// Grouped expert FFN (gate+up then down) over an expert-sorted token block.
+struct ExpertFfnPlan {
+  const uint16_t* xg;  // [P, H]
+  const int32_t* offsets;
+  const int32_t* active;
+  const int32_t* num_active;
+  const void* W_gate;
+  const void* W_up;
+  const void* W_down;
+  const float* s_gate;
+  const float* s_up;
+  const float* s_down;
+  bool int8;
+  int H, I, E, P;
+  uint16_t* h;        // [P, I] scratch
+  float* Y;           // [P, H]
+  float* partials;    // stream-K partial slots
+  int32_t* counters;  // zeroed, kMaxCtas entries
+  int32_t* status;
+  int num_ctas;
+};
+cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream);
+
+// Resolves cuTensorMapEncodeTiled through the runtime (no link-time libcuda).
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                       CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                       CUtensorMapFloatOOBfill);
+TensorMapEncodeFn tensor_map_encoder();
+
+}  // namespace moe

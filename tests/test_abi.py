@@ -1,0 +1,132 @@
+"""The C-ABI library builds, loads and exports what include/moe.h declares; host-side
+argument checks reject bad calls before any CUDA work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from routed_expert_ffn_softmax_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+BF16, INT8 = 0, 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = moe_build.build()
+    L = ctypes.CDLL(path)
+    P, i, z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.moe_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.moe_workspace_size.restype = z
+    L.moe_status_string.argtypes = [i]
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_ffn_forward.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, P, z, P]
+    L.moe_expert_ffn.argtypes = [P, P, P, P, P, P, P, P, P, P, i, i, i, i, i, P, P, z, P]
+    L.moe_route_topk.argtypes = [P, i, i, i, P, P, P, P, P, P, P, P, P]
+    L.moe_gather.argtypes = [P, i, i, i, P, P, P]
+    L.moe_combine.argtypes = [P, P, P, i, i, i, P, P]
+    return L
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted([
+        "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
+        "moe_expert_ffn", "moe_combine", "moe_ffn_forward"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exports_are_c_symbols():
+    out = os.popen(f"nm -D --defined-only {moe_build.LIB}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.moe_status_string(code).decode()
+        assert s.startswith("MOE_")
+    assert b"unknown" in lib.moe_status_string(99)
+
+
+def test_workspace_size(lib):
+    ws = lib.moe_workspace_size
+    n1 = ws(1, 4096, 14336, 8, 2, BF16)
+    n64 = ws(64, 4096, 14336, 8, 2, BF16)
+    assert 0 < n1 < n64
+    assert n1 % 256 == 0
+    # grows with the token block: xg (2 B) + Y (4 B) + h (2 B/I) per assignment
+    assert n64 - n1 >= 63 * 2 * (2 * 4096 + 4 * 4096 + 2 * 14336)
+    assert ws(0, 256, 512, 8, 2, BF16) > 0
+    assert ws(-1, 256, 512, 8, 2, BF16) == 0
+    assert ws(1, 256, 512, 8, 9, BF16) == 0          # top_k > E
+    assert ws(1, 256, 512, 300, 2, BF16) == 0        # E > 256
+    assert ws(1, 260, 512, 8, 2, BF16) == 0          # H % 8
+    assert ws(1, 4096, 1536, 128, 8, INT8) > 0
+    assert ws(1, 4096 + 64, 1536, 128, 8, INT8) == 0  # int8 needs H % 128 == 0
+    assert ws(1, 256, 512, 8, 2, 7) == 0             # unknown weight type
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced (the calls below fail first)
+
+
+def fwd(lib, T=1, H=256, I=512, E=8, k=2, wtype=BF16, x=FAKE, logits=FAKE, Wg=FAKE, Wu=FAKE, Wd=FAKE,
+        sg=None, su=None, sd=None, out=FAKE, ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.moe_workspace_size(max(T, 0), H, I, E, k, wtype) if T >= 0 else 0
+    return lib.moe_ffn_forward(x, logits, Wg, Wu, Wd, sg, su, sd, wtype, T, H, I, E, k, out, ws, ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments_before_launch(lib):
+    assert fwd(lib, T=-1) == INVALID
+    assert fwd(lib, k=0) == INVALID
+    assert fwd(lib, k=9) == INVALID
+    assert fwd(lib, E=300, k=2) == UNSUPPORTED
+    assert fwd(lib, H=260) == INVALID
+    assert fwd(lib, I=0) == INVALID
+    assert fwd(lib, wtype=5) == INVALID
+    assert fwd(lib, x=None) == INVALID
+    assert fwd(lib, Wd=None) == INVALID
+    assert fwd(lib, x=FAKE + 8) == INVALID                 # x must be 16-byte aligned
+    assert fwd(lib, ws=FAKE + 16) == INVALID               # workspace must be 256-byte aligned
+    assert fwd(lib, ws_bytes=1024) == WORKSPACE
+    # INT8: scales are required and dimensions must be multiples of 128
+    assert fwd(lib, H=4096, I=1536, E=128, k=8, wtype=INT8) == INVALID
+    assert fwd(lib, H=4096 + 8, I=1536, E=128, k=8, wtype=INT8, sg=FAKE, su=FAKE, sd=FAKE) == INVALID
+    assert fwd(lib, H=4096, I=1536, E=128, k=8, wtype=INT8, sg=FAKE, su=FAKE, sd=FAKE, ws_bytes=16) == WORKSPACE
+    # T = 0 is a no-op that touches nothing
+    assert fwd(lib, T=0, x=None, logits=None, out=None, ws=None) in (OK, INVALID)
+    assert fwd(lib, T=0) == OK
+
+
+def test_other_entry_points_reject_bad_arguments(lib):
+    F = FAKE
+    assert lib.moe_route_topk(F, -1, 8, 2, F, F, F, F, F, F, F, F, None) == INVALID
+    assert lib.moe_route_topk(F, 4, 8, 9, F, F, F, F, F, F, F, F, None) == INVALID
+    assert lib.moe_route_topk(F, 4, 512, 2, F, F, F, F, F, F, F, F, None) == UNSUPPORTED
+    assert lib.moe_route_topk(None, 4, 8, 2, F, F, F, F, F, F, F, F, None) == INVALID
+    assert lib.moe_route_topk(F, 0, 8, 2, F, F, F, F, F, F, F, F, None) == OK
+    assert lib.moe_gather(F, 4, 100, 2, F, F, None) == INVALID      # H % 8
+    assert lib.moe_gather(F + 4, 4, 128, 2, F, F, None) == INVALID  # alignment
+    assert lib.moe_gather(F, 0, 128, 2, F, F, None) == OK
+    assert lib.moe_combine(F, F, F, 4, 0, 128, F, None) == INVALID
+    assert lib.moe_combine(F, F, None, 4, 2, 128, F, None) == INVALID
+    assert lib.moe_combine(F, F, F, 0, 2, 128, F, None) == OK
+    ws_need = lib.moe_workspace_size(4, 256, 512, 8, 2, BF16)
+    assert lib.moe_expert_ffn(F, F, F, F, F, F, F, None, None, None, BF16, 256, 512, 8, 8, F, F, 64, None) == WORKSPACE
+    assert lib.moe_expert_ffn(F, F, F, F, F, F, F, None, None, None, BF16, 256, 512, 8, -1, F, F, ws_need, None) == INVALID
+    assert lib.moe_expert_ffn(F, F, F, F, F, F, F, None, None, None, BF16, 256, 512, 8, 0, F, F, ws_need, None) == OK
+    assert lib.moe_expert_ffn(F, F, F, F, F, F, F, None, None, None, INT8, 256, 512, 8, 8, F, F, ws_need, None) == INVALID
