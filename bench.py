@@ -1,0 +1,496 @@
+"""Benchmark of the routed-expert FFN decode step on GB300.
+
+One step = one pass of the whole path (route -> gather -> gate+up -> down -> combine)
+through the C ABI over one decode batch of synthetic tokens. Default workload: the
+Mixtral-8x7B-shaped expert layer (H=4096, I=14336, E=8, top-2, BF16 weights) at
+T=16 tokens (about 4 tokens per expert). The metric is the weight-stream bandwidth:
+bytes of the active experts' weights (each read once) per second; tokens/s is
+reported beside it.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+        [--config NAME] [--T T] [--sweep] [--no-cpu-baseline]
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path is not sharded); value = all ranks' bytes / the slowest rank's time.
+`--impl reference` times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_workloads as mw  # noqa: E402
+
+METRIC = "expert-FFN decode weight-stream HBM GB/s (% of peak) and tokens/s, 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS_PER_STEP = 6  # route_topk, route_scan, gather, gate+up, down, combine
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; a recorded DRAM-traffic figure is used only while it matches."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "routed_expert_ffn_softmax_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the current kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[workload]
+        if e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+class Workload:
+    """Device-resident weights (several distinct layer copies, so consecutive steps do not
+    re-read the previous step's experts from L2) and one decode batch per copy. The number
+    of active experts per batch (which sets the weight bytes a step must stream) is read
+    from the library's own routing kernel."""
+
+    def __init__(self, cfg: mw.MoEConfig, T: int, copies: int, device, moe, seed: int = 0):
+        self.cfg, self.T, self.device = cfg, T, device
+        self.layers, self.tokens = [], []
+        for c in range(copies):
+            self.layers.append(mw.make_layer(cfg, seed=seed + 1000 * c, device=device))
+            self.tokens.append(mw.make_tokens(cfg, T, seed=seed + 1000 * c, device=device))
+        self.active = []
+        k = cfg.top_k
+        for x, lg in self.tokens:
+            i32 = dict(dtype=torch.int32, device=device)
+            outs = [torch.empty(T, k, **i32), torch.empty(T, k, device=device), torch.empty(cfg.E, **i32),
+                    torch.empty(cfg.E + 1, **i32), torch.empty(T * k, **i32), torch.empty(T, k, **i32),
+                    torch.empty(cfg.E, **i32), torch.empty(1, **i32)]
+            moe.moe_route_topk(lg, k, *outs)
+            self.active.append(int(outs[-1].item()))
+        self.wt = 1 if cfg.wtype == "int8" else 0
+
+    def weight_bytes(self, c: int) -> int:
+        return self.active[c] * self.cfg.weight_bytes_per_expert
+
+    def mean_weight_bytes(self) -> float:
+        return sum(self.weight_bytes(c) for c in range(len(self.layers))) / len(self.layers)
+
+    def act_bytes(self) -> int:
+        """Token-side algorithmic bytes of the expert kernels: xg read, h write + read, Y write."""
+        cfg, P = self.cfg, self.T * self.cfg.top_k
+        return P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 4
+
+
+# ------------------------------------------------------------------ our implementation
+def bench_ours(args, cfg, T):
+    import routed_expert_ffn_softmax_gb300 as moe
+    from routed_expert_ffn_softmax_gb300 import build as moe_build
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        moe_build.build()
+    if ws_n > 1:
+        dist.barrier()
+    moe.load()
+
+    copies = args.copies
+    wl = Workload(cfg, T, copies, dev, moe)
+    stream = torch.cuda.current_stream()
+    ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wl.wt, dev)
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+
+    def step(c):
+        L = wl.layers[c]
+        x, lg = wl.tokens[c]
+        moe.moe_ffn_forward(x, lg, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
+                            cfg.top_k, out, ws, stream)
+
+    def barrier_sync():
+        torch.cuda.synchronize()
+        if ws_n > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        for i in range(args.warmup):
+            step(i % copies)
+        barrier_sync()
+        if moe.workspace_status(ws) != 0:
+            raise RuntimeError("a kernel reported a timed-out wait during warm-up")
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        ev0.record(stream)
+        for i in range(args.steps):
+            evs[i].record(stream)
+            step(i % copies)
+        evs[-1].record(stream)
+        ev1.record(stream)
+        barrier_sync()
+    clocks = clk.summary()
+    total_ms = ev0.elapsed_time(ev1)
+    per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    if moe.workspace_status(ws) != 0:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    bytes_timed = sum(wl.weight_bytes(i % copies) for i in range(args.steps))
+    if ws_n > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = ws_n * bytes_timed / (total_ms * 1e-3) / 1e9
+    tokens_s = ws_n * T * args.steps / (total_ms * 1e-3)
+
+    # ---- dominant kernels: the expert FFN pair (gate+up, down), timed alone with events
+    r = {n: torch.empty(s, dtype=dt, device=dev) for n, s, dt in (
+        ("ids", (T, cfg.top_k), torch.int32), ("w", (T, cfg.top_k), torch.float32), ("counts", (cfg.E,), torch.int32),
+        ("offsets", (cfg.E + 1,), torch.int32), ("st", (T * cfg.top_k,), torch.int32),
+        ("inv", (T, cfg.top_k), torch.int32), ("act", (cfg.E,), torch.int32), ("na", (1,), torch.int32))}
+    xg = torch.empty(T * cfg.top_k, cfg.H, dtype=torch.bfloat16, device=dev)
+    Y = torch.empty(T * cfg.top_k, cfg.H, dtype=torch.float32, device=dev)
+    ffn_ev, ffn_bytes = [], []
+    n_ffn = max(min(args.steps, 200), 20)
+    for i in range(n_ffn + 3):
+        c = i % copies
+        L = wl.layers[c]
+        x, lg = wl.tokens[c]
+        moe.moe_route_topk(lg, cfg.top_k, r["ids"], r["w"], r["counts"], r["offsets"], r["st"], r["inv"], r["act"],
+                           r["na"], stream)
+        moe.moe_gather(x, cfg.top_k, r["st"], xg, stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        moe.moe_expert_ffn(xg, r["offsets"], r["act"], r["na"], L["W_gate"], L["W_up"], L["W_down"], L["s_gate"],
+                           L["s_up"], L["s_down"], Y, ws, stream)
+        b.record(stream)
+        moe.moe_combine(Y, r["inv"], r["w"], cfg.top_k, out, stream)
+        if i >= 3:
+            ffn_ev.append((a, b))
+            ffn_bytes.append(wl.weight_bytes(c) + wl.act_bytes())
+    torch.cuda.synchronize()
+    ffn_t = [a.elapsed_time(b) for a, b in ffn_ev]
+    ffn_avg_ms = sum(ffn_t) / len(ffn_t)
+    ffn_achieved = (sum(ffn_bytes) / len(ffn_bytes)) / (ffn_avg_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    workload_name = f"{cfg.name}_T{T}"
+    traffic = recorded_traffic(workload_name)
+
+    # ---- end to end through the C ABI: host inputs in, host result out, every step
+    x_h = [t[0].cpu().pin_memory() for t in wl.tokens]
+    lg_h = [t[1].cpu().pin_memory() for t in wl.tokens]
+    out_h = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(wl.tokens[0][0])
+    lg_d = torch.empty_like(wl.tokens[0][1])
+
+    def e2e_step(c):
+        L = wl.layers[c]
+        x_d.copy_(x_h[c], non_blocking=True)
+        lg_d.copy_(lg_h[c], non_blocking=True)
+        moe.moe_ffn_forward(x_d, lg_d, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
+                            cfg.top_k, out, ws, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i % copies)
+    barrier_sync()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(args.steps):
+        e2e_step(i % copies)
+    b.record(stream)
+    barrier_sync()
+    e2e_ms = a.elapsed_time(b)
+    if ws_n > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = ws_n * bytes_timed / (e2e_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "ms_per_step_median": round(statistics.median(per_step), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.wtype == "bf16" else "int8 weights, bf16 activations",
+        "data": "synthetic (seeded N(0,1) tokens and logits, N(0,0.02) weights)",
+        "pct_of_peak": round(100.0 * value / ws_n / peak, 2),
+        "tokens_per_s": round(tokens_s, 1),
+        "config": {
+            "workload": workload_name, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
+            "weights": cfg.wtype, "T": T, "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
+            "active_experts_mean": round(sum(wl.active) / len(wl.active), 2),
+            "tokens_per_expert_mean": round(T * cfg.top_k * len(wl.active) / sum(wl.active), 2),
+            "weight_bytes_per_step_mean": int(wl.mean_weight_bytes()),
+            "l2": f"inputs larger than L2: each step streams >= "
+                  f"{min(wl.weight_bytes(c) for c in range(copies)) / 1e6:.0f} MB of expert weights, "
+                  f"rotating over {copies} distinct weight copies",
+        },
+        "roofline": {
+            "kernel": "expert FFN stream kernels (gate+up with SiLU*up, then down), timed together",
+            "bound": "hbm",
+            "achieved": round(ffn_achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
+            "unit": "GB/s",
+            "frac": round(ffn_achieved / peak, 4),
+            "traffic": traffic,
+            "avg_launch_ms": round(ffn_avg_ms, 5),
+            "algorithmic_bytes_per_launch": int(sum(ffn_bytes) / len(ffn_bytes)),
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 2},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+    }
+    if args.sweep and rank == 0:
+        result["sweep"] = sweep(cfg, dev, moe, copies)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, T, wl, budget_s=args.cpu_budget)
+    if ws_n > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def sweep(cfg, dev, moe, copies):
+    """GB/s and tokens/s at every T of the workload (same method, fewer steps)."""
+    rows = []
+    for T in cfg.T:
+        wl = Workload(cfg, T, copies, dev, moe)
+        ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wl.wt, dev)
+        out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+        s = torch.cuda.current_stream()
+
+        def step(c):
+            L = wl.layers[c]
+            x, lg = wl.tokens[c]
+            moe.moe_ffn_forward(x, lg, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
+                                cfg.top_k, out, ws, s)
+        for i in range(10):
+            step(i % copies)
+        torch.cuda.synchronize()
+        n = 100
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for i in range(n):
+            step(i % copies)
+        b.record(s)
+        torch.cuda.synchronize()
+        if moe.workspace_status(ws) != 0:
+            raise RuntimeError("a kernel reported a timed-out wait")
+        ms = a.elapsed_time(b) / n
+        wb = sum(wl.weight_bytes(i % copies) for i in range(n)) / n
+        rows.append({"T": T, "active_experts": round(sum(wl.active) / len(wl.active), 2),
+                     "us_per_step": round(ms * 1e3, 2), "GB_s": round(wb / (ms * 1e-3) / 1e9, 1),
+                     "tokens_per_s": round(T / (ms * 1e-3), 1)})
+        del wl, ws
+        torch.cuda.empty_cache()
+    return rows
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline leg)
+def oracle_rate(cfg, T, budget_s, layer_cpu, x, lg):
+    """Run the oracle token by token over the batch (cycling) until the time budget is spent,
+    at least one token; return (weight GB/s for the whole batch, tokens/s, tokens run, seconds)."""
+    import oracle
+    ro = oracle.route(lg, cfg.top_k)
+    full_bytes = ro["num_active"] * cfg.weight_bytes_per_expert
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        t = n % T
+        oracle.forward(x[t:t + 1], lg[t:t + 1], layer_cpu["W_gate"], layer_cpu["W_up"], layer_cpu["W_down"],
+                       layer_cpu["s_gate"], layer_cpu["s_up"], layer_cpu["s_down"], wtype=cfg.wtype, top_k=cfg.top_k)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    per_token = dt / n
+    # the oracle's cost is linear in tokens: the whole batch takes T * per_token
+    return full_bytes / (T * per_token) / 1e9, 1.0 / per_token, n, dt
+
+
+def cores_used():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    omp = os.environ.get("OMP_NUM_THREADS")
+    return int(omp) if omp and omp.isdigit() else n
+
+
+def cpu_baseline(cfg, T, wl, budget_s):
+    layer = {n: (v.cpu() if v is not None else None) for n, v in wl.layers[0].items()}
+    x, lg = (t.cpu() for t in wl.tokens[0])
+    gbs, tok_s, n, dt = oracle_rate(cfg, T, budget_s, layer, x, lg)
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+            "tokens_per_s": round(tok_s, 3),
+            "sample": f"{n} token evaluations cycling over the {T} tokens of the same batch ({dt:.1f} s of CPU "
+                      f"time); the oracle's time is linear in tokens, so GB/s = active-expert weight bytes of "
+                      f"the batch / ({T} x time per token)"}
+
+
+def bench_reference(args, cfg, T):
+    """The CPU oracle on the host cores, same metric and config (rank 0 only)."""
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    x, lg = mw.make_tokens(cfg, T, device="cpu")
+    ro = oracle.route(lg, cfg.top_k)
+    layer = mw.make_layer(cfg, device="cpu")
+    nsteps = args.steps + args.warmup
+    per_step_budget = max(0.02, args.cpu_budget * 4 / nsteps)
+    vals, times = [], []
+    for i in range(nsteps):
+        gbs, tok_s, n, dt = oracle_rate(cfg, T, per_step_budget, layer, x, lg)
+        if i >= args.warmup:
+            vals.append(gbs)
+            times.append(T / tok_s)
+    value = statistics.mean(vals)
+    ms_step = 1e3 * statistics.mean(times)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "GB/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 accumulate, bf16 inputs (CPU oracle)",
+        "data": "synthetic (seeded N(0,1) tokens and logits, N(0,0.02) weights)",
+        "tokens_per_s": round(T / (ms_step * 1e-3), 3),
+        "config": {"workload": f"{cfg.name}_T{T}", "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
+                   "weights": cfg.wtype, "T": T, "active_experts": ro["num_active"]},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": f"each step runs the oracle token by token over the T={T} batch for about "
+                                   f"{per_step_budget:.2f} s (at least one token) and scales to the whole batch "
+                                   f"(time is linear in tokens)"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="mixtral8x7b", choices=sorted(mw.CONFIGS))
+    ap.add_argument("--T", type=int, default=16)
+    ap.add_argument("--copies", type=int, default=3, help="distinct weight copies rotated across steps")
+    ap.add_argument("--sweep", action="store_true", help="also measure every T of the workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = mw.CONFIGS[args.config]
+    if args.impl == "reference":
+        res = bench_reference(args, cfg, args.T)
+    else:
+        res = bench_ours(args, cfg, args.T)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

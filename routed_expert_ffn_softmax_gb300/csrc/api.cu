@@ -5,7 +5,7 @@
 #include <atomic>
 #include <cstdint>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "expert_stream.cuh"
 #include "moe_launch.h"
 

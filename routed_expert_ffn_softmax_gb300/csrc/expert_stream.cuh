@@ -47,6 +47,7 @@ constexpr int kNMax = 64;                        // tokens per pass
 constexpr int kNT = kNMax / 8;                   // n8 tiles per pass
 constexpr int kTable = 256;                      // max experts (routing limit)
 constexpr int kMaxCtas = 256;                    // partial-slot capacity of the workspace
+constexpr int kIssueGroup = 4;                   // reduction stages issued back to back per row block
 constexpr int kPartialFloats = kNT * 4 * kConsumerThreads;  // one CTA slot: 32 regs x 256 threads
 
 template <bool kInt8>
@@ -61,6 +62,7 @@ struct Geometry {
   static constexpr int kTableBytes = (4 * kTable + 16) * 4;
   static constexpr int kSmem = kStages * kStage + kBarBytes + kTableBytes;
   static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment for the 128B swizzle");
+  static_assert(kIssueGroup <= kStages, "an issue group must fit in the ring");
 };
 
 struct Args {
@@ -91,6 +93,84 @@ __device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7
 struct Unit {
   int e, tok0, ntok, rb;
 };
+
+// One stage of MMAs for a warp: its m16 weight tile (rows rowLo / rowHi) against NT n8 token
+// tiles. NT is a compile-time constant so no instruction is issued for unused token tiles.
+template <bool kInt8, int NT>
+__device__ __forceinline__ void stage_mma(float (&acc)[kNT][4], const uint8_t* st, int rowLo, int rowHi,
+                                          int brow, int t) {
+  using G = Geometry<kInt8>;
+  const uint8_t* sb = st + kABytes;
+  if constexpr (!kInt8) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
+      const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const uint4 bv = *reinterpret_cast<const uint4*>(sb + j * G::kBTileBytes + swz(brow, 4 * b + t));
+        mma_16816_bf16(acc[j], alo.x, ahi.x, alo.y, ahi.y, bv.x, bv.y);
+        mma_16816_bf16(acc[j], alo.z, ahi.z, alo.w, ahi.w, bv.z, bv.w);
+      }
+    }
+  } else {
+    float accg[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) accg[j][q] = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      // 16 int8 weights per row: reduction index 64b + 16t + [0, 16)
+      const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
+      const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
+      const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
+      const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+      uint32_t a_lo_l[4], a_lo_h[4], a_hi_l[4], a_hi_h[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        int8x4_to_bf16x2x2(aw_lo[s], a_lo_l[s], a_lo_h[s]);
+        int8x4_to_bf16x2x2(aw_hi[s], a_hi_l[s], a_hi_h[s]);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        // the same 16 reduction indices of the lane's token row: 32 bytes = chunks 2t, 2t+1
+        const uint8_t* tb = sb + j * G::kBTileBytes + b * 1024;
+        const uint4 b0 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t));
+        const uint4 b1 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t + 1));
+        mma_16816_bf16(accg[j], a_lo_l[0], a_hi_l[0], a_lo_h[0], a_hi_h[0], b0.x, b0.y);
+        mma_16816_bf16(accg[j], a_lo_l[1], a_hi_l[1], a_lo_h[1], a_hi_h[1], b0.z, b0.w);
+        mma_16816_bf16(accg[j], a_lo_l[2], a_hi_l[2], a_lo_h[2], a_hi_h[2], b1.x, b1.y);
+        mma_16816_bf16(accg[j], a_lo_l[3], a_hi_l[3], a_lo_h[3], a_hi_h[3], b1.z, b1.w);
+      }
+    }
+    const float* ss = reinterpret_cast<const float*>(sb + G::kBBytes);
+    const float slo = ss[rowLo];
+    const float shi = ss[rowHi];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      acc[j][0] = fmaf(slo, accg[j][0], acc[j][0]);
+      acc[j][1] = fmaf(slo, accg[j][1], acc[j][1]);
+      acc[j][2] = fmaf(shi, accg[j][2], acc[j][2]);
+      acc[j][3] = fmaf(shi, accg[j][3], acc[j][3]);
+    }
+  }
+}
+
+template <bool kInt8>
+__device__ __forceinline__ void stage_mma_dispatch(int nt8, float (&acc)[kNT][4], const uint8_t* st, int rowLo,
+                                                   int rowHi, int brow, int t) {
+  switch (nt8) {
+    case 1: stage_mma<kInt8, 1>(acc, st, rowLo, rowHi, brow, t); break;
+    case 2: stage_mma<kInt8, 2>(acc, st, rowLo, rowHi, brow, t); break;
+    case 3: stage_mma<kInt8, 3>(acc, st, rowLo, rowHi, brow, t); break;
+    case 4: stage_mma<kInt8, 4>(acc, st, rowLo, rowHi, brow, t); break;
+    case 5: stage_mma<kInt8, 5>(acc, st, rowLo, rowHi, brow, t); break;
+    case 6: stage_mma<kInt8, 6>(acc, st, rowLo, rowHi, brow, t); break;
+    case 7: stage_mma<kInt8, 7>(acc, st, rowLo, rowHi, brow, t); break;
+    default: stage_mma<kInt8, 8>(acc, st, rowLo, rowHi, brow, t); break;
+  }
+}
 
 template <bool kInt8, bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -197,62 +277,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    int64_t cur_u = -1;
-    Unit un{};
-    for (int64_t it = it_beg; it < it_end; ++it) {
-      const int64_t u = it / KI;
-      const int kk = static_cast<int>(it - u * KI);
-      if (u != cur_u) {
-        un = decode(u);
-        cur_u = u;
-      }
+    int64_t u = it_beg / KI;
+    int kk0 = static_cast<int>(it_beg - u * KI);
+    Unit un = it_beg < it_end ? decode(u) : Unit{};
+    for (int64_t it = it_beg; it < it_end && ok;) {
       const int nt8 = (un.ntok + 7) >> 3;
+      // Issue up to kIssueGroup consecutive reduction stages of the same rows back to back,
+      // so each weight row is requested as one longer contiguous run.
+      int64_t n = KI - kk0;
+      if (n > it_end - it) n = it_end - it;
+      if (n > kIssueGroup) n = kIssueGroup;
       bool drained = true;
-      if (lane == 0) drained = mbar_wait(&empty[stage], phase ^ 1);
+      if (lane == 0) {
+        int s = stage;
+        uint32_t ph = phase;
+        for (int64_t q = 0; q < n && drained; ++q) {
+          drained = mbar_wait(&empty[s], ph ^ 1);
+          if (++s == G::kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
       drained = __shfl_sync(0xffffffffu, drained, 0);
       if (!drained) {
         ok = false;
         break;
       }
-      uint8_t* st = smem + stage * G::kStage;
-      const int k0 = kk * G::kK;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&full[stage], kABytes + nt8 * G::kBTileBytes);
-        if (kGateUp) {
-          tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 64, un.e, policy);
-          tma_load_3d(st + 64 * kRowBytes, &tmA1, &full[stage], k0, un.rb * 64, un.e, policy);
-        } else {
-          tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 128, un.e, policy);
-        }
-        uint8_t* sb = st + kABytes;
-        for (int j = 0; j < nt8; ++j) {
-          tma_load_2d(sb + j * G::kBTileBytes, &tmB, &full[stage], k0, un.tok0 + 8 * j);
-          if (kInt8) tma_load_2d(sb + j * G::kBTileBytes + 1024, &tmB, &full[stage], k0 + 64, un.tok0 + 8 * j);
-        }
-      }
-      if (kInt8) {
-        float* sdst = reinterpret_cast<float*>(st + kABytes + G::kBBytes);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int row = lane + 32 * q4;
-          const float* sbase;
-          int grow;
+      for (int64_t q = 0; q < n; ++q) {
+        const int kk = kk0 + static_cast<int>(q);
+        uint8_t* st = smem + stage * G::kStage;
+        const int k0 = kk * G::kK;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], kABytes + nt8 * G::kBTileBytes);
           if (kGateUp) {
-            sbase = row < 64 ? args.s0 : args.s1;
-            grow = un.rb * 64 + (row & 63);
+            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 64, un.e, policy);
+            tma_load_3d(st + 64 * kRowBytes, &tmA1, &full[stage], k0, un.rb * 64, un.e, policy);
           } else {
-            sbase = args.s0;
-            grow = un.rb * 128 + row;
+            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 128, un.e, policy);
           }
-          grow = grow < args.rows ? grow : args.rows - 1;  // rows past the end are zero-filled by TMA
-          cp_async_4(sdst + row, sbase + (static_cast<int64_t>(un.e) * args.rows + grow) * KG + kk);
+          uint8_t* sb = st + kABytes;
+          for (int j = 0; j < nt8; ++j) {
+            tma_load_2d(sb + j * G::kBTileBytes, &tmB, &full[stage], k0, un.tok0 + 8 * j);
+            if (kInt8) tma_load_2d(sb + j * G::kBTileBytes + 1024, &tmB, &full[stage], k0 + 64, un.tok0 + 8 * j);
+          }
         }
-        cp_async_arrive_noinc(&full[stage]);
+        if (kInt8) {
+          float* sdst = reinterpret_cast<float*>(st + kABytes + G::kBBytes);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int row = lane + 32 * q4;
+            const float* sbase;
+            int grow;
+            if (kGateUp) {
+              sbase = row < 64 ? args.s0 : args.s1;
+              grow = un.rb * 64 + (row & 63);
+            } else {
+              sbase = args.s0;
+              grow = un.rb * 128 + row;
+            }
+            grow = grow < args.rows ? grow : args.rows - 1;  // rows past the end are zero-filled by TMA
+            cp_async_4(sdst + row, sbase + (static_cast<int64_t>(un.e) * args.rows + grow) * KG + kk);
+          }
+          cp_async_arrive_noinc(&full[stage]);
+        }
+        ++issued;
+        if (++stage == G::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
-      ++issued;
-      if (++stage == G::kStages) {
-        stage = 0;
-        phase ^= 1;
+      it += n;
+      kk0 += static_cast<int>(n);
+      if (kk0 == KI && it < it_end) {
+        kk0 = 0;
+        ++u;
+        un = decode(u);
       }
     }
     // Never leave with copies in flight: wait for the last phase issued on each stage.
@@ -288,101 +388,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int brow = kInt8 ? g : sg;
 
   float acc[kNT][4];
-  float accg[kInt8 ? kNT : 1][4];
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true;
-  int64_t cur_u = -1;
-  Unit un{};
   const int64_t first_unit = it_beg / KI;
+  int64_t u = first_unit;
+  int kk = static_cast<int>(it_beg - u * KI);
+  Unit un{};
+  if (it_beg < it_end) un = decode(u);
+#pragma unroll
+  for (int j = 0; j < kNT; ++j)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
 
 #pragma unroll 1
   for (int64_t it = it_beg; it < it_end; ++it) {
-    const int64_t u = it / KI;
-    const int kk = static_cast<int>(it - u * KI);
-    if (u != cur_u) {
+    if (kk == 0 && it != it_beg) {  // first stage of the next unit
+      ++u;
       un = decode(u);
-      cur_u = u;
 #pragma unroll
       for (int j = 0; j < kNT; ++j)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
     }
     const int nt8 = (un.ntok + 7) >> 3;
-
     if (ok && !mbar_wait(&full[stage], phase)) {
       ok = false;
       atomicExch(args.status, kStatusWaitFullTimeout);
     }
-    if (ok) {
-      const uint8_t* st = smem + stage * G::kStage;
-      const uint8_t* sb = st + kABytes;
-      if constexpr (!kInt8) {
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
-          const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
-#pragma unroll
-          for (int j = 0; j < kNT; ++j) {
-            if (j < nt8) {
-              const uint4 bv = *reinterpret_cast<const uint4*>(sb + j * G::kBTileBytes + swz(brow, 4 * b + t));
-              mma_16816_bf16(acc[j], alo.x, ahi.x, alo.y, ahi.y, bv.x, bv.y);
-              mma_16816_bf16(acc[j], alo.z, ahi.z, alo.w, ahi.w, bv.z, bv.w);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < kNT; ++j)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) accg[j][q] = 0.0f;
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          // 16 int8 weights per row: reduction index 64b + 16t + [0, 16)
-          const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
-          const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
-          const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
-          const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
-          uint32_t a_lo_l[4], a_lo_h[4], a_hi_l[4], a_hi_h[4];
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            int8x4_to_bf16x2x2(aw_lo[s], a_lo_l[s], a_lo_h[s]);
-            int8x4_to_bf16x2x2(aw_hi[s], a_hi_l[s], a_hi_h[s]);
-          }
-#pragma unroll
-          for (int j = 0; j < kNT; ++j) {
-            if (j < nt8) {
-              // the same 16 reduction indices of the lane's token row: 32 bytes = chunks 2t, 2t+1
-              const uint8_t* tb = sb + j * G::kBTileBytes + b * 1024;
-              const uint4 b0 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t));
-              const uint4 b1 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t + 1));
-              mma_16816_bf16(accg[j], a_lo_l[0], a_hi_l[0], a_lo_h[0], a_hi_h[0], b0.x, b0.y);
-              mma_16816_bf16(accg[j], a_lo_l[1], a_hi_l[1], a_lo_h[1], a_hi_h[1], b0.z, b0.w);
-              mma_16816_bf16(accg[j], a_lo_l[2], a_hi_l[2], a_lo_h[2], a_hi_h[2], b1.x, b1.y);
-              mma_16816_bf16(accg[j], a_lo_l[3], a_hi_l[3], a_lo_h[3], a_hi_h[3], b1.z, b1.w);
-            }
-          }
-        }
-        const float* ss = reinterpret_cast<const float*>(sb + G::kBBytes);
-        const float slo = ss[rowLo];
-        const float shi = ss[rowHi];
-#pragma unroll
-        for (int j = 0; j < kNT; ++j) {
-          acc[j][0] = fmaf(slo, accg[j][0], acc[j][0]);
-          acc[j][1] = fmaf(slo, accg[j][1], acc[j][1]);
-          acc[j][2] = fmaf(shi, accg[j][2], acc[j][2]);
-          acc[j][3] = fmaf(shi, accg[j][3], acc[j][3]);
-        }
-      }
-    }
+    if (ok) stage_mma_dispatch<kInt8>(nt8, acc, smem + stage * G::kStage, rowLo, rowHi, brow, t);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
     if (++stage == G::kStages) {
       stage = 0;
       phase ^= 1;
     }
-
-    if (kk != KI - 1 && it != it_end - 1) continue;
+    const bool piece_end = (kk == KI - 1) || (it == it_end - 1);
+    if (++kk == KI) kk = 0;
+    if (!piece_end) continue;
 
     // ---------------- end of this CTA's piece of unit u ----------------
     const int64_t ub = u * KI;
