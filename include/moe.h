@@ -140,6 +140,30 @@ moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets,
                             void* workspace, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_expert_ffn without a workspace, for callers that cannot allocate device memory when
+ * they call this library (for example a plugin inside another runtime whose device memory
+ * belongs to that runtime's pool, or a decode loop that must not call cudaMalloc mid-step).
+ * The paper has no counterpart of this entry point; it changes only who owns the scratch.
+ *   Computes exactly what moe_expert_ffn computes, with the same arguments minus the
+ *   workspace; the result may differ from moe_expert_ffn's only in fp32 summation order
+ *   when the device has more than 160 SMs.
+ *   Scratch: one fixed 32 MiB array inside this library, reserved on every GPU that loads
+ *   the library until the process exits. P * I * 2 bytes (the bf16 intermediate h) must
+ *   fit in about 22 MiB of it; larger requests return MOE_ERR_WORKSPACE and launch nothing.
+ *   All calls share that array and it keeps the last call's contents: calls whose kernels
+ *   overlap on one GPU (several streams or host threads) race and give wrong results.
+ *   The first call on a device looks up the array's device address with that device
+ *   current; make it before any stream capture starts on that device.
+ *   Calls no cudaMalloc/cudaFree and no allocating library routine.
+ */
+moe_status_t moe_expert_ffn_noalloc(const uint16_t* xg, const int32_t* expert_offsets,
+                                    const int32_t* active_experts, const int32_t* num_active,
+                                    const void* W_gate, const void* W_up, const void* W_down,
+                                    const float* s_gate, const float* s_up, const float* s_down,
+                                    moe_wtype_t wtype, int H, int I, int E, int P, float* Y,
+                                    moe_stream_t stream);
+
+/*
  * Routing-weighted combine back to row-major token order (HiNa-MoE §4.1, third
  * layout transformation):
  *   out[t, r] = bf16( sum_{j < top_k} topk_w[t, j] * Y[inv_pos[t, j], r] ),

@@ -23,6 +23,7 @@ __all__ = [
     "MoeError", "MOE_W_BF16", "MOE_W_INT8_G128", "load", "lib_path",
     "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
     "moe_expert_ffn", "moe_combine", "moe_ffn_forward", "alloc_workspace", "workspace_status",
+    "moe_expert_ffn_noalloc",
 ]
 
 MOE_W_BF16 = 0
@@ -154,3 +155,20 @@ def moe_ffn_forward(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, top_k
         _ptr(x), _ptr(logits), _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down),
         _wtype(W_gate), T, H, I, E, top_k, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def moe_expert_ffn_noalloc(xg, expert_offsets, active_experts, num_active, W_gate, W_up, W_down, s_gate, s_up,
+                           s_down, Y, stream=None) -> None:
+    """moe_expert_ffn for callers that cannot allocate: no workspace argument; the library's
+    fixed scratch area is used instead (see include/moe.h for its size limit and the rule
+    that calls overlapping on one GPU race)."""
+    P, H = xg.shape
+    E, I, _ = W_gate.shape
+    lib = load()
+    f = lib.moe_expert_ffn_noalloc
+    P_, i_ = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [P_, P_, P_, P_, P_, P_, P_, P_, P_, P_, i_, i_, i_, i_, i_, P_, P_]
+    f.restype = i_
+    _check("moe_expert_ffn_noalloc", f(
+        _ptr(xg), _ptr(expert_offsets), _ptr(active_experts), _ptr(num_active), _ptr(W_gate), _ptr(W_up),
+        _ptr(W_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _wtype(W_gate), H, I, E, P, _ptr(Y), _stream(stream)))

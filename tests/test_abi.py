@@ -41,7 +41,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
-        "moe_expert_ffn", "moe_combine", "moe_ffn_forward"])
+        "moe_expert_ffn", "moe_expert_ffn_noalloc", "moe_combine", "moe_ffn_forward"])
 
 
 def test_library_exports_every_declared_symbol(lib):
