@@ -21,6 +21,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 //   ctrl      status word (byte 0) + stream-K counters at byte 256
 //   partials  stream-K partial slots
 //   h         [P, I] bf16 (gate+up output)
+//   INT8 only: h16 [P, I] fp16, xg16 [P, H] fp16, h_scale [P], xg_scale [P] f32
 //   --- moe_ffn_forward only ---
 //   ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg [P,H] bf16, Y [P,H] f32
 constexpr size_t kCtrlBytes = 2048;
@@ -28,10 +29,10 @@ constexpr size_t kCountersOffset = 256;
 constexpr int kZeroWords = static_cast<int>((kCountersOffset + 4 * kMaxCtas) / 4);
 
 struct Layout {
-  size_t ctrl, partials, h, ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg, Y, total;
+  size_t ctrl, partials, h, h16, xg16, h_scale, xg_scale, ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg, Y, total;
 };
 
-Layout layout(int64_t P, int H, int I, int E) {
+Layout layout(int64_t P, int H, int I, int E, bool int8) {
   Layout L{};
   size_t o = 0;
   L.ctrl = o;
@@ -40,6 +41,17 @@ Layout layout(int64_t P, int H, int I, int E) {
   o = align_up(o + sizeof(float) * static_cast<size_t>(kMaxCtas) * 2 * kPartialFloats);
   L.h = o;
   o = align_up(o + 2 * static_cast<size_t>(P) * I);
+  L.h16 = L.xg16 = L.h_scale = L.xg_scale = o;
+  if (int8) {
+    L.h16 = o;
+    o = align_up(o + 2 * static_cast<size_t>(P) * I);
+    L.xg16 = o;
+    o = align_up(o + 2 * static_cast<size_t>(P) * H);
+    L.h_scale = o;
+    o = align_up(o + 4 * static_cast<size_t>(P));
+    L.xg_scale = o;
+    o = align_up(o + 4 * static_cast<size_t>(P));
+  }
   L.ids = o;
   o = align_up(o + 4 * static_cast<size_t>(P));
   L.w = o;
@@ -101,7 +113,7 @@ moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const in
                             int E, int P, float* Y, char* ws, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms < 1) return MOE_ERR_CUDA;
-  const Layout L = layout(P, H, I, E);
+  const Layout L = layout(P, H, I, E, wtype == MOE_W_INT8_G128);
   moe::ExpertFfnPlan plan{};
   plan.xg = xg;
   plan.offsets = offsets;
@@ -119,6 +131,10 @@ moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const in
   plan.E = E;
   plan.P = P;
   plan.h = reinterpret_cast<uint16_t*>(ws + L.h);
+  plan.h16 = reinterpret_cast<uint16_t*>(ws + L.h16);
+  plan.xg16 = reinterpret_cast<uint16_t*>(ws + L.xg16);
+  plan.h_scale = reinterpret_cast<float*>(ws + L.h_scale);
+  plan.xg_scale = reinterpret_cast<float*>(ws + L.xg_scale);
   plan.Y = Y;
   plan.partials = reinterpret_cast<float*>(ws + L.partials);
   plan.counters = reinterpret_cast<int32_t*>(ws + L.ctrl + kCountersOffset);
@@ -153,7 +169,7 @@ const char* moe_status_string(moe_status_t s) {
 
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, moe_wtype_t wtype) {
   if (check_sizes(T, H, I, E, top_k, wtype) != MOE_OK) return 0;
-  return layout(static_cast<int64_t>(T) * top_k, H, I, E).total;
+  return layout(static_cast<int64_t>(T) * top_k, H, I, E, wtype == MOE_W_INT8_G128).total;
 }
 
 moe_status_t moe_route_topk(const float* logits, int T, int E, int top_k, int32_t* topk_ids, float* topk_w,
@@ -199,8 +215,8 @@ moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets, c
       !aligned(active_experts, 4) || !aligned(num_active, 4))
     return MOE_ERR_INVALID_ARG;
   if (!weights_ok(W_gate, W_up, W_down, s_gate, s_up, s_down, wtype)) return MOE_ERR_INVALID_ARG;
-  const Layout L = layout(P, H, I, E);
-  if (ws_bytes < L.ids) return MOE_ERR_WORKSPACE;  // ctrl + partials + h
+  const Layout L = layout(P, H, I, E, wtype == MOE_W_INT8_G128);
+  if (ws_bytes < L.ids) return MOE_ERR_WORKSPACE;  // ctrl + partials + h (+ INT8 fp16 copies)
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   cudaError_t e = cudaMemsetAsync(ws + L.ctrl, 0, kCountersOffset + 4 * kMaxCtas, s);
@@ -235,7 +251,7 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
     return MOE_ERR_INVALID_ARG;
   if (!weights_ok(W_gate, W_up, W_down, s_gate, s_up, s_down, wtype)) return MOE_ERR_INVALID_ARG;
   const int P = T * top_k;
-  const Layout L = layout(P, H, I, E);
+  const Layout L = layout(P, H, I, E, wtype == MOE_W_INT8_G128);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   const int sms = sm_count();
   if (sms < 1) return MOE_ERR_CUDA;

@@ -12,9 +12,11 @@
 //   * Every GPU on which this library is loaded reserves kScratchBytes (32 MiB) for the
 //     array, from module load until the process exits, whether or not this entry point
 //     is ever called.
-//   * The token block must fit: P * I * 2 bytes of intermediate at most kHMaxBytes
-//     (about 22 MiB: up to about 5600 rows at I = 2048, or 800 rows at I = 14336);
-//     larger requests return MOE_ERR_WORKSPACE and launch nothing.
+//   * The token block must fit: P * I * 2 bytes of intermediate (BF16 weights), or
+//     P * (4 * I + 2 * H + 8) bytes (INT8 weights: h plus fp16 copies of h and of the token
+//     block with their row scales), at most kHMaxBytes (about 22 MiB; BF16: up to about 5600
+//     rows at I = 2048, or 800 rows at I = 14336); larger requests return MOE_ERR_WORKSPACE
+//     and launch nothing.
 //   * At most kCtas (160) CTAs take part, one per SM, whatever the SM count.
 //   * All calls share the one array, which keeps what the last call left in it. Calls whose
 //     kernels overlap on the GPU (different streams, or different host threads, on the same
@@ -108,8 +110,14 @@ extern "C" moe_status_t moe_expert_ffn_noalloc(const uint16_t* xg, const int32_t
   if (wtype == MOE_W_INT8_G128 && (!s_gate || !s_up || !s_down || !is_aligned(s_gate, 4) ||
                                    !is_aligned(s_up, 4) || !is_aligned(s_down, 4)))
     return MOE_ERR_INVALID_ARG;
-  // the fixed scratch must hold the intermediate h [P, I] bf16
-  if (static_cast<uint64_t>(P) * static_cast<uint64_t>(I) * 2u > kHMaxBytes) return MOE_ERR_WORKSPACE;
+  // the fixed scratch must hold the intermediate h [P, I] bf16 (and, for INT8, the fp16 copies)
+  const bool int8 = wtype == MOE_W_INT8_G128;
+  auto up256 = [](uint64_t x) { return (x + 255) / 256 * 256; };
+  const uint64_t h_bytes = up256(uint64_t(P) * uint64_t(I) * 2u);
+  const uint64_t h16_bytes = int8 ? h_bytes : 0;
+  const uint64_t xg16_bytes = int8 ? up256(uint64_t(P) * uint64_t(H) * 2u) : 0;
+  const uint64_t scale_bytes = int8 ? up256(uint64_t(P) * 4u) : 0;
+  if (h_bytes + h16_bytes + xg16_bytes + 2 * scale_bytes > kHMaxBytes) return MOE_ERR_WORKSPACE;
 
   char* scratch = nullptr;
   int sms = 0;
@@ -129,12 +137,16 @@ extern "C" moe_status_t moe_expert_ffn_noalloc(const uint16_t* xg, const int32_t
   plan.s_gate = s_gate;
   plan.s_up = s_up;
   plan.s_down = s_down;
-  plan.int8 = wtype == MOE_W_INT8_G128;
+  plan.int8 = int8;
   plan.H = H;
   plan.I = I;
   plan.E = E;
   plan.P = P;
   plan.h = reinterpret_cast<uint16_t*>(scratch + kHOffset);
+  plan.h16 = reinterpret_cast<uint16_t*>(scratch + kHOffset + h_bytes);
+  plan.xg16 = reinterpret_cast<uint16_t*>(scratch + kHOffset + h_bytes + h16_bytes);
+  plan.h_scale = reinterpret_cast<float*>(scratch + kHOffset + h_bytes + h16_bytes + xg16_bytes);
+  plan.xg_scale = reinterpret_cast<float*>(scratch + kHOffset + h_bytes + h16_bytes + xg16_bytes + scale_bytes);
   plan.Y = Y;
   plan.partials = reinterpret_cast<float*>(scratch + kPartialsOffset);
   plan.counters = reinterpret_cast<int32_t*>(scratch + kCountersOffset);

@@ -1,5 +1,6 @@
 // Host side of the weight-streaming expert kernels: TMA descriptors and launches.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -42,16 +43,83 @@ bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows,
   return r == CUDA_SUCCESS;
 }
 
-// Token block {K (contiguous), P rows} bf16; box = 64 elements x 8 rows; 128-byte swizzle.
-bool encode_tokens(CUtensorMap* map, const void* X, int K, int P) {
+// Token block {K (contiguous), P rows} bf16 or fp16; box = 64 elements x 8 rows; 128-byte swizzle.
+bool encode_tokens(CUtensorMap* map, const void* X, int K, int P, bool fp16 = false) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(P)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   cuuint32_t box[2] = {64, 8};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides,
+  CUresult r = tensor_map_encoder()(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                    const_cast<void*>(X), dims, strides,
                                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// fp16 copy of bf16 rows for the INT8 path: each row is multiplied by 2^-k, with k chosen so that
+// its largest magnitude lands in [2^14, 2^15) (inside fp16's range, k clamped to [-100, 127]),
+// and row_scale[p] = 2^k restores it after the MMA. Every value within 2^-31 of the row's
+// largest keeps its bf16 bits exactly in fp16; smaller ones round to fp16's subnormal grid.
+constexpr int kRowThreads = 256;
+
+__global__ void __launch_bounds__(kRowThreads)
+    rows_to_f16_kernel(const uint4* __restrict__ src, int K8, int64_t P, uint4* __restrict__ dst,
+                       float* __restrict__ row_scale) {
+  __shared__ float s_max[kRowThreads / 32];
+  pdl_wait_predecessor();
+  pdl_allow_successor();
+  const int tid = threadIdx.x;
+  for (int64_t p = blockIdx.x; p < P; p += gridDim.x) {
+    const uint4* s4 = src + p * K8;
+    float m = 0.0f;
+    for (int c = tid; c < K8; c += kRowThreads) {
+      const uint4 v = s4[c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((tid & 31) == 0) s_max[tid >> 5] = m;
+    __syncthreads();
+    m = s_max[0];
+#pragma unroll
+    for (int i = 1; i < kRowThreads / 32; ++i) m = fmaxf(m, s_max[i]);
+    int k = 0;
+    if (m > 0.0f && m <= 3.0e38f) {
+      int e = 0;
+      frexpf(m, &e);  // m = f * 2^e, 0.5 <= f < 1
+      k = e - 15;
+      k = k < -100 ? -100 : (k > 127 ? 127 : k);
+    }
+    const float down = ldexpf(1.0f, -k);
+    uint4* d4 = dst + p * K8;
+    for (int c = tid; c < K8; c += kRowThreads) {
+      const uint4 v = s4[c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w[i] << 16) * down,
+                                             __uint_as_float(w[i] & 0xffff0000u) * down);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      d4[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid == 0) row_scale[p] = ldexpf(1.0f, k);
+    __syncthreads();  // s_max is reused by the next row
+  }
+}
+
+cudaError_t launch_rows_to_f16(const uint16_t* src, int K, int P, uint16_t* dst, float* row_scale, int num_sms,
+                               cudaStream_t s) {
+  int blocks = P < num_sms * 4 ? P : num_sms * 4;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(rows_to_f16_kernel, dim3(blocks), dim3(kRowThreads), 0, s, reinterpret_cast<const uint4*>(src),
+                    K / 8, static_cast<int64_t>(P), reinterpret_cast<uint4*>(dst), row_scale);
 }
 
 template <bool kInt8, bool kGateUp>
@@ -76,8 +144,9 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
   if (!encode_weights(&tg, p.W_gate, kInt8, p.H, p.I, p.E, 64) ||
       !encode_weights(&tu, p.W_up, kInt8, p.H, p.I, p.E, 64) ||
-      !encode_weights(&td, p.W_down, kInt8, p.I, p.H, p.E, 128) || !encode_tokens(&txg, p.xg, p.H, p.P) ||
-      !encode_tokens(&th, p.h, p.I, p.P))
+      !encode_weights(&td, p.W_down, kInt8, p.I, p.H, p.E, 128) ||
+      !encode_tokens(&txg, kInt8 ? p.xg16 : p.xg, p.H, p.P, kInt8) ||
+      !encode_tokens(&th, kInt8 ? p.h16 : p.h, p.I, p.P, kInt8))
     return cudaErrorInvalidValue;
   cudaError_t e = prepare_kernel<kInt8, true>();
   if (e != cudaSuccess) return e;
@@ -94,7 +163,12 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
   a.E = p.E;
   a.P = p.P;
 
+  if (kInt8) {
+    e = launch_rows_to_f16(p.xg, p.H, p.P, p.xg16, p.xg_scale, p.num_ctas, s);
+    if (e != cudaSuccess) return e;
+  }
   stream::Args gu = a;
+  gu.row_scale = p.xg_scale;
   gu.s0 = p.s_gate;
   gu.s1 = p.s_up;
   gu.out = p.h;
@@ -105,7 +179,12 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
                  tg, tu, txg, gu);
   if (e != cudaSuccess) return e;
 
+  if (kInt8) {
+    e = launch_rows_to_f16(p.h, p.I, p.P, p.h16, p.h_scale, p.num_ctas, s);
+    if (e != cudaSuccess) return e;
+  }
   stream::Args dn = a;
+  dn.row_scale = p.h_scale;
   dn.s0 = p.s_down;
   dn.s1 = p.s_down;
   dn.out = p.Y;

@@ -80,6 +80,9 @@ struct Args {
   int K;                      // reduction length: H (gate+up) or I (down)
   int E;
   int P;                      // rows of the token block
+  // INT8 only: the token tiles are fp16 copies of the bf16 rows, each row multiplied by a power
+  // of two that keeps it inside fp16's range; row_scale[p] undoes that factor (exactly).
+  const float* row_scale;
 };
 
 // MMA row/column g (0..7) -> row within an 8-row swizzle atom. Lanes g and g^1 share a
@@ -121,7 +124,8 @@ __device__ __forceinline__ void stage_mma(float (&acc)[kNT][4], const uint8_t* s
       for (int q = 0; q < 4; ++q) accg[j][q] = 0.0f;
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
-      // 16 int8 weights per row: reduction index 64b + 16t + [0, 16)
+      // 16 int8 weights per row: reduction index 64b + 16t + [0, 16); converted exactly to fp16
+      // and multiplied with the fp16 token tile (see the token-row scales in Args)
       const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
       const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
       const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
@@ -129,8 +133,8 @@ __device__ __forceinline__ void stage_mma(float (&acc)[kNT][4], const uint8_t* s
       uint32_t a_lo_l[4], a_lo_h[4], a_hi_l[4], a_hi_h[4];
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        int8x4_to_bf16x2x2(aw_lo[s], a_lo_l[s], a_lo_h[s]);
-        int8x4_to_bf16x2x2(aw_hi[s], a_hi_l[s], a_hi_h[s]);
+        int8x4_to_f16x2x2(aw_lo[s], a_lo_l[s], a_lo_h[s]);
+        int8x4_to_f16x2x2(aw_hi[s], a_hi_l[s], a_hi_h[s]);
       }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
@@ -138,10 +142,10 @@ __device__ __forceinline__ void stage_mma(float (&acc)[kNT][4], const uint8_t* s
         const uint8_t* tb = sb + j * G::kBTileBytes + b * 1024;
         const uint4 b0 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t));
         const uint4 b1 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t + 1));
-        mma_16816_bf16(accg[j], a_lo_l[0], a_hi_l[0], a_lo_h[0], a_hi_h[0], b0.x, b0.y);
-        mma_16816_bf16(accg[j], a_lo_l[1], a_hi_l[1], a_lo_h[1], a_hi_h[1], b0.z, b0.w);
-        mma_16816_bf16(accg[j], a_lo_l[2], a_hi_l[2], a_lo_h[2], a_hi_h[2], b1.x, b1.y);
-        mma_16816_bf16(accg[j], a_lo_l[3], a_hi_l[3], a_lo_h[3], a_hi_h[3], b1.z, b1.w);
+        mma_16816_f16(accg[j], a_lo_l[0], a_hi_l[0], a_lo_h[0], a_hi_h[0], b0.x, b0.y);
+        mma_16816_f16(accg[j], a_lo_l[1], a_hi_l[1], a_lo_h[1], a_hi_h[1], b0.z, b0.w);
+        mma_16816_f16(accg[j], a_lo_l[2], a_hi_l[2], a_lo_h[2], a_hi_h[2], b1.x, b1.y);
+        mma_16816_f16(accg[j], a_lo_l[3], a_hi_l[3], a_lo_h[3], a_hi_h[3], b1.z, b1.w);
       }
     }
     const float* ss = reinterpret_cast<const float*>(sb + G::kBBytes);
@@ -487,8 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int col = 2 * t + c;
               const int n = 8 * j + (kInt8 ? col : sigma(col));
               if (n < un.ntok) {
-                const float gv = acc[j][c];
-                const float uv = acc[j][2 + c];
+                const float rs = kInt8 ? args.row_scale[un.tok0 + n] : 1.0f;
+                const float gv = acc[j][c] * rs;
+                const float uv = acc[j][2 + c] * rs;
                 const float silu = gv / (1.0f + expf(-gv));
                 h[static_cast<int64_t>(un.tok0 + n) * args.out_ld + i] = __float2bfloat16_rn(silu * uv);
               }
@@ -509,8 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = 8 * j + (kInt8 ? col : sigma(col));
             if (n < un.ntok) {
               float* yr = y + static_cast<int64_t>(un.tok0 + n) * args.out_ld;
-              if (r_lo < args.rows) yr[r_lo] = acc[j][c];
-              if (r_hi < args.rows) yr[r_hi] = acc[j][2 + c];
+              const float rs = kInt8 ? args.row_scale[un.tok0 + n] : 1.0f;
+              if (r_lo < args.rows) yr[r_lo] = acc[j][c] * rs;
+              if (r_hi < args.rows) yr[r_hi] = acc[j][2 + c] * rs;
             }
           }
         }

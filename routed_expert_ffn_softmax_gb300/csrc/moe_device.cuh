@@ -141,21 +141,26 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// ---------------------------------------------------------------- INT8 -> bf16
-// Four signed bytes of `w` (little-endian order q0..q3) -> bf16 pairs
-// lo = (q0, q1), hi = (q2, q3); exact for every int8 value.
-// Each byte is offset to unsigned (q + 128), placed in the low mantissa byte of the
-// float 2^23 (bits 0x4B000000), and 2^23 + 128 is subtracted, which leaves q exactly.
-// A value with at most 8 significant bits has zero low 16 bits, so its bf16 is the
-// float's high half.
-__device__ __forceinline__ void int8x4_to_bf16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate (same fragment layout).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- INT8 -> fp16
+// Four signed bytes of `w` (little-endian q0..q3) -> fp16 pairs lo = (q0, q1), hi = (q2, q3),
+// exact for every int8 value. Flipping each byte's top bit gives u = q + 128 (0..255); placed
+// under the high byte 0x64, a 16-bit lane is the fp16 number 1024 + u, and subtracting 1152
+// (bits 0x6480) leaves q. Per four weights: one logic op, two byte permutes, two fp16x2 subs.
+__device__ __forceinline__ void int8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;
-  const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
-  const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
-  const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
-  const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
-  lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-  hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+  const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x4140);  // [u0, 0x64, u1, 0x64]
+  const uint32_t p23 = __byte_perm(u, 0x64646464u, 0x4342);  // [u2, 0x64, u3, 0x64]
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(p01), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(p23), "r"(0x64806480u));
 }
 
 }  // namespace moe

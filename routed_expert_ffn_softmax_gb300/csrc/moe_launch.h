@@ -52,6 +52,11 @@ struct ExpertFfnPlan {
   bool int8;
   int H, I, E, P;
   uint16_t* h;        // [P, I] scratch
+  // INT8 only (scratch): fp16 copies of the token block and of h, and their row scales
+  uint16_t* xg16;     // [P, H]
+  uint16_t* h16;      // [P, I]
+  float* xg_scale;    // [P]
+  float* h_scale;     // [P]
   float* Y;           // [P, H]
   float* partials;    // stream-K partial slots
   int32_t* counters;  // zeroed, kMaxCtas entries

@@ -207,6 +207,22 @@ def test_expert_ffn_entry_point_matches_oracle(T, H, I, E, k, wtype, skew):
     assert_moe_close(to_np_f32(out), oracle.bf16_bits_to_f32(ref["out"]), wtype, "out")
 
 
+@pytest.mark.parametrize("x_scale", [2.0 ** 17, 2.0 ** -30, 1.0])
+def test_int8_activation_range(x_scale):
+    """INT8 runs the tensor cores in fp16; token rows far outside fp16's range (large or tiny)
+    must still match the oracle to a purely relative bound."""
+    T, H, I, E, k = 9, 256, 384, 8, 2
+    cfg, L, x, lg = small_case(T, H, I, E, k, "int8", seed=77)
+    xs = (x.float() * x_scale).to(torch.bfloat16)
+    out, _ = run_forward_ws(L, xs, lg, k)
+    ref = oracle.forward(xs, lg, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
+                         wtype="int8", top_k=k)
+    r = oracle.bf16_bits_to_f32(ref["out"]).astype(np.float64)
+    g = to_np_f32(out).astype(np.float64)
+    assert np.all(np.isfinite(g)) and np.abs(r).max() > 0
+    assert np.abs(g - r).max() <= 2e-2 * np.abs(r).max()
+
+
 def test_forward_is_deterministic_and_repeatable():
     cfg, L, x, lg = small_case(64, 512, 1024, 8, 2, "bf16", seed=3)
     a, ws = run_forward_ws(L, x, lg, 2)
