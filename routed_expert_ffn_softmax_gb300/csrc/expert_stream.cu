@@ -28,18 +28,19 @@ TensorMapEncodeFn tensor_map_encoder() {
 
 namespace {
 
-// Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage of
-// 128 bytes along K by `box_rows` rows of one expert; 128-byte swizzle.
+// Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage of 64
+// reduction elements by `box_rows` rows of one expert. BF16 rows are 128 bytes per stage and use
+// the 128-byte swizzle; INT8 rows are 64 bytes and are not swizzled.
 bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows, int E, int box_rows) {
   const cuuint64_t eb = int8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(E)};
   cuuint64_t strides[2] = {K * eb, static_cast<cuuint64_t>(K) * rows * eb};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = tensor_map_encoder()(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                                     const_cast<void*>(W), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                                    int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -142,9 +143,9 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
   using G = stream::Geometry<kInt8>;
   CUtensorMap tg, tu, td, txg, th;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
-  if (!encode_weights(&tg, p.W_gate, kInt8, p.H, p.I, p.E, 64) ||
-      !encode_weights(&tu, p.W_up, kInt8, p.H, p.I, p.E, 64) ||
-      !encode_weights(&td, p.W_down, kInt8, p.I, p.H, p.E, 128) ||
+  if (!encode_weights(&tg, p.W_gate, kInt8, p.H, p.I, p.E, G::kRowsA / 2) ||
+      !encode_weights(&tu, p.W_up, kInt8, p.H, p.I, p.E, G::kRowsA / 2) ||
+      !encode_weights(&td, p.W_down, kInt8, p.I, p.H, p.E, G::kRowsA) ||
       !encode_tokens(&txg, kInt8 ? p.xg16 : p.xg, p.H, p.P, kInt8) ||
       !encode_tokens(&th, kInt8 ? p.h16 : p.h, p.I, p.P, kInt8))
     return cudaErrorInvalidValue;
@@ -175,7 +176,7 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
   gu.out_ld = p.I;
   gu.rows = p.I;
   gu.K = p.H;
-  e = launch_pdl(stream::expert_stream_kernel<kInt8, true>, dim3(p.num_ctas), dim3(stream::kThreads), G::kSmem, s,
+  e = launch_pdl(stream::expert_stream_kernel<kInt8, true>, dim3(p.num_ctas), dim3(G::kThreads), G::kSmem, s,
                  tg, tu, txg, gu);
   if (e != cudaSuccess) return e;
 
@@ -191,7 +192,7 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
   dn.out_ld = p.H;
   dn.rows = p.H;
   dn.K = p.I;
-  return launch_pdl(stream::expert_stream_kernel<kInt8, false>, dim3(p.num_ctas), dim3(stream::kThreads), G::kSmem,
+  return launch_pdl(stream::expert_stream_kernel<kInt8, false>, dim3(p.num_ctas), dim3(G::kThreads), G::kSmem,
                     s, td, td, th, dn);
 }
 

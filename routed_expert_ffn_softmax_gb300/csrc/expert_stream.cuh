@@ -6,30 +6,34 @@
 // for every row p of an active expert e's token block, fp32 accumulation (§4.2.1).
 //
 // How (GB300 design; the pages' AMX micro-kernel is prior art, not the blueprint):
-//  * The weights are the large operand and are read exactly once per 64 routed
-//    tokens, in their general row-major layout (§2.2; "transform I, not W", §4.1).
-//    They sit on the 16-row side of the MMA ("swap AB"), the few tokens on the
-//    8-wide side, so even one token per expert runs on the tensor cores (§4.2.1:
-//    the matrix engine is used for every row count, no vector-unit fallback).
-//  * One persistent CTA per SM. A producer warp streams 128 weight rows x 128 bytes
-//    per stage with TMA (cp.async.bulk.tensor, evict-first L2 policy: the weights
-//    have no reuse, the streaming analogue of tileloadt1 in §4.2.2) together with the
-//    stage's token tiles, through a ring of mbarrier-guarded stages. Eight consumer
-//    warps run mma.sync m16n8k16 out of shared memory.
+//  * The weights are the large operand and are read exactly once per pass of tokens,
+//    in their general row-major layout (§2.2; "transform I, not W", §4.1). They sit on
+//    the 16-row side of the MMA ("swap AB"), the few tokens on the 8-wide side, so even
+//    one token per expert runs on the tensor cores (§4.2.1: the matrix engine is used
+//    for every row count, no vector-unit fallback).
+//  * One persistent CTA per SM. A producer warp streams one stage of weight rows
+//    (16 KB) with TMA (cp.async.bulk.tensor, evict-first L2 policy: the weights have no
+//    reuse, the streaming analogue of tileloadt1 in §4.2.2) together with the stage's
+//    token tiles, through a ring of mbarrier-guarded stages; consumer warps run
+//    mma.sync m16n8k16 out of shared memory, one 16-row weight tile each.
+//      BF16: 128 rows x 128 B (64 elements) per stage, 8 consumer warps, <= 64 tokens/pass.
+//      INT8: 256 rows x 64 B (64 elements) per stage, 16 consumer warps, <= 32 tokens/pass;
+//            twice the warps per weight byte, because every int8 weight is converted to
+//            fp16 in registers before it reaches the tensor core. Each consumer lane reads
+//            its two rows' group scales itself, so the producer issues nothing but TMA.
 //  * Gate and up rows of the same intermediate index are paired inside one MMA tile
 //    (tile rows 0-7 gate, 8-15 up), so the SiLU(g)*u epilogue is register-local
 //    (the second layout transformation of §4.1 happens in this epilogue: h is
 //    written token-major, the layout the down kernel's token tiles load). The down
 //    kernel writes Y token-major (the third transformation).
-//  * Work = (active expert, pass of <= 64 tokens, block of output rows) x reduction
-//    stages. The flattened stage range is split evenly over the CTAs (stream-K), so
-//    every SM streams the same number of weight bytes whatever the routing. A unit
-//    cut by a CTA boundary is finished by whichever of its CTAs arrives last
-//    (atomic counter, no waiting), which sums the fp32 partials in a fixed order,
-//    so results are deterministic.
-//  * Shared-memory tiles use the 128-byte TMA swizzle; the MMA's row and column
-//    order is permuted (sigma below) so that every 16-byte shared load of a warp is
-//    bank-conflict free.
+//  * Work = (active expert, pass of tokens, block of output rows) x reduction stages.
+//    The flattened stage range is split evenly over the CTAs (stream-K), so every SM
+//    streams the same number of weight bytes whatever the routing. A unit cut by a CTA
+//    boundary is finished by whichever of its CTAs arrives last (atomic counter, no
+//    waiting), which sums the fp32 partials in a fixed order: results are deterministic.
+//  * Shared-memory loads are bank-conflict free: BF16 tiles use the 128-byte TMA swizzle
+//    with the MMA's row/column order permuted (sigma); INT8 weight rows are 64 bytes
+//    apart, so the two rows a quarter-warp reads fall in different bank halves.
 #pragma once
 
 #include "moe_device.cuh"
@@ -37,32 +41,33 @@
 namespace moe {
 namespace stream {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kRowsA = 128;                      // weight rows per stage
-constexpr int kRowBytes = 128;                   // bytes of each weight row per stage
-constexpr int kABytes = kRowsA * kRowBytes;      // 16 KB
-constexpr int kNMax = 64;                        // tokens per pass
-constexpr int kNT = kNMax / 8;                   // n8 tiles per pass
-constexpr int kTable = 256;                      // max experts (routing limit)
-constexpr int kMaxCtas = 256;                    // partial-slot capacity of the workspace
-constexpr int kIssueGroup = 4;                   // reduction stages issued back to back per row block
-constexpr int kPartialFloats = kNT * 4 * kConsumerThreads;  // one CTA slot: 32 regs x 256 threads
+constexpr int kTable = 256;          // max experts (routing limit)
+constexpr int kMaxCtas = 256;        // partial-slot capacity of the workspace
+constexpr int kIssueGroup = 4;       // reduction stages issued back to back per row block
+constexpr int kABytes = 16384;       // weight bytes per stage
+constexpr int kPartialFloats = 8192; // one CTA's partial slot (fp32)
 
 template <bool kInt8>
 struct Geometry {
-  static constexpr int kK = kInt8 ? 128 : 64;            // reduction elements per stage
-  static constexpr int kBTileBytes = kInt8 ? 2048 : 1024;  // one n8 token tile per stage
+  static constexpr int kConsumerWarps = kInt8 ? 16 : 8;
+  static constexpr int kConsumerThreads = kConsumerWarps * 32;
+  static constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+  static constexpr int kRowsA = kInt8 ? 256 : 128;        // weight rows per stage
+  static constexpr int kRowBytes = kInt8 ? 64 : 128;      // bytes of each weight row per stage
+  static constexpr int kK = 64;                           // reduction elements per stage
+  static constexpr int kNMax = kInt8 ? 32 : 64;           // tokens per pass
+  static constexpr int kNT = kNMax / 8;                   // n8 token tiles per pass
+  static constexpr int kBTileBytes = 1024;                // one n8 tile: 8 rows x 64 x 2 B
   static constexpr int kBBytes = kNT * kBTileBytes;
-  static constexpr int kSBytes = kInt8 ? 1024 : 0;       // 128 fp32 scales, padded
-  static constexpr int kStage = kABytes + kBBytes + kSBytes;  // multiple of 1024
-  static constexpr int kStages = kInt8 ? 6 : 8;
+  static constexpr int kStage = kABytes + kBBytes;
+  static constexpr int kStages = kInt8 ? 10 : 8;
   static constexpr int kBarBytes = 2 * kStages * 8;
-  static constexpr int kTableBytes = (4 * kTable + 16) * 4;
+  static constexpr int kTableBytes = (4 * kTable + 32) * 4;
   static constexpr int kSmem = kStages * kStage + kBarBytes + kTableBytes;
+  static_assert(kRowsA * kRowBytes == kABytes, "a stage holds 16 KB of weights");
   static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment for the 128B swizzle");
   static_assert(kIssueGroup <= kStages, "an issue group must fit in the ring");
+  static_assert(kNT * 4 * kConsumerThreads == kPartialFloats, "partial slot size");
 };
 
 struct Args {
@@ -87,7 +92,7 @@ struct Args {
 
 // MMA row/column g (0..7) -> row within an 8-row swizzle atom. Lanes g and g^1 share a
 // quarter-warp; sigma puts them in rows whose swizzle keys differ in bit 2, so their
-// 64-byte halves land on disjoint banks.
+// 64-byte halves land on disjoint banks (BF16 tiles).
 __device__ __forceinline__ int sigma(int g) { return ((g & 1) << 2) | (g >> 1); }
 
 // Byte offset of 16-byte chunk `c` of row `r` in a tile of 128-byte rows (128B swizzle).
@@ -100,8 +105,8 @@ struct Unit {
 // One stage of MMAs for a warp: its m16 weight tile (rows rowLo / rowHi) against NT n8 token
 // tiles. NT is a compile-time constant so no instruction is issued for unused token tiles.
 template <bool kInt8, int NT>
-__device__ __forceinline__ void stage_mma(float (&acc)[kNT][4], const uint8_t* st, int rowLo, int rowHi,
-                                          int brow, int t) {
+__device__ __forceinline__ void stage_mma(float (&acc)[Geometry<kInt8>::kNT][4], const uint8_t* st, int rowLo,
+                                          int rowHi, int brow, int t, float slo, float shi) {
   using G = Geometry<kInt8>;
   const uint8_t* sb = st + kABytes;
   if constexpr (!kInt8) {
@@ -117,40 +122,33 @@ __device__ __forceinline__ void stage_mma(float (&acc)[kNT][4], const uint8_t* s
       }
     }
   } else {
+    // 16 int8 weights per row: reduction index 16t + [0, 16) of this stage's 64; converted
+    // exactly to fp16 and multiplied with the fp16 token tile (see Args::row_scale)
+    const uint4 alo = *reinterpret_cast<const uint4*>(st + rowLo * 64 + t * 16);
+    const uint4 ahi = *reinterpret_cast<const uint4*>(st + rowHi * 64 + t * 16);
+    const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
+    const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+    uint32_t a_lo_l[4], a_lo_h[4], a_hi_l[4], a_hi_h[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      int8x4_to_f16x2x2(aw_lo[s], a_lo_l[s], a_lo_h[s]);
+      int8x4_to_f16x2x2(aw_hi[s], a_hi_l[s], a_hi_h[s]);
+    }
     float accg[NT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+    for (int j = 0; j < NT; ++j) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) accg[j][q] = 0.0f;
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      // 16 int8 weights per row: reduction index 64b + 16t + [0, 16); converted exactly to fp16
-      // and multiplied with the fp16 token tile (see the token-row scales in Args)
-      const uint4 alo = *reinterpret_cast<const uint4*>(st + swz(rowLo, 4 * b + t));
-      const uint4 ahi = *reinterpret_cast<const uint4*>(st + swz(rowHi, 4 * b + t));
-      const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
-      const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
-      uint32_t a_lo_l[4], a_lo_h[4], a_hi_l[4], a_hi_h[4];
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        int8x4_to_f16x2x2(aw_lo[s], a_lo_l[s], a_lo_h[s]);
-        int8x4_to_f16x2x2(aw_hi[s], a_hi_l[s], a_hi_h[s]);
-      }
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        // the same 16 reduction indices of the lane's token row: 32 bytes = chunks 2t, 2t+1
-        const uint8_t* tb = sb + j * G::kBTileBytes + b * 1024;
-        const uint4 b0 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t));
-        const uint4 b1 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t + 1));
-        mma_16816_f16(accg[j], a_lo_l[0], a_hi_l[0], a_lo_h[0], a_hi_h[0], b0.x, b0.y);
-        mma_16816_f16(accg[j], a_lo_l[1], a_hi_l[1], a_lo_h[1], a_hi_h[1], b0.z, b0.w);
-        mma_16816_f16(accg[j], a_lo_l[2], a_hi_l[2], a_lo_h[2], a_hi_h[2], b1.x, b1.y);
-        mma_16816_f16(accg[j], a_lo_l[3], a_hi_l[3], a_lo_h[3], a_hi_h[3], b1.z, b1.w);
-      }
+      // the same 16 reduction indices of the lane's token row: 32 bytes = chunks 2t, 2t+1
+      const uint8_t* tb = sb + j * G::kBTileBytes;
+      const uint4 b0 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t));
+      const uint4 b1 = *reinterpret_cast<const uint4*>(tb + swz(brow, 2 * t + 1));
+      mma_16816_f16(accg[j], a_lo_l[0], a_hi_l[0], a_lo_h[0], a_hi_h[0], b0.x, b0.y);
+      mma_16816_f16(accg[j], a_lo_l[1], a_hi_l[1], a_lo_h[1], a_hi_h[1], b0.z, b0.w);
+      mma_16816_f16(accg[j], a_lo_l[2], a_hi_l[2], a_lo_h[2], a_hi_h[2], b1.x, b1.y);
+      mma_16816_f16(accg[j], a_lo_l[3], a_hi_l[3], a_lo_h[3], a_hi_h[3], b1.z, b1.w);
     }
-    const float* ss = reinterpret_cast<const float*>(sb + G::kBBytes);
-    const float slo = ss[rowLo];
-    const float shi = ss[rowHi];
+    // this stage is half of one 128-wide scale group: its partial sum takes the group scale
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       acc[j][0] = fmaf(slo, accg[j][0], acc[j][0]);
@@ -162,26 +160,41 @@ __device__ __forceinline__ void stage_mma(float (&acc)[kNT][4], const uint8_t* s
 }
 
 template <bool kInt8>
-__device__ __forceinline__ void stage_mma_dispatch(int nt8, float (&acc)[kNT][4], const uint8_t* st, int rowLo,
-                                                   int rowHi, int brow, int t) {
-  switch (nt8) {
-    case 1: stage_mma<kInt8, 1>(acc, st, rowLo, rowHi, brow, t); break;
-    case 2: stage_mma<kInt8, 2>(acc, st, rowLo, rowHi, brow, t); break;
-    case 3: stage_mma<kInt8, 3>(acc, st, rowLo, rowHi, brow, t); break;
-    case 4: stage_mma<kInt8, 4>(acc, st, rowLo, rowHi, brow, t); break;
-    case 5: stage_mma<kInt8, 5>(acc, st, rowLo, rowHi, brow, t); break;
-    case 6: stage_mma<kInt8, 6>(acc, st, rowLo, rowHi, brow, t); break;
-    case 7: stage_mma<kInt8, 7>(acc, st, rowLo, rowHi, brow, t); break;
-    default: stage_mma<kInt8, 8>(acc, st, rowLo, rowHi, brow, t); break;
+__device__ __forceinline__ void stage_mma_dispatch(int nt8, float (&acc)[Geometry<kInt8>::kNT][4],
+                                                   const uint8_t* st, int rowLo, int rowHi, int brow, int t,
+                                                   float slo, float shi) {
+  if constexpr (kInt8) {
+    switch (nt8) {
+      case 1: stage_mma<kInt8, 1>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 2: stage_mma<kInt8, 2>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 3: stage_mma<kInt8, 3>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      default: stage_mma<kInt8, 4>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+    }
+  } else {
+    switch (nt8) {
+      case 1: stage_mma<kInt8, 1>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 2: stage_mma<kInt8, 2>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 3: stage_mma<kInt8, 3>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 4: stage_mma<kInt8, 4>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 5: stage_mma<kInt8, 5>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 6: stage_mma<kInt8, 6>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      case 7: stage_mma<kInt8, 7>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+      default: stage_mma<kInt8, 8>(acc, st, rowLo, rowHi, brow, t, slo, shi); break;
+    }
   }
 }
 
 template <bool kInt8, bool kGateUp>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Geometry<kInt8>::kThreads, 1)
     expert_stream_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Args args) {
   using G = Geometry<kInt8>;
-  constexpr int kRowsPerUnit = kGateUp ? 64 : 128;  // output rows per unit
+  constexpr int kNMax = G::kNMax;
+  constexpr int kNT = G::kNT;
+  constexpr int kCW = G::kConsumerWarps;
+  constexpr int kCT = G::kConsumerThreads;
+  constexpr int kPairRows = G::kRowsA / 2;                       // gate (or up) rows per stage
+  constexpr int kRowsPerUnit = kGateUp ? kPairRows : G::kRowsA;  // output rows per unit
 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStage);
@@ -198,12 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < G::kStages; ++s) {
-      mbar_init(&full[s], kInt8 ? 33 : 1);  // producer expect_tx (+ 32 cp.async arrivals)
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&full[s], 1);  // the producer's expect_tx arrival
+      mbar_init(&empty[s], kCW);
     }
     fence_mbar_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (warp == kCW && lane == 0) {
     tma_prefetch_desc(&tmA0);
     if (kGateUp) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
@@ -213,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_allow_successor();
 
   // ---- per-CTA schedule tables: active experts, their token blocks, pass prefix
+  // (threads 0..255, i.e. warps 0..7, build them)
   int A = *args.num_active;
   A = A < 0 ? 0 : (A > args.E ? args.E : A);
   int passes = 0;
@@ -236,9 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += n;
   }
-  if (warp < kConsumerWarps && lane == 31) s_misc[warp] = incl;
+  if (tid < kTable && lane == 31) s_misc[warp] = incl;
   __syncthreads();
-  if (warp < kConsumerWarps) {
+  if (tid < kTable) {
     int add = 0;
     for (int w = 0; w < warp; ++w) add += s_misc[w];
     t_pp[tid + 1] = incl + add;
@@ -273,10 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     return r;
   };
 
-  if (warp == kConsumerWarps) {
+  if (warp == kCW) {
     // =========================== producer warp ===========================
     const uint64_t policy = l2_policy_evict_first();
-    const int KG = args.K / 128;  // scale groups per row (int8)
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -315,35 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[stage], kABytes + nt8 * G::kBTileBytes);
           if (kGateUp) {
-            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 64, un.e, policy);
-            tma_load_3d(st + 64 * kRowBytes, &tmA1, &full[stage], k0, un.rb * 64, un.e, policy);
+            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * kPairRows, un.e, policy);
+            tma_load_3d(st + kPairRows * G::kRowBytes, &tmA1, &full[stage], k0, un.rb * kPairRows, un.e, policy);
           } else {
-            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * 128, un.e, policy);
+            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * G::kRowsA, un.e, policy);
           }
           uint8_t* sb = st + kABytes;
-          for (int j = 0; j < nt8; ++j) {
-            tma_load_2d(sb + j * G::kBTileBytes, &tmB, &full[stage], k0, un.tok0 + 8 * j);
-            if (kInt8) tma_load_2d(sb + j * G::kBTileBytes + 1024, &tmB, &full[stage], k0 + 64, un.tok0 + 8 * j);
-          }
-        }
-        if (kInt8) {
-          float* sdst = reinterpret_cast<float*>(st + kABytes + G::kBBytes);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int row = lane + 32 * q4;
-            const float* sbase;
-            int grow;
-            if (kGateUp) {
-              sbase = row < 64 ? args.s0 : args.s1;
-              grow = un.rb * 64 + (row & 63);
-            } else {
-              sbase = args.s0;
-              grow = un.rb * 128 + row;
-            }
-            grow = grow < args.rows ? grow : args.rows - 1;  // rows past the end are zero-filled by TMA
-            cp_async_4(sdst + row, sbase + (static_cast<int64_t>(un.e) * args.rows + grow) * KG + kk);
-          }
-          cp_async_arrive_noinc(&full[stage]);
+          for (int j = 0; j < nt8; ++j) tma_load_2d(sb + j * G::kBTileBytes, &tmB, &full[stage], k0, un.tok0 + 8 * j);
         }
         ++issued;
         if (++stage == G::kStages) {
@@ -380,14 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ============================ consumer warps ============================
-  const int cw = warp;           // 0..7
-  const int ctid = tid;          // 0..255
+  const int cw = warp;           // 0 .. kCW-1
+  const int ctid = tid;          // 0 .. kCT-1
   const int g = lane >> 2;
   const int t = lane & 3;
-  const int sg = sigma(g);
+  const int sg = kInt8 ? g : sigma(g);
   // weight rows of this warp's MMA tile (rows g / g+8 of the m16 tile)
   const int rowLo = kGateUp ? cw * 8 + sg : cw * 16 + sg;
-  const int rowHi = kGateUp ? 64 + cw * 8 + sg : cw * 16 + 8 + sg;
+  const int rowHi = kGateUp ? kPairRows + cw * 8 + sg : cw * 16 + 8 + sg;
   // token row of this lane's B fragment inside each n8 tile (MMA column g)
   const int brow = kInt8 ? g : sg;
 
@@ -399,7 +390,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t u = first_unit;
   int kk = static_cast<int>(it_beg - u * KI);
   Unit un{};
-  if (it_beg < it_end) un = decode(u);
+  // INT8: this lane's two weight rows' group scales for the current unit (read straight from
+  // global memory; each 32-byte sector serves eight groups, so most reads hit L1)
+  const int KG = args.K / 128;
+  const float* scale_lo = nullptr;
+  const float* scale_hi = nullptr;
+  auto scale_rows = [&]() {
+    if constexpr (kInt8) {
+      int glo, ghi;
+      const float* blo;
+      const float* bhi;
+      if (kGateUp) {
+        glo = ghi = un.rb * kPairRows + cw * 8 + sg;
+        blo = args.s0;
+        bhi = args.s1;
+      } else {
+        glo = un.rb * G::kRowsA + cw * 16 + sg;
+        ghi = glo + 8;
+        blo = bhi = args.s0;
+      }
+      glo = glo < args.rows ? glo : args.rows - 1;  // rows past the end are zero-filled by TMA
+      ghi = ghi < args.rows ? ghi : args.rows - 1;
+      scale_lo = blo + (static_cast<int64_t>(un.e) * args.rows + glo) * KG;
+      scale_hi = bhi + (static_cast<int64_t>(un.e) * args.rows + ghi) * KG;
+    }
+  };
+  if (it_beg < it_end) {
+    un = decode(u);
+    scale_rows();
+  }
 #pragma unroll
   for (int j = 0; j < kNT; ++j)
 #pragma unroll
@@ -410,17 +429,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kk == 0 && it != it_beg) {  // first stage of the next unit
       ++u;
       un = decode(u);
+      scale_rows();
 #pragma unroll
       for (int j = 0; j < kNT; ++j)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
     }
     const int nt8 = (un.ntok + 7) >> 3;
+    float slo = 1.0f, shi = 1.0f;
+    if constexpr (kInt8) {  // one 128-wide scale group spans two stages
+      slo = __ldg(scale_lo + (kk >> 1));
+      shi = __ldg(scale_hi + (kk >> 1));
+    }
     if (ok && !mbar_wait(&full[stage], phase)) {
       ok = false;
       atomicExch(args.status, kStatusWaitFullTimeout);
     }
-    if (ok) stage_mma_dispatch<kInt8>(nt8, acc, smem + stage * G::kStage, rowLo, rowHi, brow, t);
+    if (ok) stage_mma_dispatch<kInt8>(nt8, acc, smem + stage * G::kStage, rowLo, rowHi, brow, t, slo, shi);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
     if (++stage == G::kStages) {
@@ -446,16 +471,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kNT; ++j)
         if (j < nt8)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) mine[(j * 4 + q) * kConsumerThreads] = acc[j][q];
+          for (int q = 0; q < 4; ++q) mine[(j * 4 + q) * kCT] = acc[j][q];
       __threadfence();
-      named_bar_sync(1, kConsumerThreads);
+      named_bar_sync(1, kCT);
       if (ctid == 0) {
         const int old = atomicAdd(&args.counters[c_first], 1);
         const int last = (old == static_cast<int>(c_last - c_first));
         if (last) args.counters[c_first] = 0;  // leave the counter clean for the next launch
         s_misc[8] = last;
       }
-      named_bar_sync(1, kConsumerThreads);
+      named_bar_sync(1, kCT);
       finish = s_misc[8] != 0;
       if (finish) {
         __threadfence();
@@ -471,16 +496,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kNT; ++j)
             if (j < nt8)
 #pragma unroll
-              for (int q = 0; q < 4; ++q) acc[j][q] += __ldcg(src + (j * 4 + q) * kConsumerThreads);
+              for (int q = 0; q < 4; ++q) acc[j][q] += __ldcg(src + (j * 4 + q) * kCT);
         }
       }
-      named_bar_sync(1, kConsumerThreads);  // s_misc[8] is reused by the next piece
+      named_bar_sync(1, kCT);  // s_misc[8] is reused by the next piece
     }
     if (!finish) continue;
 
     // ---------------- epilogue ----------------
     if constexpr (kGateUp) {
-      const int i = un.rb * 64 + cw * 8 + sg;  // intermediate index of rows g (gate) / g+8 (up)
+      const int i = un.rb * kPairRows + cw * 8 + sg;  // intermediate index of rows g (gate) / g+8 (up)
       if (i < args.rows) {
         __nv_bfloat16* h = static_cast<__nv_bfloat16*>(args.out);
 #pragma unroll
@@ -502,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      const int r_lo = un.rb * 128 + cw * 16 + sg;
+      const int r_lo = un.rb * G::kRowsA + cw * 16 + sg;
       const int r_hi = r_lo + 8;
       float* y = static_cast<float*>(args.out);
 #pragma unroll
