@@ -221,12 +221,12 @@ __global__ void __launch_bounds__(Geometry<kInt8>::kThreads, 1)
     if (kGateUp) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
   }
-  // Everything below reads what earlier kernels wrote.
-  pdl_wait_predecessor();
-  pdl_allow_successor();
-
   // ---- per-CTA schedule tables: active experts, their token blocks, pass prefix
-  // (threads 0..255, i.e. warps 0..7, build them)
+  // (threads 0..255, i.e. warps 0..7, build them). They are read before waiting for the
+  // preceding kernel: every kernel of this library waits for its predecessor before it lets
+  // its successor start, so all work two launches back has completed, and the routing tables
+  // are always at least that far back (moe_ffn_forward's gather, or moe_expert_ffn's leading
+  // memset, sits in between). The token block and h are read only after the wait below.
   int A = *args.num_active;
   A = A < 0 ? 0 : (A > args.E ? args.E : A);
   int passes = 0;
@@ -297,7 +297,55 @@ __global__ void __launch_bounds__(Geometry<kInt8>::kThreads, 1)
     int64_t u = it_beg / KI;
     int kk0 = static_cast<int>(it_beg - u * KI);
     Unit un = it_beg < it_end ? decode(u) : Unit{};
-    for (int64_t it = it_beg; it < it_end && ok;) {
+    auto issue_a = [&](int stg, const Unit& w, int kk) {
+      uint8_t* st = smem + stg * G::kStage;
+      const int k0 = kk * G::kK;
+      if (kGateUp) {
+        tma_load_3d(st, &tmA0, &full[stg], k0, w.rb * kPairRows, w.e, policy);
+        tma_load_3d(st + kPairRows * G::kRowBytes, &tmA1, &full[stg], k0, w.rb * kPairRows, w.e, policy);
+      } else {
+        tma_load_3d(st, &tmA0, &full[stg], k0, w.rb * G::kRowsA, w.e, policy);
+      }
+    };
+    auto issue_b = [&](int stg, const Unit& w, int kk) {
+      uint8_t* sb = smem + stg * G::kStage + kABytes;
+      const int nt8 = (w.ntok + 7) >> 3;
+      for (int j = 0; j < nt8; ++j) tma_load_2d(sb + j * G::kBTileBytes, &tmB, &full[stg], kk * G::kK, w.tok0 + 8 * j);
+    };
+    // The weights do not depend on the preceding kernel: the weight tiles of the first ring's
+    // worth of stages are requested before waiting for it, their token tiles after.
+    const int64_t npre = (it_end - it_beg) < G::kStages ? (it_end - it_beg) : G::kStages;
+    {
+      int64_t pu = u;
+      int pk = kk0;
+      Unit pun = un;
+      for (int64_t q = 0; q < npre; ++q) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[q], kABytes + ((pun.ntok + 7) >> 3) * G::kBTileBytes);
+          issue_a(static_cast<int>(q), pun, pk);
+        }
+        if (++pk == KI && q + 1 < npre) {
+          pk = 0;
+          pun = decode(++pu);
+        }
+      }
+    }
+    pdl_wait_predecessor();
+    pdl_allow_successor();
+    for (int64_t q = 0; q < npre; ++q) {
+      if (lane == 0) issue_b(static_cast<int>(q), un, kk0);
+      ++issued;
+      if (++stage == G::kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+      if (++kk0 == KI) {
+        kk0 = 0;
+        ++u;
+        if (it_beg + q + 1 < it_end) un = decode(u);
+      }
+    }
+    for (int64_t it = it_beg + npre; it < it_end && ok;) {
       const int nt8 = (un.ntok + 7) >> 3;
       // Issue up to kIssueGroup consecutive reduction stages of the same rows back to back,
       // so each weight row is requested as one longer contiguous run.
@@ -323,18 +371,10 @@ __global__ void __launch_bounds__(Geometry<kInt8>::kThreads, 1)
       }
       for (int64_t q = 0; q < n; ++q) {
         const int kk = kk0 + static_cast<int>(q);
-        uint8_t* st = smem + stage * G::kStage;
-        const int k0 = kk * G::kK;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[stage], kABytes + nt8 * G::kBTileBytes);
-          if (kGateUp) {
-            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * kPairRows, un.e, policy);
-            tma_load_3d(st + kPairRows * G::kRowBytes, &tmA1, &full[stage], k0, un.rb * kPairRows, un.e, policy);
-          } else {
-            tma_load_3d(st, &tmA0, &full[stage], k0, un.rb * G::kRowsA, un.e, policy);
-          }
-          uint8_t* sb = st + kABytes;
-          for (int j = 0; j < nt8; ++j) tma_load_2d(sb + j * G::kBTileBytes, &tmB, &full[stage], k0, un.tok0 + 8 * j);
+          issue_a(stage, un, kk);
+          issue_b(stage, un, kk);
         }
         ++issued;
         if (++stage == G::kStages) {
@@ -371,6 +411,9 @@ __global__ void __launch_bounds__(Geometry<kInt8>::kThreads, 1)
   }
 
   // ============================ consumer warps ============================
+  // the stages' token tiles, the row scales and the counters come from earlier kernels
+  pdl_wait_predecessor();
+  pdl_allow_successor();
   const int cw = warp;           // 0 .. kCW-1
   const int ctid = tid;          // 0 .. kCT-1
   const int g = lane >> 2;
