@@ -147,9 +147,9 @@ moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets,
  *   Computes exactly what moe_expert_ffn computes, with the same arguments minus the
  *   workspace; the result may differ from moe_expert_ffn's only in fp32 summation order
  *   when the device has more than 160 SMs.
- *   Scratch: one fixed 32 MiB array inside this library, reserved on every GPU that loads
+ *   Scratch: one fixed 48 MiB array inside this library, reserved on every GPU that loads
  *   the library until the process exits. P * I * 2 bytes (the bf16 intermediate h; for
- *   INT8 weights P * (4 * I + 2 * H + 8) bytes) must fit in about 22 MiB of it; larger
+ *   INT8 weights P * (4 * I + 2 * H + 8) bytes) must fit in about 28 MiB of it; larger
  *   requests return MOE_ERR_WORKSPACE and launch nothing.
  *   All calls share that array and it keeps the last call's contents: calls whose kernels
  *   overlap on one GPU (several streams or host threads) race and give wrong results.

@@ -11,8 +11,8 @@
 
 namespace {
 
-using moe::stream::kMaxCtas;
-using moe::stream::kPartialFloats;
+constexpr int kMaxCtas = moe::kPartialCtas;
+constexpr int kPartialFloats = moe::kPartialSlotFloats;
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }

@@ -9,13 +9,13 @@
 // g_expert_ffn_scratch below, instead of a caller-supplied workspace.
 //
 // Costs and limits, for users:
-//   * Every GPU on which this library is loaded reserves kScratchBytes (32 MiB) for the
+//   * Every GPU on which this library is loaded reserves kScratchBytes (48 MiB) for the
 //     array, from module load until the process exits, whether or not this entry point
 //     is ever called.
 //   * The token block must fit: P * I * 2 bytes of intermediate (BF16 weights), or
 //     P * (4 * I + 2 * H + 8) bytes (INT8 weights: h plus fp16 copies of h and of the token
-//     block with their row scales), at most kHMaxBytes (about 22 MiB; BF16: up to about 5600
-//     rows at I = 2048, or 800 rows at I = 14336); larger requests return MOE_ERR_WORKSPACE
+//     block with their row scales), at most kHMaxBytes (about 28 MiB; BF16: up to about 7100
+//     rows at I = 2048, or 1000 rows at I = 14336); larger requests return MOE_ERR_WORKSPACE
 //     and launch nothing.
 //   * At most kCtas (160) CTAs take part, one per SM, whatever the SM count.
 //   * All calls share the one array, which keeps what the last call left in it. Calls whose
@@ -36,12 +36,12 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(32) << 20;
+constexpr size_t kScratchBytes = size_t(48) << 20;
 constexpr int kCtas = 160;                 // partial-slot capacity
 constexpr size_t kCountersOffset = 256;    // status word at byte 0, counters at 256
-constexpr size_t kZeroBytes = kCountersOffset + 4 * moe::stream::kMaxCtas;
+constexpr size_t kZeroBytes = kCountersOffset + 4 * moe::kPartialCtas;
 constexpr size_t kPartialsOffset = 2048;
-constexpr size_t kPartialsBytes = size_t(kCtas) * 2 * moe::stream::kPartialFloats * sizeof(float);
+constexpr size_t kPartialsBytes = size_t(kCtas) * 2 * moe::kPartialSlotFloats * sizeof(float);
 constexpr size_t kHOffset = kPartialsOffset + kPartialsBytes;
 constexpr size_t kHMaxBytes = kScratchBytes - kHOffset;
 static_assert(kZeroBytes <= kPartialsOffset, "control words overlap the partials");

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "expert_stream.cuh"
+#include "expert_tc.cuh"
 #include "moe_launch.h"
 
 namespace moe {
@@ -28,6 +29,9 @@ TensorMapEncodeFn tensor_map_encoder() {
 
 namespace {
 
+// BF16 expert kernels: tcgen05 with TMEM accumulators (true) or mma.sync (false).
+constexpr bool kBf16OnTensorMemory = true;
+
 // Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage of 64
 // reduction elements by `box_rows` rows of one expert. BF16 rows are 128 bytes per stage and use
 // the 128-byte swizzle; INT8 rows are 64 bytes and are not swizzled.
@@ -44,11 +48,12 @@ bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows,
   return r == CUDA_SUCCESS;
 }
 
-// Token block {K (contiguous), P rows} bf16 or fp16; box = 64 elements x 8 rows; 128-byte swizzle.
-bool encode_tokens(CUtensorMap* map, const void* X, int K, int P, bool fp16 = false) {
+// Token block {K (contiguous), P rows} bf16 or fp16; box = 64 elements x `box_rows` rows;
+// 128-byte swizzle.
+bool encode_tokens(CUtensorMap* map, const void* X, int K, int P, bool fp16 = false, int box_rows = 8) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(P)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box[2] = {64, 8};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = tensor_map_encoder()(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                                     const_cast<void*>(X), dims, strides,
@@ -138,6 +143,59 @@ cudaError_t prepare_kernel() {
   return e;
 }
 
+template <bool kGateUp>
+cudaError_t prepare_tc_kernel() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<bool> done[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::Geo<kGateUp>::kSmem);
+  if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+// BF16 on tcgen05: weight boxes of 128 rows, token boxes of 16 rows.
+cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
+  CUtensorMap tg, tu, td, txg, th;
+  if (!tensor_map_encoder()) return cudaErrorNotSupported;
+  if (!encode_weights(&tg, p.W_gate, false, p.H, p.I, p.E, 128) ||
+      !encode_weights(&tu, p.W_up, false, p.H, p.I, p.E, 128) ||
+      !encode_weights(&td, p.W_down, false, p.I, p.H, p.E, 128) || !encode_tokens(&txg, p.xg, p.H, p.P, false, 16) ||
+      !encode_tokens(&th, p.h, p.I, p.P, false, 16))
+    return cudaErrorInvalidValue;
+  cudaError_t e = prepare_tc_kernel<true>();
+  if (e != cudaSuccess) return e;
+  e = prepare_tc_kernel<false>();
+  if (e != cudaSuccess) return e;
+  tc::Args a{};
+  a.offsets = p.offsets;
+  a.active = p.active;
+  a.num_active = p.num_active;
+  a.partials = p.partials;
+  a.counters = p.counters;
+  a.status = p.status;
+  a.E = p.E;
+  a.P = p.P;
+  tc::Args gu = a;
+  gu.out = p.h;
+  gu.out_ld = p.I;
+  gu.rows = p.I;
+  gu.K = p.H;
+  e = launch_pdl(tc::expert_tc_kernel<true>, dim3(p.num_ctas), dim3(tc::kThreads), tc::Geo<true>::kSmem, s, tg, tu,
+                 txg, gu);
+  if (e != cudaSuccess) return e;
+  tc::Args dn = a;
+  dn.out = p.Y;
+  dn.out_ld = p.H;
+  dn.rows = p.H;
+  dn.K = p.I;
+  return launch_pdl(tc::expert_tc_kernel<false>, dim3(p.num_ctas), dim3(tc::kThreads), tc::Geo<false>::kSmem, s, td,
+                    td, th, dn);
+}
+
 template <bool kInt8>
 cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
   using G = stream::Geometry<kInt8>;
@@ -199,7 +257,8 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream) {
-  return plan.int8 ? launch_both<true>(plan, stream) : launch_both<false>(plan, stream);
+  if (plan.int8) return launch_both<true>(plan, stream);
+  return kBf16OnTensorMemory ? launch_tc(plan, stream) : launch_both<false>(plan, stream);
 }
 
 }  // namespace moe

@@ -37,6 +37,11 @@ cudaError_t launch_gather(const uint16_t* x, int T, int H, int k, const int32_t*
 cudaError_t launch_combine(const float* Y, const int32_t* inv_pos, const float* w, int T, int k, int H,
                            uint16_t* out, int num_sms, cudaStream_t stream);
 
+// fp32 slots per CTA the expert kernels' stream-K partials need (the larger of the two kernel
+// families), and the CTA capacity the workspace provides.
+constexpr int kPartialSlotFloats = 16384;
+constexpr int kPartialCtas = 256;
+
 // Grouped expert FFN (gate+up then down) over an expert-sorted token block.
 struct ExpertFfnPlan {
   const uint16_t* xg;  // [P, H]
