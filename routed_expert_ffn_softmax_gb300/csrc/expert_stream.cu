@@ -29,21 +29,23 @@ TensorMapEncodeFn tensor_map_encoder() {
 
 namespace {
 
-// BF16 expert kernels: tcgen05 with TMEM accumulators (true) or mma.sync (false).
-constexpr bool kBf16OnTensorMemory = true;
+// Expert kernels: tcgen05 with TMEM accumulators (true) or mma.sync (false).
+constexpr bool kOnTensorMemory = true;
 
-// Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage of 64
-// reduction elements by `box_rows` rows of one expert. BF16 rows are 128 bytes per stage and use
-// the 128-byte swizzle; INT8 rows are 64 bytes and are not swizzled.
-bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows, int E, int box_rows) {
+// Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage of
+// reduction elements by `box_rows` rows of one expert. BF16 rows are 64 elements (128 bytes) per
+// stage and use the 128-byte swizzle; INT8 rows are 64 bytes, not swizzled, for the mma.sync
+// kernels, and 128 bytes (one scale group) with the 128-byte swizzle for the tcgen05 kernels.
+bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows, int E, int box_rows,
+                    bool int8_swizzled = false) {
   const cuuint64_t eb = int8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(E)};
   cuuint64_t strides[2] = {K * eb, static_cast<cuuint64_t>(K) * rows * eb};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {(int8 && int8_swizzled) ? 128u : 64u, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = tensor_map_encoder()(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                                     const_cast<void*>(W), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                                    (int8 && !int8_swizzled) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -143,7 +145,7 @@ cudaError_t prepare_kernel() {
   return e;
 }
 
-template <bool kGateUp>
+template <bool kInt8, bool kGateUp>
 cudaError_t prepare_tc_kernel() {
   constexpr int kMaxDev = 64;
   static std::atomic<bool> done[kMaxDev];
@@ -151,24 +153,29 @@ cudaError_t prepare_tc_kernel() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::Geo<kGateUp>::kSmem);
+  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kInt8, kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::Geo<kInt8, kGateUp>::kSmem);
   if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
-// BF16 on tcgen05: weight boxes of 128 rows, token boxes of 16 rows.
+// tcgen05 kernels: weight boxes of 128 rows by 128 bytes, token boxes of 16 rows. INT8 first
+// makes the fp16 token copy (and, between the two kernels, the fp16 copy of h).
+template <bool kInt8>
 cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
+  using GU = tc::Geo<kInt8, true>;
+  using DN = tc::Geo<kInt8, false>;
   CUtensorMap tg, tu, td, txg, th;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
-  if (!encode_weights(&tg, p.W_gate, false, p.H, p.I, p.E, 128) ||
-      !encode_weights(&tu, p.W_up, false, p.H, p.I, p.E, 128) ||
-      !encode_weights(&td, p.W_down, false, p.I, p.H, p.E, 128) || !encode_tokens(&txg, p.xg, p.H, p.P, false, 16) ||
-      !encode_tokens(&th, p.h, p.I, p.P, false, 16))
+  if (!encode_weights(&tg, p.W_gate, kInt8, p.H, p.I, p.E, 128, true) ||
+      !encode_weights(&tu, p.W_up, kInt8, p.H, p.I, p.E, 128, true) ||
+      !encode_weights(&td, p.W_down, kInt8, p.I, p.H, p.E, 128, true) ||
+      !encode_tokens(&txg, kInt8 ? p.xg16 : p.xg, p.H, p.P, kInt8, 16) ||
+      !encode_tokens(&th, kInt8 ? p.h16 : p.h, p.I, p.P, kInt8, 16))
     return cudaErrorInvalidValue;
-  cudaError_t e = prepare_tc_kernel<true>();
+  cudaError_t e = prepare_tc_kernel<kInt8, true>();
   if (e != cudaSuccess) return e;
-  e = prepare_tc_kernel<false>();
+  e = prepare_tc_kernel<kInt8, false>();
   if (e != cudaSuccess) return e;
   tc::Args a{};
   a.offsets = p.offsets;
@@ -179,20 +186,34 @@ cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
   a.status = p.status;
   a.E = p.E;
   a.P = p.P;
+  if (kInt8) {
+    e = launch_rows_to_f16(p.xg, p.H, p.P, p.xg16, p.xg_scale, p.num_ctas, s);
+    if (e != cudaSuccess) return e;
+  }
   tc::Args gu = a;
   gu.out = p.h;
   gu.out_ld = p.I;
   gu.rows = p.I;
   gu.K = p.H;
-  e = launch_pdl(tc::expert_tc_kernel<true>, dim3(p.num_ctas), dim3(tc::kThreads), tc::Geo<true>::kSmem, s, tg, tu,
+  gu.s0 = p.s_gate;
+  gu.s1 = p.s_up;
+  gu.row_scale = p.xg_scale;
+  e = launch_pdl(tc::expert_tc_kernel<kInt8, true>, dim3(p.num_ctas), dim3(GU::kThreads), GU::kSmem, s, tg, tu,
                  txg, gu);
   if (e != cudaSuccess) return e;
+  if (kInt8) {
+    e = launch_rows_to_f16(p.h, p.I, p.P, p.h16, p.h_scale, p.num_ctas, s);
+    if (e != cudaSuccess) return e;
+  }
   tc::Args dn = a;
   dn.out = p.Y;
   dn.out_ld = p.H;
   dn.rows = p.H;
   dn.K = p.I;
-  return launch_pdl(tc::expert_tc_kernel<false>, dim3(p.num_ctas), dim3(tc::kThreads), tc::Geo<false>::kSmem, s, td,
+  dn.s0 = p.s_down;
+  dn.s1 = p.s_down;
+  dn.row_scale = p.h_scale;
+  return launch_pdl(tc::expert_tc_kernel<kInt8, false>, dim3(p.num_ctas), dim3(DN::kThreads), DN::kSmem, s, td,
                     td, th, dn);
 }
 
@@ -257,8 +278,8 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream) {
-  if (plan.int8) return launch_both<true>(plan, stream);
-  return kBf16OnTensorMemory ? launch_tc(plan, stream) : launch_both<false>(plan, stream);
+  if (kOnTensorMemory) return plan.int8 ? launch_tc<true>(plan, stream) : launch_tc<false>(plan, stream);
+  return plan.int8 ? launch_both<true>(plan, stream) : launch_both<false>(plan, stream);
 }
 
 }  // namespace moe
