@@ -37,7 +37,7 @@ namespace tc {
 
 constexpr int kEpiThreads = 128;    // warps 2..5
 constexpr int kTable = 256;
-constexpr int kIssueGroup = 4;
+constexpr int kIssueGroup = 1;  // stages issued per producer wake-up: each as soon as its slot drains
 constexpr int kPartialFloats = 16384;  // one CTA slot: 128 rows x 128 accumulator columns
 constexpr int kConvWarp0 = 6;          // first INT8 converter warp
 constexpr int kConvWarps = 8;
@@ -617,7 +617,9 @@ __global__ void __launch_bounds__(Geo<kInt8, kGateUp>::kThreads, 1)
           }
           tc_fence_after_sync();
         }
-        if (ok && !mbar_wait(&full[stage], phase)) {
+        // INT8: the converters arrive on a_full after they saw the stage land, so that wait also
+        // covers the token tile the MMAs read
+        if (!kInt8 && ok && !mbar_wait(&full[stage], phase)) {
           ok = false;
           atomicExch(args.status, kStatusWaitFullTimeout);
         }
