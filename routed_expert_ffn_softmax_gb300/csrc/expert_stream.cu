@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "expert_pair.cuh"
 #include "expert_stream.cuh"
 #include "expert_tc.cuh"
 #include "moe_launch.h"
@@ -217,6 +218,130 @@ cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
                     td, th, dn);
 }
 
+// ---- INT8 on CTA pairs
+template <bool kGateUp>
+cudaError_t prepare_pair_kernel() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<bool> done[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(pair::expert_pair_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           pair::Geo<kGateUp>::kSmem);
+  if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+// Pairs of the pair kernel that can be resident at once on this device (a persistent stream-K
+// grid must not be larger, or the late pairs would run after the others instead of beside them).
+template <bool kGateUp>
+cudaError_t resident_pairs(int* pairs) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDev) {
+    const int c = cache[dev].load(std::memory_order_acquire);
+    if (c > 0) {
+      *pairs = c;
+      return cudaSuccess;
+    }
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kPartialCtas);
+  cfg.blockDim = dim3(pair::kThreads);
+  cfg.dynamicSmemBytes = pair::Geo<kGateUp>::kSmem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, pair::expert_pair_kernel<kGateUp>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorNotSupported;
+  if (dev < kMaxDev) cache[dev].store(n, std::memory_order_release);
+  *pairs = n;
+  return cudaSuccess;
+}
+
+// Launch on `pairs` clusters of two CTAs, with programmatic dependent launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pairs_pdl(void (*kernel)(KArgs...), int pairs, size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(pair::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// INT8: fp16 token copy, gate+up on pairs, fp16 copy of h, down on pairs. Weight boxes are one
+// CTA's 128 rows by 128 bytes; token boxes are 8 rows (a CTA holds half of a pass's tokens).
+cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
+  CUtensorMap tg, tu, td, txg, th;
+  if (!tensor_map_encoder()) return cudaErrorNotSupported;
+  if (!encode_weights(&tg, p.W_gate, true, p.H, p.I, p.E, 128, true) ||
+      !encode_weights(&tu, p.W_up, true, p.H, p.I, p.E, 128, true) ||
+      !encode_weights(&td, p.W_down, true, p.I, p.H, p.E, 128, true) ||
+      !encode_tokens(&txg, p.xg16, p.H, p.P, true, 8) || !encode_tokens(&th, p.h16, p.I, p.P, true, 8))
+    return cudaErrorInvalidValue;
+  cudaError_t e = prepare_pair_kernel<true>();
+  if (e == cudaSuccess) e = prepare_pair_kernel<false>();
+  int pairs_gu = 0, pairs_dn = 0;
+  if (e == cudaSuccess) e = resident_pairs<true>(&pairs_gu);
+  if (e == cudaSuccess) e = resident_pairs<false>(&pairs_dn);
+  if (e != cudaSuccess) return e;
+  const int max_pairs = p.num_ctas / 2 > 0 ? p.num_ctas / 2 : 1;
+  pairs_gu = pairs_gu < max_pairs ? pairs_gu : max_pairs;
+  pairs_dn = pairs_dn < max_pairs ? pairs_dn : max_pairs;
+  tc::Args a{};
+  a.offsets = p.offsets;
+  a.active = p.active;
+  a.num_active = p.num_active;
+  a.partials = p.partials;
+  a.counters = p.counters;
+  a.status = p.status;
+  a.E = p.E;
+  a.P = p.P;
+  e = launch_rows_to_f16(p.xg, p.H, p.P, p.xg16, p.xg_scale, p.num_ctas, s);
+  if (e != cudaSuccess) return e;
+  tc::Args gu = a;
+  gu.out = p.h;
+  gu.out_ld = p.I;
+  gu.rows = p.I;
+  gu.K = p.H;
+  gu.s0 = p.s_gate;
+  gu.s1 = p.s_up;
+  gu.row_scale = p.xg_scale;
+  e = launch_pairs_pdl(pair::expert_pair_kernel<true>, pairs_gu, pair::Geo<true>::kSmem, s, tg, tu, txg, gu);
+  if (e != cudaSuccess) return e;
+  e = launch_rows_to_f16(p.h, p.I, p.P, p.h16, p.h_scale, p.num_ctas, s);
+  if (e != cudaSuccess) return e;
+  tc::Args dn = a;
+  dn.out = p.Y;
+  dn.out_ld = p.H;
+  dn.rows = p.H;
+  dn.K = p.I;
+  dn.s0 = p.s_down;
+  dn.s1 = p.s_down;
+  dn.row_scale = p.h_scale;
+  return launch_pairs_pdl(pair::expert_pair_kernel<false>, pairs_dn, pair::Geo<false>::kSmem, s, td, td, th, dn);
+}
+
 template <bool kInt8>
 cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
   using G = stream::Geometry<kInt8>;
@@ -278,7 +403,7 @@ cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream) {
-  if (kOnTensorMemory) return plan.int8 ? launch_tc<true>(plan, stream) : launch_tc<false>(plan, stream);
+  if (kOnTensorMemory) return plan.int8 ? launch_pair_int8(plan, stream) : launch_tc<false>(plan, stream);
   return plan.int8 ? launch_both<true>(plan, stream) : launch_both<false>(plan, stream);
 }
 
