@@ -13,10 +13,12 @@
 // Work: a cluster of two CTAs (rank 0 = even, rank 1 = odd) takes a stream-K range of
 // (expert pass, 256-row block) x stages; CTA `rank` holds rows 128 * rank .. 128 * rank + 127 of
 // the block and token rows npad / 2 * rank .. of the pass (the pair MMA reads B half from each
-// CTA's shared memory and writes each CTA's 128 rows of D into its own TMEM).
+// CTA's shared memory and writes each CTA's 128 rows of D into its own TMEM). A stage holds two
+// 16 KB weight tiles per CTA: gate and up of one scale group (gate+up), or two consecutive scale
+// groups of the down rows (down), so both kernels move the same bytes per hand-off.
 // Per CTA (15 warps):
 //   warp 0      TMA producer for this CTA's weight rows and token rows;
-//   warps 1, 14 MMA issuers, even CTA only (gate / up, or the first / second half of a down stage),
+//   warps 1, 14 MMA issuers, even CTA only (gate / up, or the first / second group of a down stage),
 //               committing to the barriers of both CTAs; warp 1 also allocates the pair's TMEM;
 //   warps 2-5   scale promotion and epilogue for this CTA's rows;
 //   warps 6-13  converters for this CTA's rows.
@@ -49,15 +51,17 @@ constexpr int kScaleLook = 4;      // group scales are fetched this many stages 
 template <bool kGateUp>
 struct Geo {
   static constexpr bool kGU = kGateUp;
-  static constexpr int kWBytes = kGateUp ? 32768 : 16384;  // this CTA's weight bytes per stage
+  static constexpr int kKStage = kGateUp ? 128 : 256;       // reduction elements per stage
+  static constexpr int kWBytes = 32768;                     // this CTA's two weight tiles per stage
   static constexpr int kBRows = kNMax / 2;                  // token rows per CTA
-  static constexpr int kBHalf = kBRows * 128;               // one 64-element half of the token tile
-  static constexpr int kBBytes = 2 * kBHalf;
+  static constexpr int kBHalf = kBRows * 128;               // one 64-element slice of the token tile
+  static constexpr int kBHalves = kKStage / 64;
+  static constexpr int kBBytes = kBHalves * kBHalf;
   static constexpr int kStage = kWBytes + kBBytes;
-  static constexpr int kStages = kGateUp ? 5 : 9;
-  static constexpr int kAccCols = 2 * kNMax;                // gate | up, or the two issuers' halves
+  static constexpr int kStages = 5;
+  static constexpr int kAccCols = 2 * kNMax;                // the two issuers' accumulators
   static constexpr int kABase = 2 * kAccCols;               // operand buffers after two accumulators
-  static constexpr int kACols = kGateUp ? 128 : 64;
+  static constexpr int kACols = 128;                        // two tiles x 128 elements (fp16 pairs)
   static constexpr int kAFit = (512 - kABase) / kACols;
   static constexpr int kABufs = kAFit < kStages ? kAFit : kStages;
   static constexpr int kBarBytes = (2 * kStages + 4 + 2 * kABufs) * 8;
@@ -72,8 +76,8 @@ struct Geo {
 };
 
 // Converters: this thread's weight row of every stage -> exact fp16 in the next TMEM operand
-// buffer (gate+up: warps 6-9 gate, 10-13 up, whole rows; down: warps 6-9 the first 64 bytes,
-// 10-13 the last 64); then tell the even CTA's issuers.
+// buffer (warps 6-9 the first tile, 10-13 the second, whole 128-byte rows); then tell the even
+// CTA's issuers.
 template <typename G>
 __device__ __forceinline__ void convert(const uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* a_full,
                                         uint64_t* a_empty, uint64_t* d_empty, uint32_t tmem_base, uint32_t rank,
@@ -84,7 +88,7 @@ __device__ __forceinline__ void convert(const uint8_t* smem, uint64_t* full, uin
   const int lane = threadIdx.x & 31;
   const int quarter = warp & 3;               // TMEM lane quarter this warp may access
   const int r = quarter * 32 + lane;          // weight row within this CTA's 128 = TMEM lane
-  const int part = (warp - kConvWarp0) >> 2;  // gate+up: gate / up; down: first / last half
+  const int part = (warp - kConvWarp0) >> 2;  // first / second tile of the stage
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
   bool ok = true;
   int stage = 0, ab = 0, db = 0;
@@ -96,10 +100,10 @@ __device__ __forceinline__ void convert(const uint8_t* smem, uint64_t* full, uin
     ok = __all_sync(0xffffffffu, ok);  // keep the warp-wide TMEM stores uniform
     tc_fence_after_sync();
     if (ok) {
-      const uint8_t* rowp = smem + stage * G::kStage + (G::kGU ? part * 16384 : 0) + r * 128;
+      const uint8_t* rowp = smem + stage * G::kStage + part * 16384 + r * 128;
 #pragma unroll
-      for (int h = 0; h < (G::kGU ? 2 : 1); ++h) {
-        const int c0 = G::kGU ? 4 * h : 4 * part;  // first 16-byte chunk (128B swizzle below)
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = 4 * h;  // first 16-byte chunk of this half (128B swizzle below)
         uint32_t o[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -109,7 +113,7 @@ __device__ __forceinline__ void convert(const uint8_t* smem, uint64_t* full, uin
           int8x4_to_f16x2x2(v.z, o[8 * i + 4], o[8 * i + 5]);
           int8x4_to_f16x2x2(v.w, o[8 * i + 6], o[8 * i + 7]);
         }
-        const int col = G::kABase + ab * G::kACols + (G::kGU ? part * 64 + 32 * h : 32 * part);
+        const int col = G::kABase + ab * G::kACols + part * 64 + 32 * h;
         tmem_st32(lane_base + col, o);
       }
     }
@@ -155,10 +159,12 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
   int kk = static_cast<int>(it_beg - u * KI);
   Unit un{};
   if (it_beg < it_end) un = decode(u);
-  // gate+up: issuer 0 the gate rows, 1 the up rows, all 8 steps; down: steps 4 * which .. + 3
-  constexpr int kSteps = G::kGU ? 8 : 4;
-  const int s0 = G::kGU ? 0 : 4 * which;
-  const uint32_t a_off = G::kABase + (G::kGU ? 64 * which : 0);
+  // issuer `which` multiplies tile `which` (gate / up, or the first / second scale group) by the
+  // token tile: 8 steps of 16 elements; gate and up share the stage's 128 token columns, the two
+  // down groups take columns 0..127 and 128..255
+  constexpr int kSteps = 8;
+  const int s0 = G::kGU ? 0 : 8 * which;
+  const uint32_t a_off = G::kABase + 64 * which;
 #pragma unroll 1
   for (int64_t it = it_beg; it < it_end; ++it) {
     if (kk == 0 && it != it_beg) un = decode(++u);
@@ -174,8 +180,8 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
       const uint64_t bdesc = umma_desc_sw128(smem_base + stage * G::kStage + G::kWBytes);
 #pragma unroll
       for (int q = 0; q < kSteps; ++q) {
-        const int s = s0 + q;  // 16-element step within the stage
-        umma_f16_pair_tmem_a(d, a + 8 * s, bdesc + (((s >> 2) * G::kBHalf + 32 * (s & 3)) >> 4), idesc, q != 0);
+        const int s = s0 + q;  // 16-element step of the token tile
+        umma_f16_pair_tmem_a(d, a + 8 * q, bdesc + (((s >> 2) * G::kBHalf + 32 * (s & 3)) >> 4), idesc, q != 0);
       }
     }
     umma_commit_pair(&empty[stage]);  // both CTAs' stages are free once these MMAs have read them
@@ -231,8 +237,14 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
         l0 = args.s0 + off;
         l1 = args.s1 + off;
       }
-      cp_async_4(ring + (put * 2) * kEpiThreads, l0 + lk);
-      if (G::kGU) cp_async_4(ring + (put * 2 + 1) * kEpiThreads, l1 + lk);
+      if constexpr (G::kGU) {  // gate and up scales of group lk
+        cp_async_4(ring + (put * 2) * kEpiThreads, l0 + lk);
+        cp_async_4(ring + (put * 2 + 1) * kEpiThreads, l1 + lk);
+      } else {  // down scales of groups 2 lk and 2 lk + 1 (none past the row's end)
+        cp_async_4(ring + (put * 2) * kEpiThreads, l0 + 2 * lk);
+        if (2 * lk + 1 < KG) cp_async_4(ring + (put * 2 + 1) * kEpiThreads, l0 + 2 * lk + 1);
+        else ring[(put * 2 + 1) * kEpiThreads] = 0.0f;
+      }
       if (++lk == KI) {
         lk = 0;
         ++lu;
@@ -288,7 +300,7 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
     fetch_next(it + kScaleLook);
     cp_async_wait<kScaleLook>();
     const float s0 = ring[(get * 2) * kEpiThreads];
-    const float s1 = G::kGU ? ring[(get * 2 + 1) * kEpiThreads] : 0.0f;
+    const float s1 = ring[(get * 2 + 1) * kEpiThreads];
     if (++get == kRing) get = 0;
     // the issuers' operand-free commit for this stage: its MMAs, and so its group sums, are done
     if (ok && !mbar_wait(&a_empty[ab], aph)) atomicExch(args.status, kStatusWaitFullTimeout), ok = false;
@@ -307,8 +319,8 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
           if constexpr (G::kGU) {
             acc0[16 * c + j] = fmaf(s0, g[j], acc0[16 * c + j]);
             acc1[16 * c + j] = fmaf(s1, v[j], acc1[16 * c + j]);
-          } else {  // down: the two issuers' halves of the group
-            acc0[16 * c + j] = fmaf(s0, g[j] + v[j], acc0[16 * c + j]);
+          } else {  // down: the stage's two scale groups
+            acc0[16 * c + j] = fmaf(s1, v[j], fmaf(s0, g[j], acc0[16 * c + j]));
           }
         }
       }
@@ -474,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int RB = (args.rows + 255) / 256;
-  const int KI = args.K / 128;
+  const int KI = (args.K + G::kKStage - 1) / G::kKStage;
   const int64_t W = static_cast<int64_t>(t_pp[A]) * RB * KI;
   const int64_t pairs = gridDim.x / 2;
   const int64_t NC = W < pairs ? W : pairs;
@@ -507,20 +519,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      auto bbytes = [](const Unit& w) { return 2 * (((w.ntok + 15) >> 4) * 8) * 128; };
+      auto bbytes = [](const Unit& w) { return G::kBHalves * (((w.ntok + 15) >> 4) * 8) * 128; };
       auto issue_a = [&](int stg, const Unit& w, int kk) {
         uint8_t* st = smem + stg * G::kStage;
         const int row0 = w.rb * 256 + 128 * static_cast<int>(rank);
-        tma_load_3d(st, &tmA0, &full[stg], kk * 128, row0, w.e, policy);
-        if (kGateUp) tma_load_3d(st + 16384, &tmA1, &full[stg], kk * 128, row0, w.e, policy);
+        if (kGateUp) {
+          tma_load_3d(st, &tmA0, &full[stg], kk * 128, row0, w.e, policy);
+          tma_load_3d(st + 16384, &tmA1, &full[stg], kk * 128, row0, w.e, policy);
+        } else {  // groups 2 kk and 2 kk + 1 (zero-filled past the row's end)
+          tma_load_3d(st, &tmA0, &full[stg], kk * 256, row0, w.e, policy);
+          tma_load_3d(st + 16384, &tmA0, &full[stg], kk * 256 + 128, row0, w.e, policy);
+        }
       };
       auto issue_b = [&](int stg, const Unit& w, int kk) {
         uint8_t* sb = smem + stg * G::kStage + G::kWBytes;
         const int half_rows = ((w.ntok + 15) >> 4) * 8;  // this CTA's token rows: npad / 2
         const int t0 = w.tok0 + half_rows * static_cast<int>(rank);
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < G::kBHalves; ++h)
           for (int j = 0; j < half_rows; j += 8)
-            tma_load_2d(sb + h * G::kBHalf + j * 128, &tmB, &full[stg], kk * 128 + 64 * h, t0 + j);
+            tma_load_2d(sb + h * G::kBHalf + j * 128, &tmB, &full[stg], kk * G::kKStage + 64 * h, t0 + j);
       };
       int64_t u = it_beg / KI;
       int kk0 = static_cast<int>(it_beg - u * KI);
