@@ -6,7 +6,6 @@
 #include <cstdint>
 
 #include "moe.h"
-#include "expert_stream.cuh"
 #include "moe_launch.h"
 
 namespace {

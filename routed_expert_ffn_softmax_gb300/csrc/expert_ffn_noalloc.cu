@@ -30,7 +30,6 @@
 #include <cstdint>
 #include <mutex>
 
-#include "expert_stream.cuh"
 #include "moe.h"
 #include "moe_launch.h"
 

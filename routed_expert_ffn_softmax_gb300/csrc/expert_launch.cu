@@ -1,4 +1,5 @@
-// Host side of the weight-streaming expert kernels: TMA descriptors and launches.
+// Host side of the expert kernels: TMA descriptors and launches (BF16: expert_tc.cuh on single
+// CTAs; INT8: expert_pair.cuh on CTA pairs, after an fp16 copy of the token rows).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -8,7 +9,6 @@
 #include <mutex>
 
 #include "expert_pair.cuh"
-#include "expert_stream.cuh"
 #include "expert_tc.cuh"
 #include "moe_launch.h"
 
@@ -30,23 +30,18 @@ TensorMapEncodeFn tensor_map_encoder() {
 
 namespace {
 
-// Expert kernels: tcgen05 with TMEM accumulators (true) or mma.sync (false).
-constexpr bool kOnTensorMemory = true;
-
-// Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage of
-// reduction elements by `box_rows` rows of one expert. BF16 rows are 64 elements (128 bytes) per
-// stage and use the 128-byte swizzle; INT8 rows are 64 bytes, not swizzled, for the mma.sync
-// kernels, and 128 bytes (one scale group) with the 128-byte swizzle for the tcgen05 kernels.
-bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows, int E, int box_rows,
-                    bool int8_swizzled = false) {
+// Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage's 128 bytes of
+// `box_rows` rows of one expert (64 bf16 or 128 int8 elements, one INT8 scale group), with the
+// 128-byte swizzle the MMA descriptors and the converters expect.
+bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows, int E, int box_rows) {
   const cuuint64_t eb = int8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(E)};
   cuuint64_t strides[2] = {K * eb, static_cast<cuuint64_t>(K) * rows * eb};
-  cuuint32_t box[3] = {(int8 && int8_swizzled) ? 128u : 64u, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {int8 ? 128u : 64u, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = tensor_map_encoder()(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                                     const_cast<void*>(W), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    (int8 && !int8_swizzled) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_SWIZZLE_128B,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -131,22 +126,7 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, int K, int P, uint16_t* dst,
                     K / 8, static_cast<int64_t>(P), reinterpret_cast<uint4*>(dst), row_scale);
 }
 
-template <bool kInt8, bool kGateUp>
-cudaError_t prepare_kernel() {
-  // the dynamic shared-memory opt-in is per device
-  constexpr int kMaxDev = 64;
-  static std::atomic<bool> done[kMaxDev];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(stream::expert_stream_kernel<kInt8, kGateUp>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, stream::Geometry<kInt8>::kSmem);
-  if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
-  return e;
-}
-
-template <bool kInt8, bool kGateUp>
+template <bool kGateUp>
 cudaError_t prepare_tc_kernel() {
   constexpr int kMaxDev = 64;
   static std::atomic<bool> done[kMaxDev];
@@ -154,29 +134,24 @@ cudaError_t prepare_tc_kernel() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kInt8, kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::Geo<kInt8, kGateUp>::kSmem);
+  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::Geo<kGateUp>::kSmem);
   if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
-// tcgen05 kernels: weight boxes of 128 rows by 128 bytes, token boxes of 16 rows. INT8 first
-// makes the fp16 token copy (and, between the two kernels, the fp16 copy of h).
-template <bool kInt8>
+// BF16: weight boxes of 128 rows by 128 bytes, token boxes of 16 rows.
 cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
-  using GU = tc::Geo<kInt8, true>;
-  using DN = tc::Geo<kInt8, false>;
   CUtensorMap tg, tu, td, txg, th;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
-  if (!encode_weights(&tg, p.W_gate, kInt8, p.H, p.I, p.E, 128, true) ||
-      !encode_weights(&tu, p.W_up, kInt8, p.H, p.I, p.E, 128, true) ||
-      !encode_weights(&td, p.W_down, kInt8, p.I, p.H, p.E, 128, true) ||
-      !encode_tokens(&txg, kInt8 ? p.xg16 : p.xg, p.H, p.P, kInt8, 16) ||
-      !encode_tokens(&th, kInt8 ? p.h16 : p.h, p.I, p.P, kInt8, 16))
+  if (!encode_weights(&tg, p.W_gate, false, p.H, p.I, p.E, 128) ||
+      !encode_weights(&tu, p.W_up, false, p.H, p.I, p.E, 128) ||
+      !encode_weights(&td, p.W_down, false, p.I, p.H, p.E, 128) || !encode_tokens(&txg, p.xg, p.H, p.P, false, 16) ||
+      !encode_tokens(&th, p.h, p.I, p.P, false, 16))
     return cudaErrorInvalidValue;
-  cudaError_t e = prepare_tc_kernel<kInt8, true>();
+  cudaError_t e = prepare_tc_kernel<true>();
   if (e != cudaSuccess) return e;
-  e = prepare_tc_kernel<kInt8, false>();
+  e = prepare_tc_kernel<false>();
   if (e != cudaSuccess) return e;
   tc::Args a{};
   a.offsets = p.offsets;
@@ -187,35 +162,21 @@ cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
   a.status = p.status;
   a.E = p.E;
   a.P = p.P;
-  if (kInt8) {
-    e = launch_rows_to_f16(p.xg, p.H, p.P, p.xg16, p.xg_scale, p.num_ctas, s);
-    if (e != cudaSuccess) return e;
-  }
   tc::Args gu = a;
   gu.out = p.h;
   gu.out_ld = p.I;
   gu.rows = p.I;
   gu.K = p.H;
-  gu.s0 = p.s_gate;
-  gu.s1 = p.s_up;
-  gu.row_scale = p.xg_scale;
-  e = launch_pdl(tc::expert_tc_kernel<kInt8, true>, dim3(p.num_ctas), dim3(GU::kThreads), GU::kSmem, s, tg, tu,
-                 txg, gu);
+  e = launch_pdl(tc::expert_tc_kernel<true>, dim3(p.num_ctas), dim3(tc::Geo<true>::kThreads), tc::Geo<true>::kSmem,
+                 s, tg, tu, txg, gu);
   if (e != cudaSuccess) return e;
-  if (kInt8) {
-    e = launch_rows_to_f16(p.h, p.I, p.P, p.h16, p.h_scale, p.num_ctas, s);
-    if (e != cudaSuccess) return e;
-  }
   tc::Args dn = a;
   dn.out = p.Y;
   dn.out_ld = p.H;
   dn.rows = p.H;
   dn.K = p.I;
-  dn.s0 = p.s_down;
-  dn.s1 = p.s_down;
-  dn.row_scale = p.h_scale;
-  return launch_pdl(tc::expert_tc_kernel<kInt8, false>, dim3(p.num_ctas), dim3(DN::kThreads), DN::kSmem, s, td,
-                    td, th, dn);
+  return launch_pdl(tc::expert_tc_kernel<false>, dim3(p.num_ctas), dim3(tc::Geo<false>::kThreads),
+                    tc::Geo<false>::kSmem, s, td, td, th, dn);
 }
 
 // ---- INT8 on CTA pairs
@@ -294,9 +255,9 @@ cudaError_t launch_pairs_pdl(void (*kernel)(KArgs...), int pairs, size_t smem, c
 cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
   CUtensorMap tg, tu, td, txg, th;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
-  if (!encode_weights(&tg, p.W_gate, true, p.H, p.I, p.E, 128, true) ||
-      !encode_weights(&tu, p.W_up, true, p.H, p.I, p.E, 128, true) ||
-      !encode_weights(&td, p.W_down, true, p.I, p.H, p.E, 128, true) ||
+  if (!encode_weights(&tg, p.W_gate, true, p.H, p.I, p.E, 128) ||
+      !encode_weights(&tu, p.W_up, true, p.H, p.I, p.E, 128) ||
+      !encode_weights(&td, p.W_down, true, p.I, p.H, p.E, 128) ||
       !encode_tokens(&txg, p.xg16, p.H, p.P, true, 8) || !encode_tokens(&th, p.h16, p.I, p.P, true, 8))
     return cudaErrorInvalidValue;
   cudaError_t e = prepare_pair_kernel<true>();
@@ -342,69 +303,10 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
   return launch_pairs_pdl(pair::expert_pair_kernel<false>, pairs_dn, pair::Geo<false>::kSmem, s, td, td, th, dn);
 }
 
-template <bool kInt8>
-cudaError_t launch_both(const ExpertFfnPlan& p, cudaStream_t s) {
-  using G = stream::Geometry<kInt8>;
-  CUtensorMap tg, tu, td, txg, th;
-  if (!tensor_map_encoder()) return cudaErrorNotSupported;
-  if (!encode_weights(&tg, p.W_gate, kInt8, p.H, p.I, p.E, G::kRowsA / 2) ||
-      !encode_weights(&tu, p.W_up, kInt8, p.H, p.I, p.E, G::kRowsA / 2) ||
-      !encode_weights(&td, p.W_down, kInt8, p.I, p.H, p.E, G::kRowsA) ||
-      !encode_tokens(&txg, kInt8 ? p.xg16 : p.xg, p.H, p.P, kInt8) ||
-      !encode_tokens(&th, kInt8 ? p.h16 : p.h, p.I, p.P, kInt8))
-    return cudaErrorInvalidValue;
-  cudaError_t e = prepare_kernel<kInt8, true>();
-  if (e != cudaSuccess) return e;
-  e = prepare_kernel<kInt8, false>();
-  if (e != cudaSuccess) return e;
-
-  stream::Args a{};
-  a.offsets = p.offsets;
-  a.active = p.active;
-  a.num_active = p.num_active;
-  a.partials = p.partials;
-  a.counters = p.counters;
-  a.status = p.status;
-  a.E = p.E;
-  a.P = p.P;
-
-  if (kInt8) {
-    e = launch_rows_to_f16(p.xg, p.H, p.P, p.xg16, p.xg_scale, p.num_ctas, s);
-    if (e != cudaSuccess) return e;
-  }
-  stream::Args gu = a;
-  gu.row_scale = p.xg_scale;
-  gu.s0 = p.s_gate;
-  gu.s1 = p.s_up;
-  gu.out = p.h;
-  gu.out_ld = p.I;
-  gu.rows = p.I;
-  gu.K = p.H;
-  e = launch_pdl(stream::expert_stream_kernel<kInt8, true>, dim3(p.num_ctas), dim3(G::kThreads), G::kSmem, s,
-                 tg, tu, txg, gu);
-  if (e != cudaSuccess) return e;
-
-  if (kInt8) {
-    e = launch_rows_to_f16(p.h, p.I, p.P, p.h16, p.h_scale, p.num_ctas, s);
-    if (e != cudaSuccess) return e;
-  }
-  stream::Args dn = a;
-  dn.row_scale = p.h_scale;
-  dn.s0 = p.s_down;
-  dn.s1 = p.s_down;
-  dn.out = p.Y;
-  dn.out_ld = p.H;
-  dn.rows = p.H;
-  dn.K = p.I;
-  return launch_pdl(stream::expert_stream_kernel<kInt8, false>, dim3(p.num_ctas), dim3(G::kThreads), G::kSmem,
-                    s, td, td, th, dn);
-}
-
 }  // namespace
 
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream) {
-  if (kOnTensorMemory) return plan.int8 ? launch_pair_int8(plan, stream) : launch_tc<false>(plan, stream);
-  return plan.int8 ? launch_both<true>(plan, stream) : launch_both<false>(plan, stream);
+  return plan.int8 ? launch_pair_int8(plan, stream) : launch_tc(plan, stream);
 }
 
 }  // namespace moe

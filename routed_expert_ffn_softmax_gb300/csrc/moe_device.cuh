@@ -119,12 +119,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
-// The mbarrier receives one arrival once this thread's earlier cp.async copies land
-// (the arrival is counted in the barrier's expected count: .noinc).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // ---------------------------------------------------------------- PDL
 // Wait until the preceding kernel in the stream has completed and its writes are visible.
 __device__ __forceinline__ void pdl_wait_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -134,28 +128,6 @@ __device__ __forceinline__ void pdl_allow_successor() { asm volatile("griddepcon
 // ---------------------------------------------------------------- named barrier
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// ---------------------------------------------------------------- MMA
-// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate.
-//  a0: (row g, k 2t..2t+1)  a1: (row g+8, k 2t..2t+1)  a2: (row g, k 2t+8..)  a3: (row g+8, k 2t+8..)
-//  b0: (k 2t..2t+1, col g)  b1: (k 2t+8..2t+9, col g)
-//  d0,d1: (row g, cols 2t, 2t+1)  d2,d3: (row g+8, cols 2t, 2t+1)      g = lane/4, t = lane%4
-__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate (same fragment layout).
-__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                              uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ---------------------------------------------------------------- INT8 -> fp16
@@ -185,12 +157,6 @@ __device__ __forceinline__ uint32_t umma_idesc_bf16_m128(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (8u << 24);
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B (both K-major), fp32 D,
-// M = 128, N = n (a multiple of 16, 16..256).
-__device__ __forceinline__ uint32_t umma_idesc_f16_m128(int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (8u << 24);
-}
-
 // Allocate `ncols` TMEM columns (a power of two >= 32); the warp must execute it together.
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(smem_slot)),
@@ -213,17 +179,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-
-// D (+)= A * B^T with A (128 rows x 16 fp16, one row per TMEM lane, two elements per column)
-// read from TMEM at `a_tmem` and B from shared memory.
-__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
       : "memory");
 }
 
@@ -266,30 +221,6 @@ __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(bar)), "r"(rank));
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-}
-
-// Wait (acquire, cluster scope) for a phase of a barrier that threads of the peer CTA arrive on;
-// false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
 }
 
 // TMEM allocation shared by the two CTAs of a pair: one warp of each CTA executes it.
