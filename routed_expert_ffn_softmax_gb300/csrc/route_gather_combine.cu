@@ -27,59 +27,111 @@ __device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
+// Top-k of one token by the calling warp. Each lane sorts its (up to 8) logits once, best first
+// (odd-even merge network, 19 compare-exchanges); every round the lanes' heads meet in an xor
+// butterfly, which leaves the winner in all lanes, and the winning lane drops its head.
+// Past E a lane holds (-inf, none), which loses to every real expert.
+__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int tok, int E, int k, int32_t* ids,
+                                           float* w, int* s_ids = nullptr) {
+  const int lane = threadIdx.x & 31;
+  const float* l = logits + static_cast<int64_t>(tok) * E;
+  constexpr int kNone = 0x7fffffff;
+  float cv[8];
+  int ci[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    const float x = e < E ? l[e] : -INFINITY;
+    cv[q] = (x != x) ? -INFINITY : x;  // NaN orders as -inf (documented: unspecified routing)
+    ci[q] = e < E ? e : kNone;
+  }
+  auto cx = [&](float& va, int& ia, float& vb, int& ib) {  // (a, b) in route order
+    if (route_better(vb, ib, va, ia)) {
+      const float tv = va;
+      const int ti = ia;
+      va = vb;
+      ia = ib;
+      vb = tv;
+      ib = ti;
+    }
+  };
+#define MOE_CX(a, b) cx(cv[a], ci[a], cv[b], ci[b])
+  MOE_CX(0, 1); MOE_CX(2, 3); MOE_CX(4, 5); MOE_CX(6, 7);
+  MOE_CX(0, 2); MOE_CX(1, 3); MOE_CX(4, 6); MOE_CX(5, 7);
+  MOE_CX(1, 2); MOE_CX(5, 6);
+  MOE_CX(0, 4); MOE_CX(1, 5); MOE_CX(2, 6); MOE_CX(3, 7);
+  MOE_CX(2, 4); MOE_CX(3, 5);
+  MOE_CX(1, 2); MOE_CX(3, 4); MOE_CX(5, 6);
+#undef MOE_CX
+  // selection round j stays with lane j % 32, slot j / 32 (k <= E <= 256)
+  float sv[8];
+  int si[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    sv[q] = 0.0f;
+    si[q] = 0;
+  }
+  float m = -INFINITY;  // the largest kept logit
+  for (int j = 0; j < k; ++j) {
+    float bv = cv[0];
+    int bi = ci[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (route_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) {  // the winner was this lane's head
+#pragma unroll
+      for (int q = 0; q < 7; ++q) {
+        cv[q] = cv[q + 1];
+        ci[q] = ci[q + 1];
+      }
+      cv[7] = -INFINITY;
+      ci[7] = kNone;
+    }
+    if (j == 0) m = bv;
+    if ((j & 31) == lane) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q == (j >> 5)) {
+          sv[q] = bv;
+          si[q] = bi;
+        }
+    }
+  }
+  // renormalised softmax over the kept logits: exp(l_j - m) / sum of them
+  float ex[8];
+  float part = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int j = lane + 32 * q;
+    ex[q] = j < k ? expf(__fsub_rn(sv[q], m)) : 0.0f;
+    part = __fadd_rn(part, ex[q]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int j = lane + 32 * q;
+    if (j < k) {
+      ids[static_cast<int64_t>(tok) * k + j] = si[q];
+      w[static_cast<int64_t>(tok) * k + j] = __fdiv_rn(ex[q], part);
+      if (s_ids != nullptr) s_ids[tok * k + j] = si[q];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kTopkWarpsPerBlock * 32)
     route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                       int32_t* __restrict__ ids, float* __restrict__ w) {
   pdl_wait_predecessor();
   pdl_allow_successor();
-  const int lane = threadIdx.x & 31;
   const int tok = blockIdx.x * kTopkWarpsPerBlock + (threadIdx.x >> 5);
-  if (tok >= T) return;
-  const float* l = logits + static_cast<int64_t>(tok) * E;
-  float v[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int e = lane + 32 * q;
-    float x = e < E ? l[e] : -INFINITY;
-    v[q] = (x != x) ? -INFINITY : x;  // NaN orders as -inf (documented: unspecified routing)
-  }
-  uint32_t taken = 0;
-  float sel0 = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;  // "none"
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = lane + 32 * q;
-      if (e < E && !((taken >> q) & 1u) && (bi == 0x7fffffff || route_better(v[q], e, bv, bi))) {
-        bv = v[q];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || route_better(ov, oi, bv, bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    bv = __shfl_sync(0xffffffffu, bv, 0);
-    bi = __shfl_sync(0xffffffffu, bi, 0);
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) {
-      ids[static_cast<int64_t>(tok) * k + j] = bi;
-      w[static_cast<int64_t>(tok) * k + j] = bv;  // the logit, turned into a weight below
-      if (j == 0) sel0 = bv;
-    }
-  }
-  if (lane == 0) {
-    float* wt = w + static_cast<int64_t>(tok) * k;
-    float denom = 0.0f;
-    for (int j = 0; j < k; ++j) denom = __fadd_rn(denom, expf(__fsub_rn(wt[j], sel0)));
-    for (int j = 0; j < k; ++j) wt[j] = __fdiv_rn(expf(__fsub_rn(wt[j], sel0)), denom);
-  }
+  if (tok < T) topk_token(logits, tok, E, k, ids, w);
 }
 
 // ---------------------------------------------------------------------------------
@@ -89,21 +141,26 @@ __global__ void __launch_bounds__(kTopkWarpsPerBlock * 32)
 constexpr int kScanThreads = 1024;
 constexpr int kScanWarps = kScanThreads / 32;
 
-__global__ void __launch_bounds__(kScanThreads)
-    route_scan_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
-                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                      int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_pos,
-                      int32_t* __restrict__ active, int32_t* __restrict__ num_active,
-                      int32_t* __restrict__ zero_words, int n_zero) {
-  __shared__ int s_cnt[256];
-  __shared__ int s_off[256];
-  __shared__ int s_run[256];
-  __shared__ int s_wsum[kScanWarps];
-  __shared__ uint32_t s_mask[256 * kScanWarps];
+struct ScanShared {
+  int cnt[256];
+  int off[256];
+  int run[256];
+  int wsum[kScanWarps];
+  uint32_t mask[256 * kScanWarps];
+};
 
-  pdl_wait_predecessor();
-  pdl_allow_successor();
-
+// `ids` may have been written earlier in the same launch (route_fused_kernel), so it is read
+// through ordinary loads, not the read-only path.
+__device__ __forceinline__ void scan_block(ScanShared& sh, const int32_t* ids, int T, int E, int k,
+                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                           int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_pos,
+                                           int32_t* __restrict__ active, int32_t* __restrict__ num_active,
+                                           int32_t* __restrict__ zero_words, int n_zero) {
+  int* s_cnt = sh.cnt;
+  int* s_off = sh.off;
+  int* s_run = sh.run;
+  int* s_wsum = sh.wsum;
+  uint32_t* s_mask = sh.mask;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -176,6 +233,93 @@ __global__ void __launch_bounds__(kScanThreads)
   }
 }
 
+__global__ void __launch_bounds__(kScanThreads)
+    route_scan_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                      int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_pos,
+                      int32_t* __restrict__ active, int32_t* __restrict__ num_active,
+                      int32_t* __restrict__ zero_words, int n_zero) {
+  __shared__ ScanShared sh;
+  pdl_wait_predecessor();
+  pdl_allow_successor();
+  scan_block(sh, ids, T, E, k, counts, offsets, sorted_token, inv_pos, active, num_active, zero_words, n_zero);
+}
+
+// Decode-sized batches (T <= 64, T * k <= 1024): one launch instead of two. The CTA's warps take
+// the tokens' top-k (kept in shared memory as well) and mark each expert's tokens in a 64-bit
+// mask; warp 0 builds the exclusive offsets and the active list; then every assignment (t, j)
+// finds its place in the stable expert-major order as offset[e] + the number of earlier tokens in
+// e's mask. The general scan above needs many more block-wide barriers.
+constexpr int kFusedRouteMaxT = 64;
+constexpr int kFusedRouteMaxP = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+    route_fused_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w,
+                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_pos,
+                       int32_t* __restrict__ active, int32_t* __restrict__ num_active,
+                       int32_t* __restrict__ zero_words, int n_zero) {
+  __shared__ int s_ids[kFusedRouteMaxP];
+  __shared__ int s_cnt[256];
+  __shared__ int s_off[256];
+  __shared__ unsigned long long s_tok[256];  // bit t: token t routed to the expert
+  pdl_wait_predecessor();
+  pdl_allow_successor();
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  for (int i = tid; i < n_zero; i += kScanThreads) zero_words[i] = 0;
+  if (tid < 256) {
+    s_cnt[tid] = 0;
+    s_tok[tid] = 0ull;
+  }
+  __syncthreads();
+  for (int tok = tid >> 5; tok < T; tok += kScanWarps) topk_token(logits, tok, E, k, ids, w, s_ids);
+  __syncthreads();
+  const int P = T * k;
+  for (int a = tid; a < P; a += kScanThreads) {
+    const int e = s_ids[a];
+    atomicAdd(&s_cnt[e], 1);
+    atomicOr(&s_tok[e], 1ull << (a / k));
+  }
+  __syncthreads();
+  if (tid < 32) {  // warp 0
+    // exclusive scan of the counts and the active list, 32 experts at a time
+    int run = 0, nact = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int c = e < E ? s_cnt[e] : 0;
+      int incl = c;
+  #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      const uint32_t act = __ballot_sync(0xffffffffu, c > 0);
+      if (e < E) {
+        s_off[e] = run + incl - c;
+        counts[e] = c;
+        offsets[e] = run + incl - c;
+        if (c > 0) active[nact + __popc(act & ((1u << lane) - 1u))] = e;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      nact += __popc(act);
+    }
+    if (lane == 0) {
+      offsets[E] = run;
+      *num_active = nact;
+    }
+  }
+  __syncthreads();
+  // stable placement: tokens of an expert in token order
+  for (int a = tid; a < P; a += kScanThreads) {
+    const int t = a / k;
+    const int e = s_ids[a];
+    const int p = s_off[e] + __popcll(s_tok[e] & ((1ull << t) - 1ull));
+    sorted_token[p] = t;
+    inv_pos[a] = p;
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // xg[p, :] = x[sorted_token[p], :], 16 bytes per thread.
 __global__ void __launch_bounds__(256)
@@ -228,6 +372,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
                          int32_t* counts, int32_t* offsets, int32_t* sorted_token, int32_t* inv_pos,
                          int32_t* active, int32_t* num_active, int32_t* zero_words, int n_zero,
                          cudaStream_t stream) {
+  if (T <= kFusedRouteMaxT && static_cast<int64_t>(T) * k <= kFusedRouteMaxP)
+    return launch_pdl(route_fused_kernel, dim3(1), dim3(kScanThreads), 0, stream, logits, T, E, k, ids, w, counts,
+                      offsets, sorted_token, inv_pos, active, num_active, zero_words, n_zero);
   const int blocks = (T + kTopkWarpsPerBlock - 1) / kTopkWarpsPerBlock;
   cudaError_t err = launch_pdl(route_topk_kernel, dim3(blocks), dim3(kTopkWarpsPerBlock * 32), 0, stream,
                                logits, T, E, k, ids, w);
