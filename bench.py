@@ -33,7 +33,15 @@ import moe_workloads as mw  # noqa: E402
 
 METRIC = "expert-FFN decode weight-stream HBM GB/s (% of peak) and tokens/s, 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 6  # route_topk, route_scan, gather, gate+up, down, combine
+
+
+def kernels_per_step(cfg, T: int) -> int:
+    """Launches of one moe_ffn_forward: routing (one fused launch for T <= 64 and T*k <= 1024,
+    else top-k and scan), gather, the expert kernels (INT8 adds the fp16 copies of the token
+    rows and of h), combine."""
+    route = 1 if (T <= 64 and T * cfg.top_k <= 1024) else 2
+    experts = 4 if cfg.wtype == "int8" else 2
+    return route + 1 + experts + 1
 
 
 # ------------------------------------------------------------------ helpers
@@ -53,11 +61,16 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources of the expert kernels (the roofline's kernels) and of their launches
+EXPERT_SOURCES = ("expert_tc.cuh", "expert_pair.cuh", "moe_device.cuh", "expert_launch.cu")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; a recorded DRAM-traffic figure is used only while it matches."""
+    """Hash of the expert kernels' sources; a recorded DRAM-traffic figure is used only while it
+    matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "routed_expert_ffn_softmax_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    for n in EXPERT_SOURCES:
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
@@ -331,7 +344,7 @@ def bench_ours(args, cfg, T):
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 2},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step(cfg, T) * args.steps,
         "clocks": clocks,
     }
     if args.sweep and rank == 0:
