@@ -25,6 +25,7 @@ import sys
 import time
 
 import torch
+import torch.distributed as dist
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -50,6 +51,17 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def aggregate_over_ranks(total_ms: float, bytes_per_rank: float, tokens_per_rank: float, ws_n: int, device):
+    """Whole-job throughput of ws_n independent replicas: every rank's bytes and tokens over the
+    slowest rank's time (max over ranks; a collective when ws_n > 1). Returns
+    (time_ms, GB/s, tokens/s)."""
+    if ws_n > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return (total_ms, ws_n * bytes_per_rank / (total_ms * 1e-3) / 1e9, ws_n * tokens_per_rank / (total_ms * 1e-3))
 
 
 def hbm_peak():
@@ -183,7 +195,6 @@ def bench_ours(args, cfg, T):
 
     ws_n, rank, local = dist_env()
     if ws_n > 1:
-        import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     dev = torch.device(f"cuda:{local}")
@@ -233,12 +244,7 @@ def bench_ours(args, cfg, T):
     if moe.workspace_status(ws) != 0:
         raise RuntimeError("a kernel reported a timed-out wait")
     bytes_timed = sum(wl.weight_bytes(i % copies) for i in range(args.steps))
-    if ws_n > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = ws_n * bytes_timed / (total_ms * 1e-3) / 1e9
-    tokens_s = ws_n * T * args.steps / (total_ms * 1e-3)
+    total_ms, value, tokens_s = aggregate_over_ranks(total_ms, bytes_timed, T * args.steps, ws_n, dev)
 
     # ---- dominant kernels: the expert FFN pair (gate+up, down), timed alone with events
     r = {n: torch.empty(s, dtype=dt, device=dev) for n, s, dt in (
@@ -297,12 +303,7 @@ def bench_ours(args, cfg, T):
         e2e_step(i % copies)
     b.record(stream)
     barrier_sync()
-    e2e_ms = a.elapsed_time(b)
-    if ws_n > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = ws_n * bytes_timed / (e2e_ms * 1e-3) / 1e9
+    e2e_ms, e2e_value, _ = aggregate_over_ranks(a.elapsed_time(b), bytes_timed, T * args.steps, ws_n, dev)
 
     result = {
         "metric": METRIC,
