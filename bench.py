@@ -33,6 +33,8 @@ sys.path.insert(0, ROOT)
 import moe_workloads as mw  # noqa: E402
 
 METRIC = "expert-FFN decode weight-stream HBM GB/s (% of peak) and tokens/s, 1 GB300"
+METRIC_HOST = ("expert-FFN decode weight-stream GB/s with the expert weights in Grace LPDDR5X, read over "
+               "NVLink-C2C (% of the measured host->device copy rate) and tokens/s, 1 GB300")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -62,6 +64,27 @@ def aggregate_over_ranks(total_ms: float, bytes_per_rank: float, tokens_per_rank
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     return (total_ms, ws_n * bytes_per_rank / (total_ms * 1e-3) / 1e9, ws_n * tokens_per_rank / (total_ms * 1e-3))
+
+
+def c2c_copy_peak(device, gbytes: float = 2.0) -> float:
+    """GB/s of a pinned host -> device copy (the copy engines over NVLink-C2C), measured here:
+    the ceiling for kernels that read weights in host memory."""
+    n = int(gbytes * 1e9)
+    src = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(n, dtype=torch.uint8, device=device)
+    for _ in range(2):
+        dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    reps = 5
+    for _ in range(reps):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    gbs = reps * n / (a.elapsed_time(b) * 1e-3) / 1e9
+    del src, dst
+    return gbs
 
 
 def hbm_peak():
@@ -154,16 +177,23 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 class Workload:
-    """Device-resident weights (several distinct layer copies, so consecutive steps do not
-    re-read the previous step's experts from L2) and one decode batch per copy. The number
-    of active experts per batch (which sets the weight bytes a step must stream) is read
-    from the library's own routing kernel."""
+    """Weights (several distinct layer copies, so consecutive steps do not re-read the previous
+    step's experts from L2) and one decode batch per copy. The weights live in HBM, or with
+    host_weights in pinned host memory (Grace LPDDR5X on a GB300 node), which the same kernels
+    read over NVLink-C2C. The number of active experts per batch (which sets the weight bytes a
+    step must stream) is read from the library's own routing kernel."""
 
-    def __init__(self, cfg: mw.MoEConfig, T: int, copies: int, device, moe, seed: int = 0):
+    def __init__(self, cfg: mw.MoEConfig, T: int, copies: int, device, moe, seed: int = 0,
+                 host_weights: bool = False):
         self.cfg, self.T, self.device = cfg, T, device
         self.layers, self.tokens = [], []
         for c in range(copies):
-            self.layers.append(mw.make_layer(cfg, seed=seed + 1000 * c, device=device))
+            layer = mw.make_layer(cfg, seed=seed + 1000 * c, device=device)
+            if host_weights:
+                layer = {n: (torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) if v is not None
+                             else None) for n, v in layer.items()}
+                torch.cuda.synchronize()
+            self.layers.append(layer)
             self.tokens.append(mw.make_tokens(cfg, T, seed=seed + 1000 * c, device=device))
         self.active = []
         k = cfg.top_k
@@ -206,7 +236,8 @@ def bench_ours(args, cfg, T):
     moe.load()
 
     copies = args.copies
-    wl = Workload(cfg, T, copies, dev, moe)
+    host = args.weights == "host"
+    wl = Workload(cfg, T, copies, dev, moe, host_weights=host)
     stream = torch.cuda.current_stream()
     ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wl.wt, dev)
     out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
@@ -275,8 +306,12 @@ def bench_ours(args, cfg, T):
     ffn_t = [a.elapsed_time(b) for a, b in ffn_ev]
     ffn_avg_ms = sum(ffn_t) / len(ffn_t)
     ffn_achieved = (sum(ffn_bytes) / len(ffn_bytes)) / (ffn_avg_ms * 1e-3) / 1e9
-    peak, peak_kind = hbm_peak()
-    workload_name = f"{cfg.name}_T{T}"
+    if host:
+        peak, peak_kind = round(c2c_copy_peak(dev), 1), "measured in this run (pinned host -> device copy, NVLink-C2C)"
+    else:
+        peak, peak_kind = hbm_peak()
+        peak_kind = f"{peak_kind} (hbm_gbs, copy bandwidth)"
+    workload_name = f"{cfg.name}_T{T}" + ("_hostweights" if host else "")
     traffic = recorded_traffic(workload_name)
 
     # ---- end to end through the C ABI: host inputs in, host result out, every step
@@ -306,7 +341,7 @@ def bench_ours(args, cfg, T):
     e2e_ms, e2e_value, _ = aggregate_over_ranks(a.elapsed_time(b), bytes_timed, T * args.steps, ws_n, dev)
 
     result = {
-        "metric": METRIC,
+        "metric": METRIC_HOST if host else METRIC,
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": ws_n,
@@ -324,6 +359,8 @@ def bench_ours(args, cfg, T):
         "config": {
             "workload": workload_name, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
             "weights": cfg.wtype, "T": T, "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
+            "weights_memory": "pinned host memory (Grace LPDDR5X), read by the kernels over NVLink-C2C" if host
+                              else "HBM",
             "active_experts_mean": round(sum(wl.active) / len(wl.active), 2),
             "tokens_per_expert_mean": round(T * cfg.top_k * len(wl.active) / sum(wl.active), 2),
             "weight_bytes_per_step_mean": int(wl.mean_weight_bytes()),
@@ -333,10 +370,10 @@ def bench_ours(args, cfg, T):
         },
         "roofline": {
             "kernel": "expert FFN stream kernels (gate+up with SiLU*up, then down), timed together",
-            "bound": "hbm",
+            "bound": "c2c" if host else "hbm",
             "achieved": round(ffn_achieved, 1),
             "peak": peak,
-            "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
+            "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(ffn_achieved / peak, 4),
             "traffic": traffic,
@@ -349,7 +386,7 @@ def bench_ours(args, cfg, T):
         "clocks": clocks,
     }
     if args.sweep and rank == 0:
-        result["sweep"] = sweep(cfg, dev, moe, copies)
+        result["sweep"] = sweep(cfg, dev, moe, copies, host)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(cfg, T, wl, budget_s=args.cpu_budget)
     if ws_n > 1:
@@ -358,11 +395,11 @@ def bench_ours(args, cfg, T):
     return result if rank == 0 else None
 
 
-def sweep(cfg, dev, moe, copies):
+def sweep(cfg, dev, moe, copies, host=False):
     """GB/s and tokens/s at every T of the workload (same method, fewer steps)."""
     rows = []
     for T in cfg.T:
-        wl = Workload(cfg, T, copies, dev, moe)
+        wl = Workload(cfg, T, copies, dev, moe, host_weights=host)
         ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wl.wt, dev)
         out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
         s = torch.cuda.current_stream()
@@ -491,6 +528,8 @@ def main():
     ap.add_argument("--config", default="mixtral8x7b", choices=sorted(mw.CONFIGS))
     ap.add_argument("--T", type=int, default=16)
     ap.add_argument("--copies", type=int, default=3, help="distinct weight copies rotated across steps")
+    ap.add_argument("--weights", choices=("device", "host"), default="device",
+                    help="where the expert weights live: HBM, or pinned host memory read over NVLink-C2C")
     ap.add_argument("--sweep", action="store_true", help="also measure every T of the workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")

@@ -22,6 +22,14 @@
  * Conventions shared by every entry point:
  *   - Every array pointer is a DEVICE pointer owned by the caller. The library
  *     allocates no memory and keeps no device state between calls.
+ *   - Exception: the expert weights and scales (W_gate, W_up, W_down, s_gate,
+ *     s_up, s_down) may also live in host memory the GPU can address (pinned or
+ *     registered; on a GB300 node the Grace LPDDR5X), passed by that memory's
+ *     device-visible address. The kernels then stream them in place over
+ *     NVLink-C2C with the same results (bit-identical) as from HBM: the pages
+ *     keep routed experts in CPU memory when they exceed GPU memory (§1) in
+ *     one general layout that CPU and GPU share (§3.1). Throughput is then
+ *     bounded by the host link instead of HBM.
  *   - bf16 arrays are passed as uint16_t bit patterns.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
  *     default stream) and never synchronises the host. Calls on one stream may
