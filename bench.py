@@ -40,10 +40,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 def kernels_per_step(cfg, T: int) -> int:
     """Launches of one moe_ffn_forward: routing (one fused launch for T <= 64 and T*k <= 1024,
-    else top-k and scan), gather, the expert kernels (INT8 adds the fp16 copies of the token
-    rows and of h), combine."""
+    else top-k and scan), gather (INT8: straight into the fp16 copy), the expert kernels (INT8
+    adds the fp16 copy of h), combine."""
     route = 1 if (T <= 64 and T * cfg.top_k <= 1024) else 2
-    experts = 4 if cfg.wtype == "int8" else 2
+    experts = 3 if cfg.wtype == "int8" else 2
     return route + 1 + experts + 1
 
 

@@ -109,7 +109,7 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const int32_t* active,
                             const int32_t* num_active, const void* Wg, const void* Wu, const void* Wd,
                             const float* sg, const float* su, const float* sd, moe_wtype_t wtype, int H, int I,
-                            int E, int P, float* Y, char* ws, cudaStream_t stream) {
+                            int E, int P, float* Y, char* ws, cudaStream_t stream, bool xg16_ready = false) {
   const int sms = sm_count();
   if (sms < 1) return MOE_ERR_CUDA;
   const Layout L = layout(P, H, I, E, wtype == MOE_W_INT8_G128);
@@ -134,6 +134,7 @@ moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const in
   plan.xg16 = reinterpret_cast<uint16_t*>(ws + L.xg16);
   plan.h_scale = reinterpret_cast<float*>(ws + L.h_scale);
   plan.xg_scale = reinterpret_cast<float*>(ws + L.xg_scale);
+  plan.xg16_ready = xg16_ready;
   plan.Y = Y;
   plan.partials = reinterpret_cast<float*>(ws + L.partials);
   plan.counters = reinterpret_cast<int32_t*>(ws + L.ctrl + kCountersOffset);
@@ -270,10 +271,15 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
   cudaError_t e = moe::launch_route(logits, T, E, top_k, ids, w, I32(L.counts), offsets, sorted_token, inv_pos,
                                     active, num_active, I32(L.ctrl), kZeroWords, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = moe::launch_gather(x, T, H, top_k, sorted_token, xg, sms, s);
+  const bool int8 = wtype == MOE_W_INT8_G128;
+  if (int8)  // the INT8 kernels read only the fp16 copy of the gathered rows: write it directly
+    e = moe::launch_gather_f16(x, H, P, sorted_token, reinterpret_cast<uint16_t*>(ws + L.xg16),
+                               reinterpret_cast<float*>(ws + L.xg_scale), sms, s);
+  else
+    e = moe::launch_gather(x, T, H, top_k, sorted_token, xg, sms, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const moe_status_t st = run_expert_ffn(xg, offsets, active, num_active, W_gate, W_up, W_down, s_gate, s_up,
-                                         s_down, wtype, H, I, E, P, Y, ws, s);
+                                         s_down, wtype, H, I, E, P, Y, ws, s, int8);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_combine(Y, inv_pos, w, T, top_k, H, out, sms, s));
 }

@@ -64,17 +64,19 @@ bool encode_tokens(CUtensorMap* map, const void* X, int K, int P, bool fp16 = fa
 // its largest magnitude lands in [2^14, 2^15) (inside fp16's range, k clamped to [-100, 127]),
 // and row_scale[p] = 2^k restores it after the MMA. Every value within 2^-31 of the row's
 // largest keeps its bf16 bits exactly in fp16; smaller ones round to fp16's subnormal grid.
+// With src_rows, output row p is source row src_rows[p]: the token gather and the fp16 copy in
+// one pass (the forward path's INT8 gather).
 constexpr int kRowThreads = 256;
 
 __global__ void __launch_bounds__(kRowThreads)
     rows_to_f16_kernel(const uint4* __restrict__ src, int K8, int64_t P, uint4* __restrict__ dst,
-                       float* __restrict__ row_scale) {
+                       float* __restrict__ row_scale, const int32_t* __restrict__ src_rows) {
   __shared__ float s_max[kRowThreads / 32];
   pdl_wait_predecessor();
   pdl_allow_successor();
   const int tid = threadIdx.x;
   for (int64_t p = blockIdx.x; p < P; p += gridDim.x) {
-    const uint4* s4 = src + p * K8;
+    const uint4* s4 = src + (src_rows != nullptr ? static_cast<int64_t>(src_rows[p]) : p) * K8;
     float m = 0.0f;
     for (int c = tid; c < K8; c += kRowThreads) {
       const uint4 v = s4[c];
@@ -119,11 +121,11 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 cudaError_t launch_rows_to_f16(const uint16_t* src, int K, int P, uint16_t* dst, float* row_scale, int num_sms,
-                               cudaStream_t s) {
+                               cudaStream_t s, const int32_t* src_rows = nullptr) {
   int blocks = P < num_sms * 4 ? P : num_sms * 4;
   if (blocks < 1) blocks = 1;
   return launch_pdl(rows_to_f16_kernel, dim3(blocks), dim3(kRowThreads), 0, s, reinterpret_cast<const uint4*>(src),
-                    K / 8, static_cast<int64_t>(P), reinterpret_cast<uint4*>(dst), row_scale);
+                    K / 8, static_cast<int64_t>(P), reinterpret_cast<uint4*>(dst), row_scale, src_rows);
 }
 
 template <bool kGateUp>
@@ -278,8 +280,10 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
   a.status = p.status;
   a.E = p.E;
   a.P = p.P;
-  e = launch_rows_to_f16(p.xg, p.H, p.P, p.xg16, p.xg_scale, p.num_ctas, s);
-  if (e != cudaSuccess) return e;
+  if (!p.xg16_ready) {
+    e = launch_rows_to_f16(p.xg, p.H, p.P, p.xg16, p.xg_scale, p.num_ctas, s);
+    if (e != cudaSuccess) return e;
+  }
   tc::Args gu = a;
   gu.out = p.h;
   gu.out_ld = p.I;
@@ -304,6 +308,11 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_gather_f16(const uint16_t* x, int H, int P, const int32_t* sorted_token, uint16_t* xg16,
+                              float* xg_scale, int num_sms, cudaStream_t stream) {
+  return launch_rows_to_f16(x, H, P, xg16, xg_scale, num_sms, stream, sorted_token);
+}
 
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream) {
   return plan.int8 ? launch_pair_int8(plan, stream) : launch_tc(plan, stream);

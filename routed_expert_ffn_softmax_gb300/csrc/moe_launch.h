@@ -37,6 +37,10 @@ cudaError_t launch_gather(const uint16_t* x, int T, int H, int k, const int32_t*
 cudaError_t launch_combine(const float* Y, const int32_t* inv_pos, const float* w, int T, int k, int H,
                            uint16_t* out, int num_sms, cudaStream_t stream);
 
+// INT8 forward path: gather the token rows straight into their fp16 copy (see ExpertFfnPlan::xg16).
+cudaError_t launch_gather_f16(const uint16_t* x, int H, int P, const int32_t* sorted_token, uint16_t* xg16,
+                              float* xg_scale, int num_sms, cudaStream_t stream);
+
 // fp32 slots per CTA the expert kernels' stream-K partials need (the larger of the two kernel
 // families), and the CTA capacity the workspace provides.
 constexpr int kPartialSlotFloats = 16384;
@@ -61,6 +65,7 @@ struct ExpertFfnPlan {
   uint16_t* xg16;     // [P, H]
   uint16_t* h16;      // [P, I]
   float* xg_scale;    // [P]
+  bool xg16_ready;    // INT8: xg16 / xg_scale were written by the gather (xg is then not read)
   float* h_scale;     // [P]
   float* Y;           // [P, H]
   float* partials;    // stream-K partial slots
