@@ -1,10 +1,11 @@
-"""Seeded synthetic workloads for the routed-expert FFN (decode regime).
+"""Seeded synthetic workloads for the routed-expert FFN and for decode-phase GQA
+attention.
 
 This module is shared by the CUDA path's tests/bench and by the CPU oracle's
-tests. It holds only input generation: the expert shapes, the seeded draws and
-the offline INT8 weight quantiser that prepares the weights both sides consume.
-It holds none of the routed-expert FFN's arithmetic (routing, gather, FFN,
-combine).
+tests. It holds only input generation: the expert and attention shapes, the
+seeded draws and the offline INT8 weight quantiser that prepares the weights
+both sides consume. It holds none of the arithmetic of either operator
+(routing, gather, FFN, combine; scores, softmax, weighted sum of values).
 
 Expert shapes and routing top-k come from HiNa-MoE (arXiv 2610.05123),
 §8.1 Table 3 ("Expert weight matrix dimensions and routing strategies"):
@@ -167,6 +168,82 @@ def make_tokens(cfg: MoEConfig, T: int, seed: Optional[int] = None, device="cpu"
     x = draw_x(T, cfg.H, seed, device)
     lg = draw_logits(T, cfg.E, seed, device, cfg.skew_experts, cfg.skew)
     return x, lg
+
+
+# ----------------------------------------------------------------------------
+# Decode-phase GQA attention inputs (HiNa-MoE §6.1, Figure 9).
+#
+# Head counts and head dim are those of the GQA models the pages name: Qwen3-30B-A3B
+# (32 query heads, 4 key/value heads: the group of 8 the pages quote), Mixtral-8x7B
+# (32 / 8) and Qwen3-235B-A22B (64 / 4); all use d = 128. Sequence lengths: the pages
+# run decode after 512-token prompts (RapidMoE, "Datasets and Workloads") and prefill
+# at 2K-32K tokens (HiNa-MoE Table 4); a decode batch here mixes lengths drawn
+# uniformly from [len_lo, len_hi]. Draws: q, K, V ~ N(0,1) -> bf16; cache rows past a
+# sequence's length are filled with NaN, which the attention must never read.
+
+@dataclasses.dataclass(frozen=True)
+class AttnConfig:
+    name: str
+    h_q: int
+    h_kv: int
+    d: int
+    B: int            # sequences in the decode batch (one new token each)
+    len_lo: int
+    len_hi: int       # also the cache capacity L_cap
+    seed: int = 0
+
+    @property
+    def group(self) -> int:
+        return self.h_q // self.h_kv
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(self.d) ** 0.5
+
+
+ATTN_CONFIGS: Dict[str, AttnConfig] = {
+    c.name: c
+    for c in (
+        AttnConfig("attn_tiny", 16, 2, 128, 5, 1, 700),
+        AttnConfig("qwen3_30b_attn", 32, 4, 128, 64, 512, 8192),
+        AttnConfig("mixtral8x7b_attn", 32, 8, 128, 16, 2048, 32768),
+        AttnConfig("qwen3_235b_attn", 64, 4, 128, 64, 512, 8192),
+    )
+}
+
+_AQ, _AK, _AV, _ALEN = 10, 11, 12, 13
+
+
+def draw_seq_lens(B: int, lo: int, hi: int, seed: int = 0) -> torch.Tensor:
+    """[B] int32 sequence lengths, uniform in [lo, hi] (drawn on the CPU)."""
+    g = _gen("cpu", seed, _ALEN)
+    return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def make_attention(cfg: AttnConfig, seed: Optional[int] = None, device="cpu",
+                   seq_lens: Optional[torch.Tensor] = None, L_cap: Optional[int] = None):
+    """(q [B,h_q,d], K [B,h_kv,L_cap,d], V [B,h_kv,L_cap,d] bf16, seq_lens [B] int32).
+
+    Rows at or past seq_lens[b] hold NaN."""
+    seed = cfg.seed if seed is None else seed
+    L_cap = cfg.len_hi if L_cap is None else L_cap
+    if seq_lens is None:
+        seq_lens = draw_seq_lens(cfg.B, cfg.len_lo, cfg.len_hi, seed)
+    B = seq_lens.shape[0]
+    q = torch.randn(B, cfg.h_q, cfg.d, generator=_gen(device, seed, _AQ), device=device).to(torch.bfloat16)
+    kv = []
+    for t in (_AK, _AV):
+        m = torch.randn(B, cfg.h_kv, L_cap, cfg.d, generator=_gen(device, seed, t), device=device)
+        m = m.to(torch.bfloat16)
+        past = torch.arange(L_cap, device=device)[None, :] >= seq_lens.to(device)[:, None].long()
+        m[past[:, None, :, None].expand_as(m)] = float("nan")
+        kv.append(m)
+    return q, kv[0], kv[1], seq_lens.to(torch.int32)
+
+
+def attention_kv_bytes(seq_lens: torch.Tensor, h_kv: int, d: int) -> int:
+    """Algorithmic bytes of the key/value rows one decode call must read (bf16)."""
+    return int(seq_lens.long().sum()) * h_kv * d * 2 * 2
 
 
 def expected_active(cfg: MoEConfig, T: int) -> float:

@@ -1,11 +1,11 @@
-"""ctypes front end of the plain CPU oracle (oracle/moe_oracle.cpp).
+"""ctypes front end of the plain CPU oracle (oracle/moe_oracle.cpp, oracle/gqa_oracle.cpp).
 
 TEST INFRASTRUCTURE ONLY: tests/, __graft_entry__.smoke() and bench.py's
 CPU-baseline leg may import this package; the CUDA product path never does.
 
 Arrays are numpy or CPU torch tensors. bf16 tensors travel as their raw
 uint16 bit patterns. Every function here only marshals arguments; the
-arithmetic is in moe_oracle.cpp.
+arithmetic is in the two C++ files.
 """
 from __future__ import annotations
 
@@ -17,7 +17,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_SRCS = [os.path.join(_HERE, "moe_oracle.cpp"), os.path.join(_HERE, "gqa_oracle.cpp")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -27,11 +27,11 @@ WTYPE = {"bf16": 0, "int8": 1}
 
 def build(force: bool = False) -> str:
     """Compile liboracle.so with g++ (sequential fp32 sums: -ffp-contract=off)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+    if not force and os.path.exists(_LIB) and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in _SRCS):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-o", tmp, _SRC]
+           "-fPIC", "-shared", "-o", tmp, *_SRCS]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -57,6 +57,10 @@ def _load():
             lib.oracle_forward.restype = i
             lib.oracle_f32_to_bf16.argtypes = [P, ctypes.c_long, P]
             lib.oracle_f32_to_bf16.restype = None
+            lib.oracle_gqa_decode.argtypes = [P, P, P, P, i, i, i, i, i, ctypes.c_float, P, P]
+            lib.oracle_gqa_decode.restype = i
+            lib.oracle_f64_to_bf16.argtypes = [P, ctypes.c_long, P]
+            lib.oracle_f64_to_bf16.restype = None
             _lib = lib
     return _lib
 
@@ -175,6 +179,32 @@ def forward(x, logits, W_gate, W_up, W_down, s_gate=None, s_up=None, s_down=None
     if rc != 0:
         raise ValueError("oracle_forward: bad sizes")
     return res
+
+
+def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float):
+    """Decode-phase GQA attention (gqa_oracle.cpp). q [B,h_q,d], K/V [B,h_kv,L_cap,d] bf16,
+    seq_lens [B] int32. Returns dict(out bf16 bits [B,h_q,d], out_f64 [B,h_q,d])."""
+    qa = _np(q, np.uint16)
+    ka = _np(k_cache, np.uint16)
+    va = _np(v_cache, np.uint16)
+    ln = _np(seq_lens, np.int32)
+    B, h_q, d = qa.shape
+    B2, h_kv, L_cap, d2 = ka.shape
+    assert B2 == B and d2 == d and va.shape == ka.shape and ln.shape == (B,)
+    out = np.zeros((B, h_q, d), np.uint16)
+    of = np.zeros((B, h_q, d), np.float64)
+    rc = _load().oracle_gqa_decode(_p(qa), _p(ka), _p(va), _p(ln), B, h_q, h_kv, d, L_cap,
+                                   float(scale), _p(out), _p(of))
+    if rc != 0:
+        raise ValueError("oracle_gqa_decode: bad sizes or sequence lengths")
+    return dict(out=out, out_f64=of)
+
+
+def f64_to_bf16_bits(a):
+    a = _np(a, np.float64)
+    out = np.zeros(a.shape, np.uint16)
+    _load().oracle_f64_to_bf16(_p(a), a.size, _p(out))
+    return out
 
 
 def f32_to_bf16_bits(a):
