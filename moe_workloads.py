@@ -236,7 +236,7 @@ def make_attention(cfg: AttnConfig, seed: Optional[int] = None, device="cpu",
         m = torch.randn(B, cfg.h_kv, L_cap, cfg.d, generator=_gen(device, seed, t), device=device)
         m = m.to(torch.bfloat16)
         past = torch.arange(L_cap, device=device)[None, :] >= seq_lens.to(device)[:, None].long()
-        m[past[:, None, :, None].expand_as(m)] = float("nan")
+        m.masked_fill_(past[:, None, :, None], float("nan"))
         kv.append(m)
     return q, kv[0], kv[1], seq_lens.to(torch.int32)
 

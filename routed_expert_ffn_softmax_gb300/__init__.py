@@ -1,6 +1,8 @@
-"""Routed-expert MoE FFN for the GB300 (sm_103a): Python binding of libmoe.so.
+"""Routed-expert MoE FFN and decode GQA attention for the GB300 (sm_103a): Python binding of
+libmoe.so.
 
-Every function here has the name of the C entry point it calls (include/moe.h)
+Every function here has the name of the C entry point it calls (include/moe.h,
+include/moe_gqa.h)
 and only marshals arguments: torch tensors in, device pointers and sizes out.
 All arithmetic runs in the library's CUDA kernels. There is no fallback: if
 libmoe.so is missing or cannot be loaded, importing the binding's functions
@@ -23,7 +25,7 @@ __all__ = [
     "MoeError", "MOE_W_BF16", "MOE_W_INT8_G128", "load", "lib_path",
     "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
     "moe_expert_ffn", "moe_combine", "moe_ffn_forward", "alloc_workspace", "workspace_status",
-    "moe_expert_ffn_noalloc",
+    "moe_expert_ffn_noalloc", "moe_gqa_workspace_size", "moe_gqa_decode", "alloc_gqa_workspace",
 ]
 
 MOE_W_BF16 = 0
@@ -65,7 +67,11 @@ def load() -> ctypes.CDLL:
         lib.moe_expert_ffn.argtypes = [P, P, P, P, P, P, P, P, P, P, i, i, i, i, i, P, P, z, P]
         lib.moe_combine.argtypes = [P, P, P, i, i, i, P, P]
         lib.moe_ffn_forward.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, P, z, P]
-        for f in ("moe_route_topk", "moe_gather", "moe_expert_ffn", "moe_combine", "moe_ffn_forward"):
+        lib.moe_gqa_workspace_size.argtypes = [i, i, i, i, i]
+        lib.moe_gqa_workspace_size.restype = z
+        lib.moe_gqa_decode.argtypes = [P, P, P, P, i, i, i, i, i, ctypes.c_float, P, P, z, P]
+        for f in ("moe_route_topk", "moe_gather", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
+                  "moe_gqa_decode"):
             getattr(lib, f).restype = i
         _lib = lib
         return lib
@@ -172,3 +178,23 @@ def moe_expert_ffn_noalloc(xg, expert_offsets, active_experts, num_active, W_gat
     _check("moe_expert_ffn_noalloc", f(
         _ptr(xg), _ptr(expert_offsets), _ptr(active_experts), _ptr(num_active), _ptr(W_gate), _ptr(W_up),
         _ptr(W_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _wtype(W_gate), H, I, E, P, _ptr(Y), _stream(stream)))
+
+
+def moe_gqa_workspace_size(B: int, h_q: int, h_kv: int, d: int, L_cap: int) -> int:
+    return int(load().moe_gqa_workspace_size(B, h_q, h_kv, d, L_cap))
+
+
+def alloc_gqa_workspace(B, h_q, h_kv, d, L_cap, device="cuda") -> torch.Tensor:
+    n = moe_gqa_workspace_size(B, h_q, h_kv, d, L_cap)
+    if n == 0:
+        raise ValueError("invalid or unsupported sizes for moe_gqa_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out, workspace, stream=None) -> None:
+    """q [B,h_q,d], k_cache/v_cache [B,h_kv,L_cap,d] bf16, seq_lens [B] int32, out [B,h_q,d] bf16."""
+    B, h_q, d = q.shape
+    _, h_kv, L_cap, _ = k_cache.shape
+    _check("moe_gqa_decode", load().moe_gqa_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, h_q, h_kv, d, L_cap, float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

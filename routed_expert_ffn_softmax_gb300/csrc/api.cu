@@ -1,11 +1,15 @@
-// C ABI of the routed-expert FFN library (declared in include/moe.h).
+// C ABI of the routed-expert FFN library (declared in include/moe.h) and of decode-phase GQA
+// attention (include/moe_gqa.h).
 // Host-side argument checks, workspace layout and the launch sequence.
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <cstdint>
 
+#include <cmath>
+
 #include "moe.h"
+#include "moe_gqa.h"
 #include "moe_launch.h"
 
 namespace {
@@ -282,6 +286,61 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
                                          s_down, wtype, H, I, E, P, Y, ws, s, int8);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_combine(Y, inv_pos, w, T, top_k, H, out, sms, s));
+}
+
+// ---------------------------------------------------------------- decode GQA attention
+namespace {
+
+constexpr size_t kGqaPartialBytes = sizeof(float) * static_cast<size_t>(kMaxCtas) * 2 * moe::kGqaSlotFloats;
+
+moe_status_t gqa_check(int B, int h_q, int h_kv, int d, int L_cap) {
+  if (B < 0 || h_q < 1 || h_kv < 1 || d < 1 || L_cap < 1 || h_q % h_kv) return MOE_ERR_INVALID_ARG;
+  if (d != 128 || h_q / h_kv > 16 || B > moe::kGqaMaxSeqs) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * h_q > INT32_MAX || static_cast<int64_t>(B) * h_kv > INT32_MAX)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+size_t moe_gqa_workspace_size(int B, int h_q, int h_kv, int d, int L_cap) {
+  if (gqa_check(B, h_q, h_kv, d, L_cap) != MOE_OK) return 0;
+  return kCtrlBytes + align_up(kGqaPartialBytes);
+}
+
+moe_status_t moe_gqa_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                            const int32_t* seq_lens, int B, int h_q, int h_kv, int d, int L_cap, float scale,
+                            uint16_t* out, void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  const moe_status_t sz = gqa_check(B, h_q, h_kv, d, L_cap);
+  if (sz != MOE_OK) return sz;
+  if (!std::isfinite(scale)) return MOE_ERR_INVALID_ARG;
+  if (B == 0) return MOE_OK;
+  if (!q || !k_cache || !v_cache || !seq_lens || !out || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(seq_lens, 4) || !aligned(workspace, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_gqa_workspace_size(B, h_q, h_kv, d, L_cap)) return MOE_ERR_WORKSPACE;
+  const int sms = sm_count();
+  if (sms < 1) return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (cudaMemsetAsync(ws, 0, kCountersOffset + 4 * kMaxCtas, s) != cudaSuccess) return MOE_ERR_CUDA;
+  moe::GqaPlan plan{};
+  plan.q = q;
+  plan.k_cache = k_cache;
+  plan.v_cache = v_cache;
+  plan.seq_lens = seq_lens;
+  plan.out = out;
+  plan.partials = reinterpret_cast<float*>(ws + kCtrlBytes);
+  plan.counters = reinterpret_cast<int32_t*>(ws + kCountersOffset);
+  plan.status = reinterpret_cast<int32_t*>(ws);
+  plan.B = B;
+  plan.h_q = h_q;
+  plan.h_kv = h_kv;
+  plan.L_cap = L_cap;
+  plan.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  plan.num_ctas = sms < kMaxCtas ? sms : kMaxCtas;
+  return cuda_status(moe::launch_gqa_decode(plan, s));
 }
 
 }  // extern "C"

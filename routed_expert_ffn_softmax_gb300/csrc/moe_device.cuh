@@ -15,6 +15,7 @@ enum : int32_t {
   kStatusWaitFullTimeout = 1,   // a consumer gave up waiting for a stage to land
   kStatusWaitEmptyTimeout = 2,  // the producer gave up waiting for a stage to drain
   kStatusDrainTimeout = 3,      // copies still in flight when the kernel gave up
+  kStatusBadSeqLen = 4,         // attention: a sequence length outside [0, L_cap] (treated as 0)
 };
 
 // Upper bound on any single wait inside a kernel (ns of %globaltimer). A wait
@@ -125,6 +126,12 @@ __device__ __forceinline__ void pdl_wait_predecessor() { asm volatile("griddepco
 // Allow the next kernel in the stream to begin launching.
 __device__ __forceinline__ void pdl_allow_successor() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Order this thread's generic-proxy shared-memory writes before later async-proxy reads of them
+// (TMA, tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- named barrier
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -151,6 +158,16 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_byte_addr) {
          (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor: MN-major tile written by TMA with the 128-byte swizzle, i.e.
+// rows of 64 MN-contiguous 16-bit elements, one row per K index. Eight K rows form a 1024-byte
+// swizzle atom (stride byte offset 1024); `mn_block_bytes` is the distance between the 64-wide
+// blocks along MN (leading byte offset).
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_byte_addr, uint32_t mn_block_bytes) {
+  return static_cast<uint64_t>((smem_byte_addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both K-major), fp32 D,
 // M = 128, N = n (a multiple of 16, 16..256).
 __device__ __forceinline__ uint32_t umma_idesc_bf16_m128(int n) {
@@ -164,6 +181,9 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* smem_slot, uint32_t ncols) 
                : "memory");
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+
+// The A operand of the instruction descriptor read MN-major (bit 15, "transpose A").
+constexpr uint32_t kIdescAMajorMN = 1u << 15;
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");

@@ -75,6 +75,24 @@ struct ExpertFfnPlan {
 };
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream);
 
+// Decode-phase GQA attention (gqa_decode.cu) over a key/value cache [B, h_kv, L_cap, 128].
+constexpr int kGqaMaxSeqs = 2048;  // sequences per call (the tile prefix lives in shared memory)
+constexpr int kGqaSlotFloats = 16 * 128 + 2 * 16;  // one stream-K partial: o[16][128], m[16], l[16]
+struct GqaPlan {
+  const uint16_t* q;        // [B, h_q, 128] bf16
+  const uint16_t* k_cache;  // [B, h_kv, L_cap, 128] bf16
+  const uint16_t* v_cache;  // [B, h_kv, L_cap, 128] bf16
+  const int32_t* seq_lens;  // [B]
+  uint16_t* out;            // [B, h_q, 128] bf16
+  float* partials;          // [kPartialCtas][2][kGqaSlotFloats]
+  int32_t* counters;        // [kPartialCtas], zeroed
+  int32_t* status;
+  int B, h_q, h_kv, L_cap;
+  float scale_log2;         // softmax scale * log2(e)
+  int num_ctas;
+};
+cudaError_t launch_gqa_decode(const GqaPlan& plan, cudaStream_t stream);
+
 // Resolves cuTensorMapEncodeTiled through the runtime (no link-time libcuda).
 using TensorMapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                        const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,

@@ -1,6 +1,7 @@
-"""The C-ABI library builds, loads and exports what include/moe.h declares; host-side
+"""The C-ABI library builds, loads and exports what include/*.h declares; host-side
 argument checks reject bad calls before any CUDA work (no GPU needed)."""
 import ctypes
+import glob
 import os
 import re
 
@@ -9,7 +10,7 @@ import pytest
 from routed_expert_ffn_softmax_gb300 import build as moe_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "moe.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
 BF16, INT8 = 0, 1
@@ -29,19 +30,25 @@ def lib():
     L.moe_route_topk.argtypes = [P, i, i, i, P, P, P, P, P, P, P, P, P]
     L.moe_gather.argtypes = [P, i, i, i, P, P, P]
     L.moe_combine.argtypes = [P, P, P, i, i, i, P, P]
+    L.moe_gqa_workspace_size.argtypes = [i, i, i, i, i]
+    L.moe_gqa_workspace_size.restype = z
+    L.moe_gqa_decode.argtypes = [P, P, P, P, i, i, i, i, i, ctypes.c_float, P, P, z, P]
     return L
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
-        "moe_expert_ffn", "moe_expert_ffn_noalloc", "moe_combine", "moe_ffn_forward"])
+        "moe_expert_ffn", "moe_expert_ffn_noalloc", "moe_combine", "moe_ffn_forward",
+        "moe_gqa_workspace_size", "moe_gqa_decode"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -130,3 +137,41 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.moe_expert_ffn(F, F, F, F, F, F, F, None, None, None, BF16, 256, 512, 8, -1, F, F, ws_need, None) == INVALID
     assert lib.moe_expert_ffn(F, F, F, F, F, F, F, None, None, None, BF16, 256, 512, 8, 0, F, F, ws_need, None) == OK
     assert lib.moe_expert_ffn(F, F, F, F, F, F, F, None, None, None, INT8, 256, 512, 8, 8, F, F, ws_need, None) == INVALID
+
+
+def test_gqa_workspace_size(lib):
+    ws = lib.moe_gqa_workspace_size
+    n = ws(64, 32, 4, 128, 8192)
+    assert n > 0 and n % 256 == 0
+    assert ws(2048, 64, 4, 128, 32768) == n           # independent of the sizes
+    assert ws(1, 32, 3, 128, 16) == 0                 # h_q not a multiple of h_kv
+    assert ws(1, 32, 1, 128, 16) == 0                 # group of 32 > 16
+    assert ws(1, 32, 4, 64, 16) == 0                  # head dim other than 128
+    assert ws(2049, 32, 4, 128, 16) == 0              # more sequences than supported
+    assert ws(1, 32, 4, 128, 0) == 0                  # empty cache
+    assert ws(-1, 32, 4, 128, 16) == 0
+
+
+def gqa(lib, B=2, h_q=32, h_kv=4, d=128, L=256, scale=0.088, q=FAKE, k=FAKE, v=FAKE, lens=FAKE, out=FAKE, ws=FAKE,
+        ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.moe_gqa_workspace_size(2, 32, 4, 128, 256)
+    return lib.moe_gqa_decode(q, k, v, lens, B, h_q, h_kv, d, L, scale, out, ws, ws_bytes, None)
+
+
+def test_gqa_rejects_bad_arguments_before_launch(lib):
+    assert gqa(lib, B=-1) == INVALID
+    assert gqa(lib, h_kv=3) == INVALID
+    assert gqa(lib, h_q=64, h_kv=2) == UNSUPPORTED     # G = 32
+    assert gqa(lib, d=64) == UNSUPPORTED
+    assert gqa(lib, B=5000) == UNSUPPORTED
+    assert gqa(lib, L=0) == INVALID
+    assert gqa(lib, scale=float("inf")) == INVALID
+    assert gqa(lib, scale=float("nan")) == INVALID
+    assert gqa(lib, q=None) == INVALID
+    assert gqa(lib, lens=None) == INVALID
+    assert gqa(lib, k=FAKE + 8) == INVALID             # caches must be 16-byte aligned
+    assert gqa(lib, lens=FAKE + 2) == INVALID
+    assert gqa(lib, ws=FAKE + 16) == INVALID
+    assert gqa(lib, ws_bytes=4096) == WORKSPACE
+    assert gqa(lib, B=0, q=None, k=None, v=None, lens=None, out=None, ws=None) == OK
