@@ -36,9 +36,12 @@ extern "C" {
  * as they are supported). Returns 0 when the sizes are invalid or unsupported. Pure host
  * computation.
  *
- * The first 4 bytes of the workspace are a status word, cleared by each call: 4 means some
- * seq_lens entry was outside [0, L_cap] (that sequence's output is then 0); 1-3 mean a kernel
- * gave up a bounded wait (which does not happen in correct operation; outputs undefined).
+ * The workspace must be zero-filled before its first use (for example with cudaMemset); every
+ * call leaves it ready for the next one, so calls need no clearing step between them. The first
+ * 4 bytes are a status word that calls set and never clear: 4 means some seq_lens entry was
+ * outside [0, L_cap] (that sequence's output is then 0; the workspace stays usable, zero the
+ * word to reset it); 1-3 mean a kernel gave up a bounded wait (which does not happen in correct
+ * operation; outputs undefined, and the whole workspace must be zero-filled again before reuse).
  */
 size_t moe_gqa_workspace_size(int B, int h_q, int h_kv, int d, int L_cap);
 
@@ -53,7 +56,8 @@ size_t moe_gqa_workspace_size(int B, int h_q, int h_kv, int d, int L_cap);
  *   out       [B, h_q, d] bf16 out
  *   workspace >= moe_gqa_workspace_size(...) bytes (device, 256-byte aligned)
  * Supported: d = 128, 1 <= G = h_q / h_kv <= 16 (h_q a multiple of h_kv), 0 <= B <= 2048,
- * L_cap >= 1; otherwise MOE_ERR_UNSUPPORTED (d, G, B) or MOE_ERR_INVALID_ARG. q, the caches and
+ * L_cap >= 1, B * h_kv * ceil(L_cap / 128) < 2^31; otherwise MOE_ERR_UNSUPPORTED (d, G, B, the
+ * tile count) or MOE_ERR_INVALID_ARG. q, the caches and
  * out must be 16-byte aligned, seq_lens 4-byte aligned. B = 0 is a no-op.
  * Each key/value row attended to is read from memory once per call. The result is
  * deterministic for a given device and does not depend on timing.

@@ -185,10 +185,11 @@ def moe_gqa_workspace_size(B: int, h_q: int, h_kv: int, d: int, L_cap: int) -> i
 
 
 def alloc_gqa_workspace(B, h_q, h_kv, d, L_cap, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for moe_gqa_decode (it must start zeroed; calls keep it so)."""
     n = moe_gqa_workspace_size(B, h_q, h_kv, d, L_cap)
     if n == 0:
         raise ValueError("invalid or unsupported sizes for moe_gqa_workspace_size")
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def moe_gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out, workspace, stream=None) -> None:

@@ -296,7 +296,8 @@ constexpr size_t kGqaPartialBytes = sizeof(float) * static_cast<size_t>(kMaxCtas
 moe_status_t gqa_check(int B, int h_q, int h_kv, int d, int L_cap) {
   if (B < 0 || h_q < 1 || h_kv < 1 || d < 1 || L_cap < 1 || h_q % h_kv) return MOE_ERR_INVALID_ARG;
   if (d != 128 || h_q / h_kv > 16 || B > moe::kGqaMaxSeqs) return MOE_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(B) * h_q > INT32_MAX || static_cast<int64_t>(B) * h_kv > INT32_MAX)
+  // the kernel counts key tiles of 128 rows over all (sequence, key/value head) pairs in 32 bits
+  if (static_cast<int64_t>(B) * h_q > INT32_MAX || static_cast<int64_t>(B) * h_kv * ((L_cap + 127) / 128) > INT32_MAX)
     return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -324,7 +325,8 @@ moe_status_t moe_gqa_decode(const uint16_t* q, const uint16_t* k_cache, const ui
   if (sms < 1) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  if (cudaMemsetAsync(ws, 0, kCountersOffset + 4 * kMaxCtas, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // No clearing launch here: the merge counters are left zero by every call, so consecutive calls
+  // are back-to-back kernels that overlap launch and prologue (programmatic dependent launch).
   moe::GqaPlan plan{};
   plan.q = q;
   plan.k_cache = k_cache;

@@ -175,3 +175,9 @@ def test_gqa_rejects_bad_arguments_before_launch(lib):
     assert gqa(lib, ws=FAKE + 16) == INVALID
     assert gqa(lib, ws_bytes=4096) == WORKSPACE
     assert gqa(lib, B=0, q=None, k=None, v=None, lens=None, out=None, ws=None) == OK
+
+
+def test_gqa_tile_count_bound(lib):
+    # 2048 sequences x 64 key/value heads x 2^17 tiles of 128 rows overflows the 32-bit tile count
+    assert lib.moe_gqa_workspace_size(2048, 64, 64, 128, 1 << 24) == 0
+    assert lib.moe_gqa_workspace_size(2048, 64, 64, 128, 1 << 20) > 0

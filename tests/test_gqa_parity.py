@@ -107,15 +107,19 @@ def test_empty_and_invalid_lengths():
     assert torch.count_nonzero(out[0].float()) == 0 and torch.count_nonzero(out[2].float()) == 0
     bound_check(out, q, k, v, ln, cfg.scale, "empty sequences")
     # a length past the cache capacity: reported in the status word, that sequence gets 0
+    ws = moe.alloc_gqa_workspace(4, 32, 4, 128, 256, DEV)
     bad = ln.clone()
     bad[1] = 257
-    out2, st2 = gpu_decode(q, k, v, bad, cfg.scale)
+    out2, st2 = gpu_decode(q, k, v, bad, cfg.scale, ws)
     assert st2 == 4
     assert torch.count_nonzero(out2[1].float()) == 0
     bound_check(out2[3:4], q[3:4], k[3:4], v[3:4], ln[3:4], cfg.scale, "beside a bad length")
-    # and the next call on the same workspace clears the status again
-    out3, st3 = gpu_decode(q, k, v, ln, cfg.scale)
-    assert st3 == 0 and torch.equal(out3, out)
+    # the status is sticky; the workspace stays usable, and zeroing the word resets it
+    out3, st3 = gpu_decode(q, k, v, ln, cfg.scale, ws)
+    assert st3 == 4 and torch.equal(out3, out)
+    ws[:4] = 0
+    out4, st4 = gpu_decode(q, k, v, ln, cfg.scale, ws)
+    assert st4 == 0 and torch.equal(out4, out)
 
 
 def test_deterministic_and_workspace_reuse():
