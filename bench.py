@@ -1,4 +1,4 @@
-"""Benchmark of the routed-expert FFN decode step on GB300.
+"""Benchmark of the routed-expert FFN decode step on GB300 (and of decode GQA attention).
 
 One step = one pass of the whole path (route -> gather -> gate+up -> down -> combine)
 through the C ABI over one decode batch of synthetic tokens. Default workload: the
@@ -7,8 +7,15 @@ T=16 tokens (about 4 tokens per expert). The metric is the weight-stream bandwid
 bytes of the active experts' weights (each read once) per second; tokens/s is
 reported beside it.
 
+`--op attention` measures decode-phase GQA attention instead (moe_gqa_decode, one new
+token per sequence against its key/value cache): one step = one call over the batch;
+the metric is the bandwidth of the key/value rows read (each once) per second, with
+sequences/s beside it. Default workload: Qwen3-30B-A3B-shaped heads (32 query heads,
+4 key/value heads, d = 128), 64 sequences of 512..8192 tokens.
+
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
         [--config NAME] [--T T] [--sweep] [--no-cpu-baseline]
+        [--op attention [--attn-config NAME]]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path is not sharded); value = all ranks' bytes / the slowest rank's time.
 `--impl reference` times the CPU oracle on the host cores instead (rank 0 only).
@@ -35,6 +42,7 @@ import moe_workloads as mw  # noqa: E402
 METRIC = "expert-FFN decode weight-stream HBM GB/s (% of peak) and tokens/s, 1 GB300"
 METRIC_HOST = ("expert-FFN decode weight-stream GB/s with the expert weights in Grace LPDDR5X, read over "
                "NVLink-C2C (% of the measured host->device copy rate) and tokens/s, 1 GB300")
+METRIC_ATTN = "decode GQA attention key/value-cache read GB/s (% of peak) and sequences/s, 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -96,29 +104,29 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# the sources of the expert kernels (the roofline's kernels) and of their launches
+# the sources of the roofline kernels and of their launches: the expert kernels, the attention kernel
 EXPERT_SOURCES = ("expert_tc.cuh", "expert_pair.cuh", "moe_device.cuh", "expert_launch.cu")
+ATTN_SOURCES = ("gqa_decode.cu", "moe_device.cuh")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the expert kernels' sources; a recorded DRAM-traffic figure is used only while it
-    matches."""
+def kernel_source_hash(sources=EXPERT_SOURCES) -> str:
+    """Hash of a kernel's sources; a recorded DRAM-traffic figure is used only while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "routed_expert_ffn_softmax_gb300", "csrc")
-    for n in EXPERT_SOURCES:
+    for n in sources:
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, sources=EXPERT_SOURCES):
     """DRAM bytes per launch from a committed ncu capture, if it matches the current kernels."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d[workload]
-        if e.get("kernel_source_hash") == kernel_source_hash():
+        if e.get("kernel_source_hash") == kernel_source_hash(sources):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -173,6 +181,18 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def per_step_times(step, n, stream):
+    """ms of n single steps, each between its own two events (after the timed region: the events
+    themselves cost the overlap between steps)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    for i in range(n):
+        evs[i].record(stream)
+        step(i)
+    evs[-1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
 
 
 # ------------------------------------------------------------------ workload
@@ -260,18 +280,17 @@ def bench_ours(args, cfg, T):
         barrier_sync()
         if moe.workspace_status(ws) != 0:
             raise RuntimeError("a kernel reported a timed-out wait during warm-up")
+        # two events around the whole timed region: an event between steps would end the overlap
+        # of one step's last kernel with the next step's first (programmatic dependent launch)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         ev0.record(stream)
         for i in range(args.steps):
-            evs[i].record(stream)
             step(i % copies)
-        evs[-1].record(stream)
         ev1.record(stream)
         barrier_sync()
     clocks = clk.summary()
     total_ms = ev0.elapsed_time(ev1)
-    per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    per_step = per_step_times(lambda i: step(i % copies), min(args.steps, 100), stream)
     if moe.workspace_status(ws) != 0:
         raise RuntimeError("a kernel reported a timed-out wait")
     bytes_timed = sum(wl.weight_bytes(i % copies) for i in range(args.steps))
@@ -519,6 +538,222 @@ def bench_reference(args, cfg, T):
     }
 
 
+# ------------------------------------------------------------------ decode GQA attention
+class AttnWorkload:
+    """One decode batch: queries, key/value caches (device-resident decode state, larger than L2 for
+    the bench's workloads, so every call streams them from HBM) and the sequence lengths."""
+
+    def __init__(self, acfg: mw.AttnConfig, device, seed: int = 0):
+        self.acfg = acfg
+        self.q, self.k, self.v, self.lens = mw.make_attention(acfg, seed=seed, device=device)
+        self.L_cap = self.k.shape[2]
+        self.kv_bytes = mw.attention_kv_bytes(self.lens, acfg.h_kv, acfg.d)
+        self.io_bytes = 2 * self.q.numel() * 2  # query in, output out (bf16)
+
+
+def bench_attention_ours(args, acfg):
+    import routed_expert_ffn_softmax_gb300 as moe
+    from routed_expert_ffn_softmax_gb300 import build as moe_build
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        moe_build.build()
+    if ws_n > 1:
+        dist.barrier()
+    moe.load()
+    wl = AttnWorkload(acfg, dev)
+    stream = torch.cuda.current_stream()
+    ws = moe.alloc_gqa_workspace(acfg.B, acfg.h_q, acfg.h_kv, acfg.d, wl.L_cap, dev)
+    out = torch.empty(acfg.B, acfg.h_q, acfg.d, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        moe.moe_gqa_decode(wl.q, wl.k, wl.v, wl.lens, acfg.scale, out, ws, stream)
+
+    def barrier_sync():
+        torch.cuda.synchronize()
+        if ws_n > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            step()
+        barrier_sync()
+        if moe.workspace_status(ws) != 0:
+            raise RuntimeError("the attention kernel reported a nonzero status during warm-up")
+        # two events around the whole timed region (see bench_ours)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier_sync()
+    clocks = clk.summary()
+    total_ms = ev0.elapsed_time(ev1)
+    per_step = per_step_times(lambda i: step(), min(args.steps, 100), stream)
+    if moe.workspace_status(ws) != 0:
+        raise RuntimeError("the attention kernel reported a nonzero status")
+    total_ms, value, seq_s = aggregate_over_ranks(total_ms, wl.kv_bytes * args.steps, acfg.B * args.steps, ws_n, dev)
+    # the one kernel of a step is the roofline's kernel: its average launch is the timed region / steps
+    avg_ms = total_ms / args.steps
+    achieved = (wl.kv_bytes + wl.io_bytes) / (avg_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    workload_name = acfg.name
+
+    # ---- end to end through the C ABI: query and lengths in from pinned host memory, output back
+    q_h = wl.q.cpu().pin_memory()
+    lens_h = wl.lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d = torch.empty_like(wl.q)
+    lens_d = torch.empty_like(wl.lens)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        moe.moe_gqa_decode(q_d, wl.k, wl.v, lens_d, acfg.scale, out, ws, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier_sync()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    barrier_sync()
+    _, e2e_value, _ = aggregate_over_ranks(a.elapsed_time(b), wl.kv_bytes * args.steps, acfg.B * args.steps, ws_n,
+                                           dev)
+    lens = wl.lens.cpu()
+    result = {
+        "metric": METRIC_ATTN,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "ms_per_step_median": round(statistics.median(per_step), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (fp32 scores, softmax and accumulation)",
+        "data": "synthetic (seeded N(0,1) queries, keys and values; lengths uniform in the stated range)",
+        "pct_of_peak": round(100.0 * value / ws_n / peak, 2),
+        "sequences_per_s": round(seq_s, 1),
+        "config": {
+            "workload": workload_name, "h_q": acfg.h_q, "h_kv": acfg.h_kv, "group": acfg.group, "d": acfg.d,
+            "B": acfg.B, "seq_len_range": [acfg.len_lo, acfg.len_hi], "L_cap": wl.L_cap,
+            "seq_len_mean": round(float(lens.float().mean()), 1),
+            "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
+            "kv_bytes_per_step": wl.kv_bytes,
+            "l2": f"inputs larger than L2: each step reads {wl.kv_bytes / 1e6:.0f} MB of keys and values",
+        },
+        "roofline": {
+            "kernel": "gqa_decode_kernel (the step's only kernel)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(workload_name, ATTN_SOURCES),
+            "avg_launch_ms": round(avg_ms, 5),
+            "algorithmic_bytes_per_launch": wl.kv_bytes + wl.io_bytes,
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": wl.q.numel() * 2 + acfg.B * 4, "d2h_bytes_per_step": out.numel() * 2},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = attention_cpu_baseline(acfg, wl, budget_s=args.cpu_budget)
+    if ws_n > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def attention_oracle_rate(acfg, q, k, v, lens, budget_s):
+    """The oracle over the batch's sequences one at a time (cycling) until the budget is spent, at
+    least one; returns (key/value GB/s, sequences/s, sequences run, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    n = done_bytes = 0
+    while True:
+        b = n % q.shape[0]
+        ln = int(lens[b])
+        oracle.gqa_decode(q[b:b + 1], k[b:b + 1, :, :ln], v[b:b + 1, :, :ln], lens[b:b + 1], acfg.scale)
+        done_bytes += ln * acfg.h_kv * acfg.d * 4
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done_bytes / dt / 1e9, n / dt, n, dt
+
+
+def attention_cpu_baseline(acfg, wl, budget_s):
+    q, lens = wl.q.cpu(), wl.lens.cpu()
+    nseq = min(acfg.B, 8)
+    k, v = wl.k[:nseq].cpu(), wl.v[:nseq].cpu()
+    gbs, seq_s, n, dt = attention_oracle_rate(acfg, q[:nseq], k, v, lens[:nseq], budget_s)
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+            "sequences_per_s": round(seq_s, 3),
+            "sample": f"{n} sequence evaluations cycling over the first {nseq} sequences of the batch "
+                      f"({dt:.1f} s); GB/s = key/value bytes those sequences read / time"}
+
+
+def bench_attention_reference(args, acfg):
+    """The CPU oracle on the host cores, same metric and config (rank 0 only)."""
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    nseq = min(acfg.B, 8)
+    lens_all = mw.draw_seq_lens(acfg.B, acfg.len_lo, acfg.len_hi, acfg.seed)
+    q, k, v, lens = mw.make_attention(acfg, seq_lens=lens_all[:nseq])
+    nsteps = args.steps + args.warmup
+    per_step_budget = max(0.02, args.cpu_budget * 4 / nsteps)
+    vals, times = [], []
+    kv_full = mw.attention_kv_bytes(lens_all, acfg.h_kv, acfg.d)
+    for i in range(nsteps):
+        gbs, seq_s, n, dt = attention_oracle_rate(acfg, q, k, v, lens, per_step_budget)
+        if i >= args.warmup:
+            vals.append(gbs)
+            times.append(kv_full / (gbs * 1e9))
+    value = statistics.mean(vals)
+    ms_step = 1e3 * statistics.mean(times)
+    return {
+        "impl": "reference",
+        "metric": METRIC_ATTN,
+        "value": round(value, 3),
+        "unit": "GB/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (CPU oracle), bf16 inputs",
+        "data": "synthetic (seeded N(0,1) queries, keys and values; lengths uniform in the stated range)",
+        "sequences_per_s": round(acfg.B / (ms_step * 1e-3), 3),
+        "config": {"workload": acfg.name, "h_q": acfg.h_q, "h_kv": acfg.h_kv, "group": acfg.group, "d": acfg.d,
+                   "B": acfg.B, "seq_len_range": [acfg.len_lo, acfg.len_hi]},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": f"each step runs the oracle over the first {nseq} sequences of the batch (cycling) "
+                                   f"for about {per_step_budget:.2f} s and scales to the whole batch's key/value bytes"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,9 +768,19 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also measure every T of the workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--op", choices=("ffn", "attention"), default="ffn",
+                    help="ffn: the routed-expert FFN (default); attention: decode GQA attention")
+    ap.add_argument("--attn-config", default="qwen3_30b_attn",
+                    choices=sorted(n for n in mw.ATTN_CONFIGS if n != "attn_tiny"))
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op == "attention":
+        acfg = mw.ATTN_CONFIGS[args.attn_config]
+        res = bench_attention_reference(args, acfg) if args.impl == "reference" else bench_attention_ours(args, acfg)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
     cfg = mw.CONFIGS[args.config]
     if args.impl == "reference":
         res = bench_reference(args, cfg, args.T)

@@ -13,8 +13,9 @@
 // it, whose probabilities are written as zero) stays in shared memory for the whole piece.
 //
 // Numerics: scores and the online softmax in fp32 (base-2 exponent, scale * log2(e) folded into
-// the scores), probabilities rounded to bf16 for the second product (its operands must share one
-// 16-bit type with V), fp32 accumulation, output rounded once to bf16.
+// the scores, the hardware's approximate 2^x at about 2^-22 relative error), probabilities rounded
+// to bf16 for the second product (its operands must share one 16-bit type with V), fp32
+// accumulation, output rounded once to bf16.
 //
 // Work split: the key tiles of all (sequence, key/value head) segments form one list; each CTA
 // (one per SM) takes a contiguous range of it (stream-K), so long and short sequences balance to
@@ -451,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* rm = red_max + sb * 4 * kN + h;
             const float mt = fmaxf(fmaxf(rm[0], rm[kN]), fmaxf(rm[2 * kN], rm[3 * kN]));
             const float m_new = fmaxf(m_run[h], mt);  // finite: every tile holds a valid key
-            alpha[h] = exp2f(m_run[h] - m_new);
-            const float pr = exp2f(sv[h] - m_new);
+            alpha[h] = ex2_approx(m_run[h] - m_new);
+            const float pr = ex2_approx(sv[h] - m_new);
             l_thr[h] = fmaf(l_thr[h], alpha[h], pr);
             m_run[h] = m_new;
             if (h < p.G) {

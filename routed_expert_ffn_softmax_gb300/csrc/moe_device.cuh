@@ -244,6 +244,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, subnormal results flushed to zero, 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Maximum of v over the 32 lanes of the warp in one instruction (NaN inputs are skipped).
 __device__ __forceinline__ float warp_max_f32(float v) {
   float r;

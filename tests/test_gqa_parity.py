@@ -7,7 +7,7 @@ each) and the output is rounded to bf16 once (<= 2^-8 |o|). Per output element,
     |gpu - o| <= 2^-8 * sum_i p_i |v_i| + 2^-8 * |o| + slack,
 where sum_i p_i |v_i| is the oracle's attention over |V| (computed exactly, float64), and the
 slack 2^-12 * sum_i p_i |v_i| + 1e-6 covers the fp32 scores (bf16 products, fp32 sums of 128),
-exp2f and the fp32 accumulation over tiles and pieces. A wrong key/value head, a transposed
+the approximate 2^x (relative error about 2^-22) and the fp32 accumulation over tiles and pieces. A wrong key/value head, a transposed
 operand or a lost tile changes outputs by about |o| itself, far above this bound for the
 random inputs here.
 """
