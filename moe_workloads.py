@@ -52,7 +52,7 @@ class MoEConfig:
     I: int            # intermediate size (gate/up output rows, down reduction)
     E: int            # routed experts
     top_k: int
-    wtype: str        # "bf16" or "int8"
+    wtype: str        # "bf16", "int8" or "int8_residual" (gate/up as W^Q + W^R, both INT8)
     T: Tuple[int, ...]  # token counts the workload is run at
     skew_experts: Tuple[int, ...] = ()
     skew: float = 0.0
@@ -60,11 +60,12 @@ class MoEConfig:
 
     @property
     def weight_bytes_per_expert(self) -> int:
-        """Algorithmic weight-stream bytes of one expert (3 matrices + scales)."""
-        per = 3 * self.H * self.I * (1 if self.wtype == "int8" else 2)
-        if self.wtype == "int8":
-            per += 4 * (2 * self.I * (self.H // GROUP) + self.H * (self.I // GROUP))
-        return per
+        """Algorithmic weight-stream bytes of one expert (3 matrices + scales; the residual split
+        streams gate and up twice: W^Q and W^R)."""
+        if self.wtype == "bf16":
+            return 3 * self.H * self.I * 2
+        gu = 2 if self.wtype == "int8_residual" else 1  # streams of gate and of up
+        return (2 * gu + 1) * self.H * self.I + 4 * (2 * gu * self.I * (self.H // GROUP) + self.H * (self.I // GROUP))
 
 
 CONFIGS: Dict[str, MoEConfig] = {
@@ -79,6 +80,7 @@ CONFIGS: Dict[str, MoEConfig] = {
                   skew_experts=(0, 1), skew=2.0),
         MoEConfig("dsv3", 7168, 2048, 256, 8, "bf16", (1, 16, 128, 512)),
         MoEConfig("qwen3_int8", 4096, 1536, 128, 8, "int8", (1, 8, 64, 256)),
+        MoEConfig("qwen3_int8_residual", 4096, 1536, 128, 8, "int8_residual", (1, 8, 64, 256)),
     )
 }
 
@@ -140,12 +142,25 @@ def quantize_int8_groupwise(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor
     return q.to(torch.int8).reshape(w.shape), s.contiguous()
 
 
+def quantize_int8_residual(w: torch.Tensor):
+    """Residual-split preparation (RapidMoE, arXiv 2610.01265, "Residual-Split Representation"):
+    W^Q = the group-128 INT8 quantisation of w, W^R = the group-128 INT8 quantisation of the fp32
+    residual w - W^Q (the pages give no bit width; both parts are INT8 here).
+    Returns (qQ int8, sQ fp32, qR int8, sR fp32), scales [..., rows, K/128]."""
+    qQ, sQ = quantize_int8_groupwise(w)
+    K = w.shape[-1]
+    deq = (qQ.float().reshape(*w.shape[:-1], K // GROUP, GROUP) * sQ.unsqueeze(-1)).reshape(w.shape)
+    qR, sR = quantize_int8_groupwise(w.float() - deq)
+    return qQ, sQ, qR, sR
+
+
 def make_layer(cfg: MoEConfig, seed: Optional[int] = None, device="cpu",
                experts: Optional[Sequence[int]] = None) -> Dict[str, torch.Tensor]:
     """Expert weights of one MoE layer: W_gate/W_up [E,I,H], W_down [E,H,I] (+ INT8 scales).
 
     For INT8 the returned W_* are int8 and s_* hold the fp32 group scales
-    (s_gate/s_up [E,I,H/128], s_down [E,H,I/128]); for BF16 s_* are None.
+    (s_gate/s_up [E,I,H/128], s_down [E,H,I/128]); for BF16 s_* are None. The residual split
+    adds Wr_gate/Wr_up (int8 residual parts) and sr_gate/sr_up (their scales).
     """
     seed = cfg.seed if seed is None else seed
     wg = draw_weights(cfg.E, cfg.I, cfg.H, seed, _WG, device, experts)
@@ -153,6 +168,15 @@ def make_layer(cfg: MoEConfig, seed: Optional[int] = None, device="cpu",
     wd = draw_weights(cfg.E, cfg.H, cfg.I, seed, _WD, device, experts)
     if cfg.wtype == "bf16":
         return dict(W_gate=wg, W_up=wu, W_down=wd, s_gate=None, s_up=None, s_down=None)
+    if cfg.wtype == "int8_residual":
+        qg, sg, rg, srg = quantize_int8_residual(wg)
+        del wg
+        qu, su, ru, sru = quantize_int8_residual(wu)
+        del wu
+        qd, sd = quantize_int8_groupwise(wd)
+        del wd
+        return dict(W_gate=qg, W_up=qu, W_down=qd, s_gate=sg, s_up=su, s_down=sd,
+                    Wr_gate=rg, Wr_up=ru, sr_gate=srg, sr_up=sru)
     qg, sg = quantize_int8_groupwise(wg)
     del wg
     qu, su = quantize_int8_groupwise(wu)

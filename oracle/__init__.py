@@ -57,6 +57,10 @@ def _load():
             lib.oracle_forward.restype = i
             lib.oracle_f32_to_bf16.argtypes = [P, ctypes.c_long, P]
             lib.oracle_f32_to_bf16.restype = None
+            lib.oracle_gateup_token_residual.argtypes = [P] * 9 + [i, i, P, P, P]
+            lib.oracle_gateup_token_residual.restype = None
+            lib.oracle_forward_residual.argtypes = [P] * 12 + [i, i, i, i, i, P, P]
+            lib.oracle_forward_residual.restype = i
             lib.oracle_gqa_decode.argtypes = [P, P, P, P, i, i, i, i, i, ctypes.c_float, P, P]
             lib.oracle_gqa_decode.restype = i
             lib.oracle_f64_to_bf16.argtypes = [P, ctypes.c_long, P]
@@ -179,6 +183,39 @@ def forward(x, logits, W_gate, W_up, W_down, s_gate=None, s_up=None, s_down=None
     if rc != 0:
         raise ValueError("oracle_forward: bad sizes")
     return res
+
+
+def gateup_token_residual(x_row, qQg, sQg, qRg, sRg, qQu, sQu, qRu, sRu):
+    """Residual-split gate/up of one token through one expert ([I,H] int8 parts, [I,H/128] scales):
+    returns (h bf16 bits [I], g f32 [I], u f32 [I])."""
+    x = _np(x_row, np.uint16)
+    parts = [_np(a, np.int8 if i % 2 == 0 else np.float32) for i, a in enumerate((qQg, sQg, qRg, sRg, qQu, sQu,
+                                                                                 qRu, sRu))]
+    I, H = parts[0].shape
+    h = np.zeros(I, np.uint16)
+    g = np.zeros(I, np.float32)
+    u = np.zeros(I, np.float32)
+    _load().oracle_gateup_token_residual(_p(x), *(_p(a) for a in parts), H, I, _p(h), _p(g), _p(u))
+    return h, g, u
+
+
+def forward_residual(x, logits, W_gate, s_gate, Wr_gate, sr_gate, W_up, s_up, Wr_up, sr_up, W_down, s_down,
+                     top_k=8):
+    """Routed-expert FFN with residual-split gate/up (see moe_oracle.cpp). Returns dict(out, out_f32)."""
+    xa = _np(x, np.uint16)
+    lg = _np(logits, np.float32)
+    q = [_np(a, np.int8) for a in (W_gate, Wr_gate, W_up, Wr_up, W_down)]
+    sc = [_np(a, np.float32) for a in (s_gate, sr_gate, s_up, sr_up, s_down)]
+    T, H = xa.shape
+    E, I, _ = q[0].shape
+    out = np.zeros((T, H), np.uint16)
+    of = np.zeros((T, H), np.float32)
+    rc = _load().oracle_forward_residual(_p(xa), _p(lg), _p(q[0]), _p(sc[0]), _p(q[1]), _p(sc[1]), _p(q[2]),
+                                         _p(sc[2]), _p(q[3]), _p(sc[3]), _p(q[4]), _p(sc[4]), T, H, I, E, top_k,
+                                         _p(out), _p(of))
+    if rc != 0:
+        raise ValueError("oracle_forward_residual: bad sizes")
+    return dict(out=out, out_f32=of)
 
 
 def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float):

@@ -23,6 +23,13 @@
 //    (round-to-nearest-even) before the down projection; SiLU(g) = g / (1 + exp(-g)).
 //  * INT8 variant (§8.1, Figure 11: symmetric group-wise quantisation): the weight
 //    is dequantised as w = float(q) * scale[row][k / 128] in fp32, then used as above.
+//  * Residual-split variant (RapidMoE, arXiv 2610.01265, "Residual-Split Representation" and
+//    "GLU Architecture Adoption"): gate and up are held as a low-precision part W^Q and the
+//    quantised residual W^R of W - W^Q, both symmetric group-128 INT8 here (the pages name no
+//    bit width), and the high-precision weight is W^H = W^Q + W^R, dequantised as
+//    w = float(qQ) * sQ + float(qR) * sR in fp32; gate and up preactivations are therefore
+//    W^Q x + W^R x. Down keeps one separately quantised INT8 copy (the pages' "dual
+//    quantization" of down_proj, which is not split).
 //  * Combine: out[t] = sum over slots j (in slot order) of w_j * y_j, fp32, then
 //    rounded once to bf16. The pages leave the combine to the framework (§4.1 ends at
 //    "write the output back in the standard row-major layout").
@@ -34,7 +41,9 @@
 // Parity pins (tests/test_oracle_pins.py): fp64 brute force over all experts with
 // masked weights, identity-weight closed form, x = 0, top_k = 1 and top_k = E closed
 // forms, identical-expert and token-permutation invariants, power-of-two-scale INT8
-// equivalence, hand-worked routing fixtures.
+// equivalence, hand-worked routing fixtures; residual split (tests/test_oracle_residual_pins.py):
+// a zero residual reduces to the INT8 oracle, a zero low part to the BF16 oracle, and gate/up
+// preactivations are the sum of the two parts' (linearity).
 
 #include <algorithm>
 #include <cmath>
@@ -78,6 +87,20 @@ float weight_at(const void* W, const float* scales, int wtype, int K, long row, 
 float dot_row(const float* a, const void* W, const float* scales, int wtype, int K, long row) {
   float acc = 0.0f;
   for (long k = 0; k < K; ++k) acc += a[k] * weight_at(W, scales, wtype, K, row, k);
+  return acc;
+}
+
+// Residual-split weight W^H[row][k] = float(qQ) * sQ + float(qR) * sR (int8, group-128 scales).
+float residual_weight_at(const int8_t* qQ, const float* sQ, const int8_t* qR, const float* sR, int K, long row,
+                         long k) {
+  const long g = row * (K / 128) + k / 128;
+  return static_cast<float>(qQ[row * K + k]) * sQ[g] + static_cast<float>(qR[row * K + k]) * sR[g];
+}
+
+float dot_row_residual(const float* a, const int8_t* qQ, const float* sQ, const int8_t* qR, const float* sR,
+                       int K, long row) {
+  float acc = 0.0f;
+  for (long k = 0; k < K; ++k) acc += a[k] * residual_weight_at(qQ, sQ, qR, sR, K, row, k);
   return acc;
 }
 
@@ -221,6 +244,59 @@ int oracle_forward(const uint16_t* x, const float* logits, const void* Wg, const
   }
   if (ids_out) std::memcpy(ids_out, ids.data(), P * 4);
   if (w_out) std::memcpy(w_out, w.data(), P * 4);
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Residual-split gate/up of one token through one expert (definition at the top):
+//   g_i = sum_c x[c] * (qQg * sQg + qRg * sRg)[i][c], u likewise, h_i = bf16(SiLU(g_i) * u_i).
+// qQ*/qR*: that expert's [I,H] int8 parts; sQ*/sR*: their [I,H/128] scales.
+void oracle_gateup_token_residual(const uint16_t* x, const int8_t* qQg, const float* sQg, const int8_t* qRg,
+                                  const float* sRg, const int8_t* qQu, const float* sQu, const int8_t* qRu,
+                                  const float* sRu, int H, int I, uint16_t* h_out, float* g_out, float* u_out) {
+  std::vector<float> xf(H);
+  for (int c = 0; c < H; ++c) xf[c] = bf16_bits_to_float(x[c]);
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < I; ++i) {
+    float g = dot_row_residual(xf.data(), qQg, sQg, qRg, sRg, H, i);
+    float u = dot_row_residual(xf.data(), qQu, sQu, qRu, sRu, H, i);
+    h_out[i] = float_to_bf16_bits(silu(g) * u);
+    if (g_out) g_out[i] = g;
+    if (u_out) u_out[i] = u;
+  }
+}
+
+// Whole routed-expert FFN with residual-split gate/up (INT8 + INT8 residual) and INT8 down:
+// routing, gather and combine as in oracle_forward; W_gate/W_up [E,I,H] int8 with their residual
+// parts Wr_gate/Wr_up and scales [E,I,H/128] each; W_down [E,H,I] int8, s_down [E,H,I/128].
+int oracle_forward_residual(const uint16_t* x, const float* logits, const int8_t* Wg, const float* sg,
+                            const int8_t* Wgr, const float* sgr, const int8_t* Wu, const float* su,
+                            const int8_t* Wur, const float* sur, const int8_t* Wd, const float* sd, int T, int H,
+                            int I, int E, int k, uint16_t* out, float* out_f32) {
+  if (T < 0 || H < 128 || I < 128 || E < 1 || k < 1 || k > E || H % 128 || I % 128) return -1;
+  if (T == 0) return 0;
+  const long P = static_cast<long>(T) * k;
+  std::vector<int32_t> ids(P), counts(E), offsets(E + 1), sorted_token(P), inv_pos(P), active(E);
+  std::vector<float> w(P);
+  int32_t num_active = 0;
+  oracle_route(logits, T, E, k, ids.data(), w.data(), counts.data(), offsets.data(), sorted_token.data(),
+               inv_pos.data(), active.data(), &num_active);
+  const size_t n_e = static_cast<size_t>(I) * H;          // elements of one expert's matrix
+  const size_t s_gu = static_cast<size_t>(I) * (H / 128);  // scales per expert, gate/up
+  const size_t s_d = static_cast<size_t>(H) * (I / 128);   // scales per expert, down
+  std::vector<uint16_t> h(I);
+  std::vector<float> y(static_cast<size_t>(k) * H);
+  for (int t = 0; t < T; ++t) {
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[t * k + j];
+      oracle_gateup_token_residual(x + static_cast<long>(t) * H, Wg + e * n_e, sg + e * s_gu, Wgr + e * n_e,
+                                   sgr + e * s_gu, Wu + e * n_e, su + e * s_gu, Wur + e * n_e, sur + e * s_gu, H,
+                                   I, h.data(), nullptr, nullptr);
+      oracle_down_token(h.data(), Wd + e * n_e, sd + e * s_d, 1, H, I, y.data() + static_cast<size_t>(j) * H);
+    }
+    oracle_combine_token(y.data(), w.data() + static_cast<long>(t) * k, k, H, out + static_cast<long>(t) * H,
+                         out_f32 ? out_f32 + static_cast<long>(t) * H : nullptr);
+  }
   return 0;
 }
 

@@ -158,6 +158,11 @@ SMALL = [
     (12, 256, 256, 32, 1, "bf16", ()),      # top_k = 1
     (4, 256, 384, 8, 2, "int8", ()),
     (70, 384, 256, 8, 4, "int8", (2,)),
+    # about one token per expert (P = T * k <= E)
+    (3, 264, 200, 8, 2, "bf16", ()),        # H, I not multiples of 64
+    (6, 256, 512, 16, 2, "bf16", (0,)),     # expert 0 gets ~6 tokens, the others 0-1
+    (2, 128, 128, 4, 2, "int8", ()),
+    (8, 640, 384, 64, 8, "int8", (5,)),     # expert 5 gets all 8 tokens, 56 others one each
 ]
 
 
@@ -207,11 +212,12 @@ def test_expert_ffn_entry_point_matches_oracle(T, H, I, E, k, wtype, skew):
     assert_moe_close(to_np_f32(out), oracle.bf16_bits_to_f32(ref["out"]), wtype, "out")
 
 
+@pytest.mark.parametrize("T", [9, 4])
 @pytest.mark.parametrize("x_scale", [2.0 ** 17, 2.0 ** -30, 1.0])
-def test_int8_activation_range(x_scale):
+def test_int8_activation_range(x_scale, T):
     """INT8 runs the tensor cores in fp16; token rows far outside fp16's range (large or tiny)
     must still match the oracle to a purely relative bound."""
-    T, H, I, E, k = 9, 256, 384, 8, 2
+    H, I, E, k = 256, 384, 8, 2
     cfg, L, x, lg = small_case(T, H, I, E, k, "int8", seed=77)
     xs = (x.float() * x_scale).to(torch.bfloat16)
     out, _ = run_forward_ws(L, xs, lg, k)
@@ -261,7 +267,8 @@ def sampled_oracle_rows(cfg, Lg, x, lg, tokens):
 
 
 FULL = [("mixtral8x7b", 1), ("mixtral8x7b", 16), ("mixtral8x7b", 64), ("mixtral8x22b", 4),
-        ("mixtral8x22b_skew", 64), ("dsv3", 1), ("dsv3", 512), ("qwen3_int8", 1), ("qwen3_int8", 256)]
+        ("mixtral8x22b_skew", 64), ("dsv3", 1), ("dsv3", 16), ("dsv3", 512), ("qwen3_int8", 1), ("qwen3_int8", 8),
+        ("qwen3_int8", 256)]
 
 
 @pytest.mark.parametrize("name,T", FULL)

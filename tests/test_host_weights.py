@@ -45,6 +45,8 @@ def forward(W, x, lg, k, cfg):
     (8, 256, 512, 8, 2, "bf16", ()),
     (150, 64, 256, 4, 2, "bf16", (0, 1)),   # several passes per expert
     (70, 384, 256, 8, 4, "int8", (2,)),     # CTA-pair kernels, half-empty last row block
+    (2, 256, 512, 8, 2, "bf16", ()),        # about one token per expert
+    (4, 256, 384, 16, 4, "int8", ()),
 ])
 def test_host_weights_match_oracle_and_device_run(T, H, I, E, k, wtype, skew):
     cfg, L, x, lg = small_case(T, H, I, E, k, wtype, seed=5 * T + H, skew=skew)
