@@ -51,7 +51,7 @@ def kernels_per_step(cfg, T: int) -> int:
     else top-k and scan), gather (INT8: straight into the fp16 copy), the expert kernels (INT8
     adds the fp16 copy of h), combine."""
     route = 1 if (T <= 64 and T * cfg.top_k <= 1024) else 2
-    experts = 3 if cfg.wtype == "int8" else 2
+    experts = 2 if cfg.wtype == "bf16" else 3
     return route + 1 + experts + 1
 
 
@@ -195,6 +195,27 @@ def per_step_times(step, n, stream):
     return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
 
 
+def ffn_forward(moe, cfg, L, x, lg, out, ws, stream):
+    """moe_ffn_forward, or moe_ffn_forward_residual for residual-split INT8 weights."""
+    if cfg.wtype == "int8_residual":
+        moe.moe_ffn_forward_residual(x, lg, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
+                                     L["Wr_gate"], L["Wr_up"], L["sr_gate"], L["sr_up"], cfg.top_k, out, ws, stream)
+    else:
+        moe.moe_ffn_forward(x, lg, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
+                            cfg.top_k, out, ws, stream)
+
+
+def expert_ffn(moe, cfg, L, xg, r, Y, ws, stream):
+    """moe_expert_ffn, or moe_expert_ffn_residual for residual-split INT8 weights."""
+    if cfg.wtype == "int8_residual":
+        moe.moe_expert_ffn_residual(xg, r["offsets"], r["act"], r["na"], L["W_gate"], L["W_up"], L["W_down"],
+                                    L["s_gate"], L["s_up"], L["s_down"], L["Wr_gate"], L["Wr_up"], L["sr_gate"],
+                                    L["sr_up"], Y, ws, stream)
+    else:
+        moe.moe_expert_ffn(xg, r["offsets"], r["act"], r["na"], L["W_gate"], L["W_up"], L["W_down"], L["s_gate"],
+                           L["s_up"], L["s_down"], Y, ws, stream)
+
+
 # ------------------------------------------------------------------ workload
 class Workload:
     """Weights (several distinct layer copies, so consecutive steps do not re-read the previous
@@ -224,7 +245,7 @@ class Workload:
                     torch.empty(cfg.E, **i32), torch.empty(1, **i32)]
             moe.moe_route_topk(lg, k, *outs)
             self.active.append(int(outs[-1].item()))
-        self.wt = 1 if cfg.wtype == "int8" else 0
+        self.wt = 0 if cfg.wtype == "bf16" else 1  # the residual split uses the INT8 workspace
 
     def weight_bytes(self, c: int) -> int:
         return self.active[c] * self.cfg.weight_bytes_per_expert
@@ -263,10 +284,8 @@ def bench_ours(args, cfg, T):
     out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
 
     def step(c):
-        L = wl.layers[c]
         x, lg = wl.tokens[c]
-        moe.moe_ffn_forward(x, lg, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
-                            cfg.top_k, out, ws, stream)
+        ffn_forward(moe, cfg, wl.layers[c], x, lg, out, ws, stream)
 
     def barrier_sync():
         torch.cuda.synchronize()
@@ -314,8 +333,7 @@ def bench_ours(args, cfg, T):
         moe.moe_gather(x, cfg.top_k, r["st"], xg, stream)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        moe.moe_expert_ffn(xg, r["offsets"], r["act"], r["na"], L["W_gate"], L["W_up"], L["W_down"], L["s_gate"],
-                           L["s_up"], L["s_down"], Y, ws, stream)
+        expert_ffn(moe, cfg, L, xg, r, Y, ws, stream)
         b.record(stream)
         moe.moe_combine(Y, r["inv"], r["w"], cfg.top_k, out, stream)
         if i >= 3:
@@ -344,8 +362,7 @@ def bench_ours(args, cfg, T):
         L = wl.layers[c]
         x_d.copy_(x_h[c], non_blocking=True)
         lg_d.copy_(lg_h[c], non_blocking=True)
-        moe.moe_ffn_forward(x_d, lg_d, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
-                            cfg.top_k, out, ws, stream)
+        ffn_forward(moe, cfg, L, x_d, lg_d, out, ws, stream)
         out_h.copy_(out, non_blocking=True)
 
     for i in range(3):
@@ -371,7 +388,8 @@ def bench_ours(args, cfg, T):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if cfg.wtype == "bf16" else "int8 weights, bf16 activations",
+        "dtype": {"bf16": "bf16", "int8": "int8 weights, bf16 activations",
+                  "int8_residual": "int8 + int8 residual gate/up, int8 down, bf16 activations"}[cfg.wtype],
         "data": "synthetic (seeded N(0,1) tokens and logits, N(0,0.02) weights)",
         "pct_of_peak": round(100.0 * value / ws_n / peak, 2),
         "tokens_per_s": round(tokens_s, 1),
@@ -424,10 +442,8 @@ def sweep(cfg, dev, moe, copies, host=False):
         s = torch.cuda.current_stream()
 
         def step(c):
-            L = wl.layers[c]
             x, lg = wl.tokens[c]
-            moe.moe_ffn_forward(x, lg, L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"], L["s_down"],
-                                cfg.top_k, out, ws, s)
+            ffn_forward(moe, cfg, wl.layers[c], x, lg, out, ws, s)
         for i in range(10):
             step(i % copies)
         torch.cuda.synchronize()
@@ -461,8 +477,14 @@ def oracle_rate(cfg, T, budget_s, layer_cpu, x, lg):
     n = 0
     while True:
         t = n % T
-        oracle.forward(x[t:t + 1], lg[t:t + 1], layer_cpu["W_gate"], layer_cpu["W_up"], layer_cpu["W_down"],
-                       layer_cpu["s_gate"], layer_cpu["s_up"], layer_cpu["s_down"], wtype=cfg.wtype, top_k=cfg.top_k)
+        L = layer_cpu
+        if cfg.wtype == "int8_residual":
+            oracle.forward_residual(x[t:t + 1], lg[t:t + 1], L["W_gate"], L["s_gate"], L["Wr_gate"], L["sr_gate"],
+                                    L["W_up"], L["s_up"], L["Wr_up"], L["sr_up"], L["W_down"], L["s_down"],
+                                    top_k=cfg.top_k)
+        else:
+            oracle.forward(x[t:t + 1], lg[t:t + 1], L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"],
+                           L["s_down"], wtype=cfg.wtype, top_k=cfg.top_k)
         n += 1
         if time.perf_counter() - t0 > budget_s:
             break

@@ -195,6 +195,35 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
                              int H, int I, int E, int top_k, uint16_t* out, void* workspace,
                              size_t ws_bytes, moe_stream_t stream);
 
+/*
+ * Residual-split INT8 experts (RapidMoE, arXiv 2610.01265, "Residual-Split Representation" and
+ * "GLU Architecture Adoption"): gate and up are held as a low-precision part W^Q and the quantised
+ * residual W^R of W - W^Q, the high-precision weight being W^H = W^Q + W^R; the gate and up
+ * preactivations are W^Q x + W^R x, summed before SiLU. Down keeps one separately quantised copy
+ * (the pages' "dual quantization" of down_proj). Here every part is symmetric group-128 INT8:
+ *   W_gate, W_up    [E, I, H] int8: W^Q;  s_gate, s_up [E, I, H/128] f32 its scales
+ *   Wr_gate, Wr_up  [E, I, H] int8: W^R;  sr_gate, sr_up [E, I, H/128] f32 its scales
+ *   W_down          [E, H, I] int8;       s_down [E, H, I/128] f32
+ * i.e. w = q * s + qr * sr for gate and up. Everything else (sizes, workspace: the INT8 figure of
+ * moe_workspace_size, conventions, the host-memory option for weights) is as in
+ * moe_expert_ffn / moe_ffn_forward with MOE_W_INT8_G128; the gate and up weight stream doubles.
+ * All residual pointers must be non-null (16-byte aligned parts, 4-byte aligned scales).
+ */
+moe_status_t moe_expert_ffn_residual(const uint16_t* xg, const int32_t* expert_offsets,
+                                     const int32_t* active_experts, const int32_t* num_active,
+                                     const void* W_gate, const void* W_up, const void* W_down,
+                                     const float* s_gate, const float* s_up, const float* s_down,
+                                     const void* Wr_gate, const void* Wr_up, const float* sr_gate,
+                                     const float* sr_up, int H, int I, int E, int P, float* Y,
+                                     void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+moe_status_t moe_ffn_forward_residual(const uint16_t* x, const float* logits, const void* W_gate,
+                                      const void* W_up, const void* W_down, const float* s_gate,
+                                      const float* s_up, const float* s_down, const void* Wr_gate,
+                                      const void* Wr_up, const float* sr_gate, const float* sr_up,
+                                      int T, int H, int I, int E, int top_k, uint16_t* out,
+                                      void* workspace, size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,6 +26,7 @@ __all__ = [
     "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
     "moe_expert_ffn", "moe_combine", "moe_ffn_forward", "alloc_workspace", "workspace_status",
     "moe_expert_ffn_noalloc", "moe_gqa_workspace_size", "moe_gqa_decode", "alloc_gqa_workspace",
+    "moe_expert_ffn_residual", "moe_ffn_forward_residual",
 ]
 
 MOE_W_BF16 = 0
@@ -67,11 +68,13 @@ def load() -> ctypes.CDLL:
         lib.moe_expert_ffn.argtypes = [P, P, P, P, P, P, P, P, P, P, i, i, i, i, i, P, P, z, P]
         lib.moe_combine.argtypes = [P, P, P, i, i, i, P, P]
         lib.moe_ffn_forward.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, P, z, P]
+        lib.moe_expert_ffn_residual.argtypes = [P] * 14 + [i, i, i, i, P, P, z, P]
+        lib.moe_ffn_forward_residual.argtypes = [P] * 12 + [i, i, i, i, i, P, P, z, P]
         lib.moe_gqa_workspace_size.argtypes = [i, i, i, i, i]
         lib.moe_gqa_workspace_size.restype = z
         lib.moe_gqa_decode.argtypes = [P, P, P, P, i, i, i, i, i, ctypes.c_float, P, P, z, P]
         for f in ("moe_route_topk", "moe_gather", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
-                  "moe_gqa_decode"):
+                  "moe_gqa_decode", "moe_expert_ffn_residual", "moe_ffn_forward_residual"):
             getattr(lib, f).restype = i
         _lib = lib
         return lib
@@ -199,3 +202,26 @@ def moe_gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out, workspace, 
     _check("moe_gqa_decode", load().moe_gqa_decode(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, h_q, h_kv, d, L_cap, float(scale), _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_expert_ffn_residual(xg, expert_offsets, active_experts, num_active, W_gate, W_up, W_down, s_gate, s_up,
+                            s_down, Wr_gate, Wr_up, sr_gate, sr_up, Y, workspace, stream=None) -> None:
+    """moe_expert_ffn with residual-split INT8 gate/up (W^Q + W^R; see include/moe.h)."""
+    P, H = xg.shape
+    E, I, _ = W_gate.shape
+    _check("moe_expert_ffn_residual", load().moe_expert_ffn_residual(
+        _ptr(xg), _ptr(expert_offsets), _ptr(active_experts), _ptr(num_active), _ptr(W_gate), _ptr(W_up),
+        _ptr(W_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(Wr_gate), _ptr(Wr_up), _ptr(sr_gate),
+        _ptr(sr_up), H, I, E, P, _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_ffn_forward_residual(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, Wr_gate, Wr_up, sr_gate, sr_up,
+                             top_k, out, workspace, stream=None) -> None:
+    """moe_ffn_forward with residual-split INT8 gate/up (W^Q + W^R; see include/moe.h)."""
+    T, H = x.shape
+    E, I, _ = W_gate.shape
+    _check("moe_ffn_forward_residual", load().moe_ffn_forward_residual(
+        _ptr(x), _ptr(logits), _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down),
+        _ptr(Wr_gate), _ptr(Wr_up), _ptr(sr_gate), _ptr(sr_up), T, H, I, E, top_k, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))

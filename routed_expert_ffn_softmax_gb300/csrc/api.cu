@@ -110,10 +110,24 @@ int sm_count() {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Residual-split parts of gate and up (INT8 only); all null when the weights are not split.
+struct Residual {
+  const void* Wg = nullptr;
+  const void* Wu = nullptr;
+  const float* sg = nullptr;
+  const float* su = nullptr;
+};
+
+bool residual_ok(const Residual& r) {
+  return r.Wg && r.Wu && r.sg && r.su && aligned(r.Wg, 16) && aligned(r.Wu, 16) && aligned(r.sg, 4) &&
+         aligned(r.su, 4);
+}
+
 moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const int32_t* active,
                             const int32_t* num_active, const void* Wg, const void* Wu, const void* Wd,
                             const float* sg, const float* su, const float* sd, moe_wtype_t wtype, int H, int I,
-                            int E, int P, float* Y, char* ws, cudaStream_t stream, bool xg16_ready = false) {
+                            int E, int P, float* Y, char* ws, cudaStream_t stream, bool xg16_ready = false,
+                            const Residual& res = Residual{}) {
   const int sms = sm_count();
   if (sms < 1) return MOE_ERR_CUDA;
   const Layout L = layout(P, H, I, E, wtype == MOE_W_INT8_G128);
@@ -128,6 +142,10 @@ moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const in
   plan.s_gate = sg;
   plan.s_up = su;
   plan.s_down = sd;
+  plan.W_gate_r = res.Wg;
+  plan.W_up_r = res.Wu;
+  plan.s_gate_r = res.sg;
+  plan.s_up_r = res.su;
   plan.int8 = wtype == MOE_W_INT8_G128;
   plan.H = H;
   plan.I = I;
@@ -205,11 +223,15 @@ moe_status_t moe_gather(const uint16_t* x, int T, int H, int top_k, const int32_
       moe::launch_gather(x, T, H, top_k, sorted_token, xg, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets, const int32_t* active_experts,
-                            const int32_t* num_active, const void* W_gate, const void* W_up, const void* W_down,
-                            const float* s_gate, const float* s_up, const float* s_down, moe_wtype_t wtype, int H,
-                            int I, int E, int P, float* Y, void* workspace, size_t ws_bytes,
-                            moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status_t expert_ffn_impl(const uint16_t* xg, const int32_t* expert_offsets, const int32_t* active_experts,
+                             const int32_t* num_active, const void* W_gate, const void* W_up, const void* W_down,
+                             const float* s_gate, const float* s_up, const float* s_down, moe_wtype_t wtype, int H,
+                             int I, int E, int P, float* Y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+                             const Residual& res) {
   if (P < 0) return MOE_ERR_INVALID_ARG;
   const moe_status_t sz = check_sizes(P, H, I, E, 1, wtype);
   if (sz != MOE_OK) return sz;
@@ -226,7 +248,36 @@ moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets, c
   cudaError_t e = cudaMemsetAsync(ws + L.ctrl, 0, kCountersOffset + 4 * kMaxCtas, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return run_expert_ffn(xg, expert_offsets, active_experts, num_active, W_gate, W_up, W_down, s_gate, s_up, s_down,
-                        wtype, H, I, E, P, Y, ws, s);
+                        wtype, H, I, E, P, Y, ws, s, false, res);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets, const int32_t* active_experts,
+                            const int32_t* num_active, const void* W_gate, const void* W_up, const void* W_down,
+                            const float* s_gate, const float* s_up, const float* s_down, moe_wtype_t wtype, int H,
+                            int I, int E, int P, float* Y, void* workspace, size_t ws_bytes,
+                            moe_stream_t stream) {
+  return expert_ffn_impl(xg, expert_offsets, active_experts, num_active, W_gate, W_up, W_down, s_gate, s_up, s_down,
+                         wtype, H, I, E, P, Y, workspace, ws_bytes, stream, Residual{});
+}
+
+moe_status_t moe_expert_ffn_residual(const uint16_t* xg, const int32_t* expert_offsets,
+                                     const int32_t* active_experts, const int32_t* num_active, const void* W_gate,
+                                     const void* W_up, const void* W_down, const float* s_gate, const float* s_up,
+                                     const float* s_down, const void* Wr_gate, const void* Wr_up,
+                                     const float* sr_gate, const float* sr_up, int H, int I, int E, int P, float* Y,
+                                     void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  Residual r;
+  r.Wg = Wr_gate;
+  r.Wu = Wr_up;
+  r.sg = sr_gate;
+  r.su = sr_up;
+  if (P > 0 && !residual_ok(r)) return MOE_ERR_INVALID_ARG;
+  return expert_ffn_impl(xg, expert_offsets, active_experts, num_active, W_gate, W_up, W_down, s_gate, s_up, s_down,
+                         MOE_W_INT8_G128, H, I, E, P, Y, workspace, ws_bytes, stream, r);
 }
 
 moe_status_t moe_combine(const float* Y, const int32_t* inv_pos, const float* topk_w, int T, int top_k, int H,
@@ -243,10 +294,14 @@ moe_status_t moe_combine(const float* Y, const int32_t* inv_pos, const float* to
       moe::launch_combine(Y, inv_pos, topk_w, T, top_k, H, out, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void* W_gate, const void* W_up,
-                             const void* W_down, const float* s_gate, const float* s_up, const float* s_down,
-                             moe_wtype_t wtype, int T, int H, int I, int E, int top_k, uint16_t* out,
-                             void* workspace, size_t ws_bytes, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status_t ffn_forward_impl(const uint16_t* x, const float* logits, const void* W_gate, const void* W_up,
+                              const void* W_down, const float* s_gate, const float* s_up, const float* s_down,
+                              moe_wtype_t wtype, int T, int H, int I, int E, int top_k, uint16_t* out,
+                              void* workspace, size_t ws_bytes, moe_stream_t stream, const Residual& res) {
   const moe_status_t sz = check_sizes(T, H, I, E, top_k, wtype);
   if (sz != MOE_OK) return sz;
   if (T == 0) return MOE_OK;
@@ -283,9 +338,37 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
     e = moe::launch_gather(x, T, H, top_k, sorted_token, xg, sms, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const moe_status_t st = run_expert_ffn(xg, offsets, active, num_active, W_gate, W_up, W_down, s_gate, s_up,
-                                         s_down, wtype, H, I, E, P, Y, ws, s, int8);
+                                         s_down, wtype, H, I, E, P, Y, ws, s, int8, res);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_combine(Y, inv_pos, w, T, top_k, H, out, sms, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void* W_gate, const void* W_up,
+                             const void* W_down, const float* s_gate, const float* s_up, const float* s_down,
+                             moe_wtype_t wtype, int T, int H, int I, int E, int top_k, uint16_t* out,
+                             void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  return ffn_forward_impl(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, wtype, T, H, I, E, top_k, out,
+                          workspace, ws_bytes, stream, Residual{});
+}
+
+moe_status_t moe_ffn_forward_residual(const uint16_t* x, const float* logits, const void* W_gate, const void* W_up,
+                                      const void* W_down, const float* s_gate, const float* s_up,
+                                      const float* s_down, const void* Wr_gate, const void* Wr_up,
+                                      const float* sr_gate, const float* sr_up, int T, int H, int I, int E,
+                                      int top_k, uint16_t* out, void* workspace, size_t ws_bytes,
+                                      moe_stream_t stream) {
+  Residual r;
+  r.Wg = Wr_gate;
+  r.Wu = Wr_up;
+  r.sg = sr_gate;
+  r.su = sr_up;
+  if (T > 0 && !residual_ok(r)) return MOE_ERR_INVALID_ARG;
+  return ffn_forward_impl(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, MOE_W_INT8_G128, T, H, I, E, top_k,
+                          out, workspace, ws_bytes, stream, r);
 }
 
 // ---------------------------------------------------------------- decode GQA attention

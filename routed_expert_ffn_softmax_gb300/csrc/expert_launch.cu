@@ -262,6 +262,12 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
       !encode_weights(&td, p.W_down, true, p.I, p.H, p.E, 128) ||
       !encode_tokens(&txg, p.xg16, p.H, p.P, true, 8) || !encode_tokens(&th, p.h16, p.I, p.P, true, 8))
     return cudaErrorInvalidValue;
+  // residual split: gate and up run over W^Q then W^R (the maps are unused otherwise)
+  const bool residual = p.W_gate_r != nullptr;
+  CUtensorMap tgr = tg, tur = tu;
+  if (residual && (!encode_weights(&tgr, p.W_gate_r, true, p.H, p.I, p.E, 128) ||
+                   !encode_weights(&tur, p.W_up_r, true, p.H, p.I, p.E, 128)))
+    return cudaErrorInvalidValue;
   cudaError_t e = prepare_pair_kernel<true>();
   if (e == cudaSuccess) e = prepare_pair_kernel<false>();
   int pairs_gu = 0, pairs_dn = 0;
@@ -292,7 +298,13 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
   gu.s0 = p.s_gate;
   gu.s1 = p.s_up;
   gu.row_scale = p.xg_scale;
-  e = launch_pairs_pdl(pair::expert_pair_kernel<true>, pairs_gu, pair::Geo<true>::kSmem, s, tg, tu, txg, gu);
+  if (residual) {
+    gu.s0r = p.s_gate_r;
+    gu.s1r = p.s_up_r;
+    gu.kq = p.H / 128;
+  }
+  e = launch_pairs_pdl(pair::expert_pair_kernel<true>, pairs_gu, pair::Geo<true>::kSmem, s, tg, tu, txg, tgr, tur,
+                       gu);
   if (e != cudaSuccess) return e;
   e = launch_rows_to_f16(p.h, p.I, p.P, p.h16, p.h_scale, p.num_ctas, s);
   if (e != cudaSuccess) return e;
@@ -304,7 +316,8 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
   dn.s0 = p.s_down;
   dn.s1 = p.s_down;
   dn.row_scale = p.h_scale;
-  return launch_pairs_pdl(pair::expert_pair_kernel<false>, pairs_dn, pair::Geo<false>::kSmem, s, td, td, th, dn);
+  return launch_pairs_pdl(pair::expert_pair_kernel<false>, pairs_dn, pair::Geo<false>::kSmem, s, td, td, th, td, td,
+                          dn);
 }
 
 }  // namespace

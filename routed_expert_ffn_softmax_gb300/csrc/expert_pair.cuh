@@ -224,25 +224,24 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
   constexpr int kRing = kScaleLook + 1;
   int64_t lu = it_beg / KI;  // unit and stage of the next scale to fetch
   int lk = static_cast<int>(it_beg - lu * KI);
-  const float* l0 = nullptr;
-  const float* l1 = nullptr;
+  int64_t off = -1;  // the row's first scale in [E, rows, K/128] (the same in every scale array)
   int put = 0, get = 0;
   auto fetch_next = [&](int64_t stage_index) {
     if (stage_index < it_end) {
-      if (l0 == nullptr || lk == 0) {
+      if (off < 0 || lk == 0) {
         const Unit w = decode(lu);
         int row = w.rb * 256 + row_off;
         row = row < args.rows ? row : args.rows - 1;  // rows past the end are zero-filled by TMA
-        const int64_t off = (static_cast<int64_t>(w.e) * args.rows + row) * KG;
-        l0 = args.s0 + off;
-        l1 = args.s1 + off;
+        off = (static_cast<int64_t>(w.e) * args.rows + row) * KG;
       }
-      if constexpr (G::kGU) {  // gate and up scales of group lk
-        cp_async_4(ring + (put * 2) * kEpiThreads, l0 + lk);
-        cp_async_4(ring + (put * 2 + 1) * kEpiThreads, l1 + lk);
+      if constexpr (G::kGU) {  // gate and up scales of group lk (stages past KG: the residual parts')
+        const bool rr = lk >= KG;
+        const int g = rr ? lk - KG : lk;
+        cp_async_4(ring + (put * 2) * kEpiThreads, (rr ? args.s0r : args.s0) + off + g);
+        cp_async_4(ring + (put * 2 + 1) * kEpiThreads, (rr ? args.s1r : args.s1) + off + g);
       } else {  // down scales of groups 2 lk and 2 lk + 1 (none past the row's end)
-        cp_async_4(ring + (put * 2) * kEpiThreads, l0 + 2 * lk);
-        if (2 * lk + 1 < KG) cp_async_4(ring + (put * 2 + 1) * kEpiThreads, l0 + 2 * lk + 1);
+        cp_async_4(ring + (put * 2) * kEpiThreads, args.s0 + off + 2 * lk);
+        if (2 * lk + 1 < KG) cp_async_4(ring + (put * 2 + 1) * kEpiThreads, args.s0 + off + 2 * lk + 1);
         else ring[(put * 2 + 1) * kEpiThreads] = 0.0f;
       }
       if (++lk == KI) {
@@ -392,7 +391,8 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                       const __grid_constant__ CUtensorMap tmB, const Args args) {
+                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0r,
+                       const __grid_constant__ CUtensorMap tmA1r, const Args args) {
   using G = Geo<kGateUp>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStage);
@@ -428,10 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  const bool residual = kGateUp && args.kq > 0;
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA0);
     if (kGateUp) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
+    if (residual) {
+      tma_prefetch_desc(&tmA0r);
+      tma_prefetch_desc(&tmA1r);
+    }
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
 
@@ -486,7 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int RB = (args.rows + 255) / 256;
-  const int KI = (args.K + G::kKStage - 1) / G::kKStage;
+  // reduction stages of a unit: one weight part, or (residual split) W^Q then W^R
+  const int KQ = (args.K + G::kKStage - 1) / G::kKStage;
+  const int KI = residual ? 2 * KQ : KQ;
   const int64_t W = static_cast<int64_t>(t_pp[A]) * RB * KI;
   const int64_t pairs = gridDim.x / 2;
   const int64_t NC = W < pairs ? W : pairs;
@@ -524,8 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + stg * G::kStage;
         const int row0 = w.rb * 256 + 128 * static_cast<int>(rank);
         if (kGateUp) {
-          tma_load_3d(st, &tmA0, &full[stg], kk * 128, row0, w.e, policy);
-          tma_load_3d(st + 16384, &tmA1, &full[stg], kk * 128, row0, w.e, policy);
+          const bool r = kk >= KQ;  // residual part
+          const int x = (r ? kk - KQ : kk) * 128;
+          tma_load_3d(st, r ? &tmA0r : &tmA0, &full[stg], x, row0, w.e, policy);
+          tma_load_3d(st + 16384, r ? &tmA1r : &tmA1, &full[stg], x, row0, w.e, policy);
         } else {  // groups 2 kk and 2 kk + 1 (zero-filled past the row's end)
           tma_load_3d(st, &tmA0, &full[stg], kk * 256, row0, w.e, policy);
           tma_load_3d(st + 16384, &tmA0, &full[stg], kk * 256 + 128, row0, w.e, policy);
@@ -535,9 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sb = smem + stg * G::kStage + G::kWBytes;
         const int half_rows = ((w.ntok + 15) >> 4) * 8;  // this CTA's token rows: npad / 2
         const int t0 = w.tok0 + half_rows * static_cast<int>(rank);
+        const int kx = (kk < KQ ? kk : kk - KQ) * G::kKStage;  // both parts meet the same tokens
         for (int h = 0; h < G::kBHalves; ++h)
           for (int j = 0; j < half_rows; j += 8)
-            tma_load_2d(sb + h * G::kBHalf + j * 128, &tmB, &full[stg], kk * G::kKStage + 64 * h, t0 + j);
+            tma_load_2d(sb + h * G::kBHalf + j * 128, &tmB, &full[stg], kx + 64 * h, t0 + j);
       };
       int64_t u = it_beg / KI;
       int kk0 = static_cast<int>(it_beg - u * KI);

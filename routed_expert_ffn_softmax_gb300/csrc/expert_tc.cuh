@@ -69,6 +69,12 @@ struct Args {
   const float* s0;
   const float* s1;
   const float* row_scale;
+  // INT8 gate+up with residual-split weights (W^Q + W^R): the scales of the residual parts, and the
+  // reduction stages of one part (0 = no residual). Stages kq .. 2 kq - 1 read the residual parts
+  // against the same token columns as stages 0 .. kq - 1.
+  const float* s0r;
+  const float* s1r;
+  int kq;
 };
 
 struct Unit {

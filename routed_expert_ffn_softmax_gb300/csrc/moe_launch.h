@@ -58,6 +58,11 @@ struct ExpertFfnPlan {
   const float* s_gate;
   const float* s_up;
   const float* s_down;
+  // INT8 only, optional: residual-split parts of gate and up (W^Q + W^R) and their scales
+  const void* W_gate_r;
+  const void* W_up_r;
+  const float* s_gate_r;
+  const float* s_up_r;
   bool int8;
   int H, I, E, P;
   uint16_t* h;        // [P, I] scratch

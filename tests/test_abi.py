@@ -48,7 +48,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
         "moe_expert_ffn", "moe_expert_ffn_noalloc", "moe_combine", "moe_ffn_forward",
-        "moe_gqa_workspace_size", "moe_gqa_decode"])
+        "moe_gqa_workspace_size", "moe_gqa_decode", "moe_expert_ffn_residual", "moe_ffn_forward_residual"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -181,3 +181,21 @@ def test_gqa_tile_count_bound(lib):
     # 2048 sequences x 64 key/value heads x 2^17 tiles of 128 rows overflows the 32-bit tile count
     assert lib.moe_gqa_workspace_size(2048, 64, 64, 128, 1 << 24) == 0
     assert lib.moe_gqa_workspace_size(2048, 64, 64, 128, 1 << 20) > 0
+
+
+def test_residual_entry_points_reject_bad_arguments(lib):
+    F = FAKE
+    P_, i, z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.moe_ffn_forward_residual.argtypes = [P_] * 12 + [i, i, i, i, i, P_, P_, z, P_]
+    lib.moe_expert_ffn_residual.argtypes = [P_] * 14 + [i, i, i, i, P_, P_, z, P_]
+    ws = lib.moe_workspace_size(4, 256, 256, 8, 2, INT8)
+    f = lambda **kw: lib.moe_ffn_forward_residual(*[kw.get(n, F) for n in (
+        "x", "lg", "Wg", "Wu", "Wd", "sg", "su", "sd", "rg", "ru", "srg", "sru")], kw.get("T", 4), kw.get("H", 256),
+        256, 8, 2, F, F, kw.get("ws", ws), None)
+    assert f(rg=None) == INVALID
+    assert f(sru=None) == INVALID
+    assert f(ru=F + 8) == INVALID          # residual parts must be 16-byte aligned
+    assert f(H=264) == INVALID             # INT8 needs H % 128 == 0
+    assert f(ws=64) == WORKSPACE
+    assert f(T=0, rg=None) == OK           # T = 0 is a no-op
+    assert lib.moe_expert_ffn_residual(*([F] * 10), None, F, F, F, 256, 256, 8, 8, F, F, ws, None) == INVALID
