@@ -253,6 +253,15 @@ class Workload:
     def mean_weight_bytes(self) -> float:
         return sum(self.weight_bytes(c) for c in range(len(self.layers))) / len(self.layers)
 
+    def step_other_bytes(self) -> int:
+        """Bytes of a whole step besides the weights: x and logits read, routing tables, the
+        gathered block, h and Y written and read once, out written."""
+        cfg, T = self.cfg, self.T
+        P = T * cfg.top_k
+        routing = 4 * (3 * P + 2 * cfg.E + 2)  # ids, w, sorted_token / inv_pos, counts, offsets, active
+        return T * cfg.H * 2 + T * cfg.E * 4 + routing + 2 * P * cfg.H * 2 + 2 * P * cfg.I * 2 + 2 * P * cfg.H * 4 \
+            + T * cfg.H * 2
+
     def act_bytes(self) -> int:
         """Token-side algorithmic bytes of the expert kernels: xg read, h write + read, Y write."""
         cfg, P = self.cfg, self.T * self.cfg.top_k
@@ -385,6 +394,7 @@ def bench_ours(args, cfg, T):
         "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 5),
         "ms_per_step_median": round(statistics.median(per_step), 5),
+        "ms_per_step_geomean": round(statistics.geometric_mean(per_step), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -393,6 +403,8 @@ def bench_ours(args, cfg, T):
         "data": "synthetic (seeded N(0,1) tokens and logits, N(0,0.02) weights)",
         "pct_of_peak": round(100.0 * value / ws_n / peak, 2),
         "tokens_per_s": round(tokens_s, 1),
+        # the routed work only: 2 flops per weight per token routed to its expert
+        "tflops": round(2 * 3 * cfg.H * cfg.I * T * cfg.top_k / (total_ms / args.steps * 1e-3) / 1e12, 3),
         "config": {
             "workload": workload_name, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
             "weights": cfg.wtype, "T": T, "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
@@ -401,6 +413,8 @@ def bench_ours(args, cfg, T):
             "active_experts_mean": round(sum(wl.active) / len(wl.active), 2),
             "tokens_per_expert_mean": round(T * cfg.top_k * len(wl.active) / sum(wl.active), 2),
             "weight_bytes_per_step_mean": int(wl.mean_weight_bytes()),
+            # every array of the step (weights, x, logits, routing tables, xg, h, Y, out), each once
+            "algorithmic_bytes_per_step_mean": int(wl.mean_weight_bytes() + wl.step_other_bytes()),
             "l2": f"inputs larger than L2: each step streams >= "
                   f"{min(wl.weight_bytes(c) for c in range(copies)) / 1e6:.0f} MB of expert weights, "
                   f"rotating over {copies} distinct weight copies",
@@ -661,6 +675,7 @@ def bench_attention_ours(args, acfg):
         "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 5),
         "ms_per_step_median": round(statistics.median(per_step), 5),
+        "ms_per_step_geomean": round(statistics.geometric_mean(per_step), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
