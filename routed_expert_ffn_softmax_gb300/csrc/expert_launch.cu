@@ -182,7 +182,7 @@ cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
 }
 
 // ---- INT8 on CTA pairs
-template <bool kGateUp>
+template <bool kGateUp, int kN>
 cudaError_t prepare_pair_kernel() {
   constexpr int kMaxDev = 64;
   static std::atomic<bool> done[kMaxDev];
@@ -190,15 +190,15 @@ cudaError_t prepare_pair_kernel() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(pair::expert_pair_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           pair::Geo<kGateUp>::kSmem);
+  e = cudaFuncSetAttribute(pair::expert_pair_kernel<kGateUp, kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           pair::Geo<kGateUp, kN>::kSmem);
   if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
 // Pairs of the pair kernel that can be resident at once on this device (a persistent stream-K
 // grid must not be larger, or the late pairs would run after the others instead of beside them).
-template <bool kGateUp>
+template <bool kGateUp, int kN>
 cudaError_t resident_pairs(int* pairs) {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev];
@@ -220,11 +220,11 @@ cudaError_t resident_pairs(int* pairs) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kPartialCtas);
   cfg.blockDim = dim3(pair::kThreads);
-  cfg.dynamicSmemBytes = pair::Geo<kGateUp>::kSmem;
+  cfg.dynamicSmemBytes = pair::Geo<kGateUp, kN>::kSmem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, pair::expert_pair_kernel<kGateUp>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, pair::expert_pair_kernel<kGateUp, kN>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorNotSupported;
   if (dev < kMaxDev) cache[dev].store(n, std::memory_order_release);
@@ -254,7 +254,8 @@ cudaError_t launch_pairs_pdl(void (*kernel)(KArgs...), int pairs, size_t smem, c
 
 // INT8: fp16 token copy, gate+up on pairs, fp16 copy of h, down on pairs. Weight boxes are one
 // CTA's 128 rows by 128 bytes; token boxes are 8 rows (a CTA holds half of a pass's tokens).
-cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
+template <int kN>
+cudaError_t launch_pair_int8_n(const ExpertFfnPlan& p, cudaStream_t s) {
   CUtensorMap tg, tu, td, txg, th;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
   if (!encode_weights(&tg, p.W_gate, true, p.H, p.I, p.E, 128) ||
@@ -268,11 +269,11 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
   if (residual && (!encode_weights(&tgr, p.W_gate_r, true, p.H, p.I, p.E, 128) ||
                    !encode_weights(&tur, p.W_up_r, true, p.H, p.I, p.E, 128)))
     return cudaErrorInvalidValue;
-  cudaError_t e = prepare_pair_kernel<true>();
-  if (e == cudaSuccess) e = prepare_pair_kernel<false>();
+  cudaError_t e = prepare_pair_kernel<true, kN>();
+  if (e == cudaSuccess) e = prepare_pair_kernel<false, kN>();
   int pairs_gu = 0, pairs_dn = 0;
-  if (e == cudaSuccess) e = resident_pairs<true>(&pairs_gu);
-  if (e == cudaSuccess) e = resident_pairs<false>(&pairs_dn);
+  if (e == cudaSuccess) e = resident_pairs<true, kN>(&pairs_gu);
+  if (e == cudaSuccess) e = resident_pairs<false, kN>(&pairs_dn);
   if (e != cudaSuccess) return e;
   const int max_pairs = p.num_ctas / 2 > 0 ? p.num_ctas / 2 : 1;
   pairs_gu = pairs_gu < max_pairs ? pairs_gu : max_pairs;
@@ -303,8 +304,8 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
     gu.s1r = p.s_up_r;
     gu.kq = p.H / 128;
   }
-  e = launch_pairs_pdl(pair::expert_pair_kernel<true>, pairs_gu, pair::Geo<true>::kSmem, s, tg, tu, txg, tgr, tur,
-                       gu);
+  e = launch_pairs_pdl(pair::expert_pair_kernel<true, kN>, pairs_gu, pair::Geo<true, kN>::kSmem, s, tg, tu, txg, tgr,
+                       tur, gu);
   if (e != cudaSuccess) return e;
   e = launch_rows_to_f16(p.h, p.I, p.P, p.h16, p.h_scale, p.num_ctas, s);
   if (e != cudaSuccess) return e;
@@ -316,8 +317,16 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
   dn.s0 = p.s_down;
   dn.s1 = p.s_down;
   dn.row_scale = p.h_scale;
-  return launch_pairs_pdl(pair::expert_pair_kernel<false>, pairs_dn, pair::Geo<false>::kSmem, s, td, td, th, td, td,
-                          dn);
+  return launch_pairs_pdl(pair::expert_pair_kernel<false, kN>, pairs_dn, pair::Geo<false, kN>::kSmem, s, td, td, th,
+                          td, td, dn);
+}
+
+// Passes of 16 tokens (three accumulator buffers) while the experts see at most about eight tokens
+// each on average, passes of 32 above: measured on GB300 (Qwen3-235B shapes), the shorter passes
+// are 3-9% faster at 1-4 tokens per expert and 14% slower at 16.
+cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
+  if (static_cast<int64_t>(p.P) <= 8LL * p.E) return launch_pair_int8_n<16>(p, s);
+  return launch_pair_int8_n<32>(p, s);
 }
 
 }  // namespace

@@ -45,12 +45,17 @@ constexpr int kConvWarp0 = 6;      // warps 6..13
 constexpr int kConvWarps = 8;
 constexpr int kIssuer1Warp = 14;
 constexpr int kThreads = 32 * (kIssuer1Warp + 1);
-constexpr int kNMax = 32;          // tokens per pass; each CTA holds kNMax / 2 of them
 constexpr int kScaleLook = 4;      // group scales are fetched this many stages ahead
 
-template <bool kGateUp>
+// kN: tokens per pass (each CTA holds kN / 2 of them), 16 or 32. Passes of 16 halve the
+// accumulator buffers, which leaves TMEM room for a third one: a stage's MMAs then wait for the
+// promotion of the stage three back instead of two, which shortens the stage period when experts
+// see a few tokens each; experts with more tokens than a pass take several passes.
+template <bool kGateUp, int kN>
 struct Geo {
   static constexpr bool kGU = kGateUp;
+  static constexpr int kNMax = kN;
+  static constexpr int kDBufs = kN <= 16 ? 3 : 2;           // accumulator buffers
   static constexpr int kKStage = kGateUp ? 128 : 256;       // reduction elements per stage
   static constexpr int kWBytes = 32768;                     // this CTA's two weight tiles per stage
   static constexpr int kBRows = kNMax / 2;                  // token rows per CTA
@@ -60,17 +65,23 @@ struct Geo {
   static constexpr int kStage = kWBytes + kBBytes;
   static constexpr int kStages = 5;
   static constexpr int kAccCols = 2 * kNMax;                // the two issuers' accumulators
-  static constexpr int kABase = 2 * kAccCols;               // operand buffers after two accumulators
+  static constexpr int kABase = kDBufs * kAccCols;          // operand buffers after the accumulators
   static constexpr int kACols = 128;                        // two tiles x 128 elements (fp16 pairs)
   static constexpr int kAFit = (512 - kABase) / kACols;
   static constexpr int kABufs = kAFit < kStages ? kAFit : kStages;
-  static constexpr int kBarBytes = (2 * kStages + 4 + 2 * kABufs) * 8;
+  static constexpr int kBarBytes = (2 * kStages + kDBufs + 2 + 2 * kABufs) * 8;
   static constexpr int kTableBytes = (4 * kTable + 32) * 4;
   static constexpr int kScaleOff = kStages * kStage + kBarBytes + kTableBytes;
   static constexpr int kScaleBytes = (kScaleLook + 1) * 2 * kEpiThreads * 4;
   static constexpr int kSmem = kScaleOff + kScaleBytes;
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
   static_assert(kABufs >= 2 && kABase + kABufs * kACols <= 512, "TMEM operand buffers");
+  // The operand-free barrier of a buffer also tells the promotion warps that a stage's group sums
+  // are done, and they wait on it by phase parity. The converters may run kDBufs stages ahead of
+  // the promotion, so the next phase of that barrier (the MMAs kABufs stages later) must not be
+  // able to complete first: with kDBufs > kABufs the parity aliases and the promotion waits for a
+  // phase it already missed.
+  static_assert(kDBufs <= kABufs, "promotion may lag at most the operand buffers");
   static_assert(128 * kAccCols <= kPartialFloats, "partial slot size");
   static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
@@ -121,7 +132,7 @@ __device__ __forceinline__ void convert(const uint8_t* smem, uint64_t* full, uin
     if (lane == 0) mbar_arrive(&empty[stage]);  // this stage's weight bytes are consumed
     tmem_wait_st();
     tc_fence_before_sync();
-    // even CTA: the stage's accumulator buffer (last used two stages ago) must be free in both
+    // even CTA: the stage's accumulator buffer (last used kDBufs stages ago) must be free in both
     // CTAs before the issuers may start on it
     if (rank == 0 && lane == 0 && ok && !mbar_wait(&d_empty[db], dph ^ 1))
       atomicExch(args.status, kStatusWaitEmptyTimeout), ok = false;
@@ -135,7 +146,7 @@ __device__ __forceinline__ void convert(const uint8_t* smem, uint64_t* full, uin
       ab = 0;
       aph ^= 1;
     }
-    if (++db == 2) {
+    if (++db == G::kDBufs) {
       db = 0;
       dph ^= 1;
     }
@@ -175,7 +186,7 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
       tc_fence_after_sync();
       const uint32_t idesc = umma_idesc_f16_m256(((un.ntok + 15) >> 4) * 16);
       const uint32_t a = tmem_base + a_off + ab * G::kACols;
-      const uint32_t d = tmem_base + db * G::kAccCols + kNMax * which;
+      const uint32_t d = tmem_base + db * G::kAccCols + G::kNMax * which;
       // descriptor of the stage's token tile; each step adds its byte offset / 16
       const uint64_t bdesc = umma_desc_sw128(smem_base + stage * G::kStage + G::kWBytes);
 #pragma unroll
@@ -191,7 +202,7 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
       ab = 0;
       aph ^= 1;
     }
-    if (++db == 2) db = 0;
+    if (++db == G::kDBufs) db = 0;
     if (++kk == KI) kk = 0;
   }
   // every issued MMA has finished before the pair's TMEM is released
@@ -208,7 +219,7 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
                                         const Args& args, int64_t it_beg, int64_t it_end, int KI, int64_t W,
                                         int64_t NC, int64_t pair_id, uint32_t rank, int* s_misc,
                                         const Decode& decode) {
-  constexpr int N = kNMax;
+  constexpr int N = G::kNMax;
   pdl_wait_predecessor();
   pdl_allow_successor();
   const int warp = threadIdx.x >> 5;
@@ -327,7 +338,7 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive_cta(&d_empty[db], 0);
-    if (++db == 2) db = 0;
+    if (++db == G::kDBufs) db = 0;
     if (++ab == G::kABufs) {
       ab = 0;
       aph ^= 1;
@@ -388,17 +399,17 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
   }
 }
 
-template <bool kGateUp>
+template <bool kGateUp, int kN>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0r,
                        const __grid_constant__ CUtensorMap tmA1r, const Args args) {
-  using G = Geo<kGateUp>;
+  using G = Geo<kGateUp, kN>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStage);
   uint64_t* empty = full + G::kStages;
-  uint64_t* d_empty = empty + G::kStages; // [2] even CTA: group sums read by both CTAs
-  uint64_t* mma_done = d_empty + 2;       // [2] one per issuer
+  uint64_t* d_empty = empty + G::kStages; // [kDBufs] even CTA: group sums read by both CTAs
+  uint64_t* mma_done = d_empty + G::kDBufs;  // [2] one per issuer
   uint64_t* a_full = mma_done + 2;        // [kABufs] even CTA: both CTAs' operands written
   uint64_t* a_empty = a_full + G::kABufs; // [kABufs] operand buffer read (issuer commits)
   int* t_e = reinterpret_cast<int*>(a_empty + G::kABufs);
@@ -418,10 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);              // producer expect_tx
       mbar_init(&empty[s], kConvWarps + 2);  // this CTA's converters + the two issuers' commits
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&d_empty[b], 2 * 4);       // promotion warps of both CTAs
-      mbar_init(&mma_done[b], 1);
-    }
+    for (int b = 0; b < G::kDBufs; ++b) mbar_init(&d_empty[b], 2 * 4);  // promotion warps of both CTAs
+    for (int b = 0; b < 2; ++b) mbar_init(&mma_done[b], 1);
     for (int b = 0; b < G::kABufs; ++b) {
       mbar_init(&a_full[b], 2 * kConvWarps);  // converter warps of both CTAs
       mbar_init(&a_empty[b], 2);              // the two issuers' commits
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       t_e[a] = e;
       t_tok0[a] = tok0;
       t_ntok[a] = ntok;
-      passes = (ntok + kNMax - 1) / kNMax;
+      passes = (ntok + G::kNMax - 1) / G::kNMax;
     }
     t_pp[a + 1] = passes;
   }
@@ -512,9 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int np = q - t_pp[lo];
     r.e = t_e[lo];
-    r.tok0 = t_tok0[lo] + np * kNMax;
-    const int left = t_ntok[lo] - np * kNMax;
-    r.ntok = left < kNMax ? left : kNMax;
+    r.tok0 = t_tok0[lo] + np * G::kNMax;
+    const int left = t_ntok[lo] - np * G::kNMax;
+    r.ntok = left < G::kNMax ? left : G::kNMax;
     return r;
   };
 
