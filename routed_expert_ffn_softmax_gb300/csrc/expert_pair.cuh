@@ -12,8 +12,12 @@
 //
 // Work: a cluster of two CTAs (rank 0 = even, rank 1 = odd) takes a stream-K range of
 // (expert pass, 256-row block) x stages; CTA `rank` holds rows 128 * rank .. 128 * rank + 127 of
-// the block and token rows npad / 2 * rank .. of the pass (the pair MMA reads B half from each
-// CTA's shared memory and writes each CTA's 128 rows of D into its own TMEM). A stage holds two
+// the block and token rows kN / 2 * rank .. of the pass (the pair MMA reads B half from each
+// CTA's shared memory and writes each CTA's 128 rows of D into its own TMEM). Every stage has the
+// same shape: the MMAs always take N = kN token columns and every CTA always loads its kN / 2 token
+// rows, whatever the pass holds. Columns past the pass's tokens meet the rows that follow them (the
+// next expert's tokens, or TMA's zero fill past the block) and are never read. Measured on GB300,
+// stages whose shape followed the pass's token count were slower: 13% at 16 tokens per expert. A stage holds two
 // 16 KB weight tiles per CTA: gate and up of one scale group (gate+up), or two consecutive scale
 // groups of the down rows (down), so both kernels move the same bytes per hand-off.
 // Per CTA (15 warps):
@@ -26,7 +30,7 @@
 // two commits per stage): converters of both CTAs arrive on the even CTA's operand-ready barrier,
 // the even CTA's converters first waiting until both CTAs' promotion warps have freed the stage's
 // accumulator buffer; the issuers' commits arrive on the same barrier in both CTAs (multicast),
-// and the operand-free commit also tells the promotion warps that the stage's group sums are done.
+// and the stage-free commit also tells the promotion warps that the stage's group sums are done.
 #pragma once
 
 #include "expert_tc.cuh"
@@ -76,12 +80,13 @@ struct Geo {
   static constexpr int kSmem = kScaleOff + kScaleBytes;
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
   static_assert(kABufs >= 2 && kABase + kABufs * kACols <= 512, "TMEM operand buffers");
-  // The operand-free barrier of a buffer also tells the promotion warps that a stage's group sums
-  // are done, and they wait on it by phase parity. The converters may run kDBufs stages ahead of
-  // the promotion, so the next phase of that barrier (the MMAs kABufs stages later) must not be
-  // able to complete first: with kDBufs > kABufs the parity aliases and the promotion waits for a
-  // phase it already missed.
-  static_assert(kDBufs <= kABufs, "promotion may lag at most the operand buffers");
+  // The stage-free barrier (shared-memory stage consumed: converters done and the stage's MMAs
+  // complete) also tells the promotion warps that the stage's group sums are done; they wait on it
+  // by phase parity. The converters may run kDBufs stages ahead of the promotion, so the next
+  // phase of that barrier (the MMAs kStages stages later) must not be able to complete first:
+  // with kDBufs > kStages the parity would alias and the promotion would wait for a phase it
+  // already missed.
+  static_assert(kDBufs <= kStages, "promotion may lag at most the shared-memory stages");
   static_assert(128 * kAccCols <= kPartialFloats, "partial slot size");
   static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
@@ -154,10 +159,10 @@ __device__ __forceinline__ void convert(const uint8_t* smem, uint64_t* full, uin
 }
 
 // Issuers (lane 0 of warps 1 and 14 of the even CTA): pair MMAs over both CTAs' rows.
-template <typename G, typename Decode>
+template <typename G>
 __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint64_t* a_full, uint64_t* a_empty,
                                       uint64_t* done_bar, uint32_t tmem_base, const Args& args, int64_t it_beg,
-                                      int64_t it_end, int KI, const Decode& decode) {
+                                      int64_t it_end) {
   pdl_wait_predecessor();
   pdl_allow_successor();
   if ((threadIdx.x & 31) != 0) return;
@@ -166,25 +171,20 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
   bool ok = true;
   int stage = 0, ab = 0, db = 0;
   uint32_t aph = 0;
-  int64_t u = it_beg / KI;
-  int kk = static_cast<int>(it_beg - u * KI);
-  Unit un{};
-  if (it_beg < it_end) un = decode(u);
   // issuer `which` multiplies tile `which` (gate / up, or the first / second scale group) by the
   // token tile: 8 steps of 16 elements; gate and up share the stage's 128 token columns, the two
   // down groups take columns 0..127 and 128..255
   constexpr int kSteps = 8;
   const int s0 = G::kGU ? 0 : 8 * which;
   const uint32_t a_off = G::kABase + 64 * which;
+  const uint32_t idesc = umma_idesc_f16_m256(G::kNMax);
 #pragma unroll 1
   for (int64_t it = it_beg; it < it_end; ++it) {
-    if (kk == 0 && it != it_beg) un = decode(++u);
     // the converters of both CTAs arrive on a_full after they saw their stage land (so this also
     // covers both halves of the token tile), the even CTA's after the accumulator buffer was freed
     if (ok && !mbar_wait(&a_full[ab], aph)) atomicExch(args.status, kStatusWaitFullTimeout), ok = false;
     if (ok) {
       tc_fence_after_sync();
-      const uint32_t idesc = umma_idesc_f16_m256(((un.ntok + 15) >> 4) * 16);
       const uint32_t a = tmem_base + a_off + ab * G::kACols;
       const uint32_t d = tmem_base + db * G::kAccCols + G::kNMax * which;
       // descriptor of the stage's token tile; each step adds its byte offset / 16
@@ -195,15 +195,15 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
         umma_f16_pair_tmem_a(d, a + 8 * q, bdesc + (((s >> 2) * G::kBHalf + 32 * (s & 3)) >> 4), idesc, q != 0);
       }
     }
-    umma_commit_pair(&empty[stage]);  // both CTAs' stages are free once these MMAs have read them
-    umma_commit_pair(&a_empty[ab]);   // and both operand buffers, and the group sums are complete
+    umma_commit_pair(&empty[stage]);  // both CTAs' stages are free once these MMAs have read them,
+                                      // and the group sums are complete
+    umma_commit_pair(&a_empty[ab]);   // and both operand buffers
     if (++stage == G::kStages) stage = 0;
     if (++ab == G::kABufs) {
       ab = 0;
       aph ^= 1;
     }
     if (++db == G::kDBufs) db = 0;
-    if (++kk == KI) kk = 0;
   }
   // every issued MMA has finished before the pair's TMEM is released
   umma_commit_pair(&done_bar[which]);
@@ -215,7 +215,7 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
 // end of each unit write h = SiLU(g) * u or Y, or publish the partial of a unit another pair
 // finishes (the last arriver reduces, in pair order).
 template <typename G, typename Decode>
-__device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64_t* d_empty, uint32_t tmem_base,
+__device__ __forceinline__ void promote(uint8_t* smem, uint64_t* empty, uint64_t* d_empty, uint32_t tmem_base,
                                         const Args& args, int64_t it_beg, int64_t it_end, int KI, int64_t W,
                                         int64_t NC, int64_t pair_id, uint32_t rank, int* s_misc,
                                         const Decode& decode) {
@@ -272,8 +272,8 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
   };
   zero();
   bool ok = true;
-  int db = 0, ab = 0;
-  uint32_t aph = 0;
+  int db = 0, stage = 0;
+  uint32_t sph = 0;
   const int64_t first_unit = it_beg / KI;
   int64_t u = first_unit;
   int kk = static_cast<int>(it_beg - u * KI);
@@ -312,8 +312,8 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
     const float s0 = ring[(get * 2) * kEpiThreads];
     const float s1 = ring[(get * 2 + 1) * kEpiThreads];
     if (++get == kRing) get = 0;
-    // the issuers' operand-free commit for this stage: its MMAs, and so its group sums, are done
-    if (ok && !mbar_wait(&a_empty[ab], aph)) atomicExch(args.status, kStatusWaitFullTimeout), ok = false;
+    // the issuers' stage-free commit for this stage: its MMAs, and so its group sums, are done
+    if (ok && !mbar_wait(&empty[stage], sph)) atomicExch(args.status, kStatusWaitFullTimeout), ok = false;
     ok = __all_sync(0xffffffffu, ok);  // keep the warp-wide TMEM loads uniform
     tc_fence_after_sync();
     const int npad = ((un.ntok + 15) >> 4) * 16;
@@ -339,9 +339,9 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* a_empty, uint64
     __syncwarp();
     if (lane == 0) mbar_arrive_cta(&d_empty[db], 0);
     if (++db == G::kDBufs) db = 0;
-    if (++ab == G::kABufs) {
-      ab = 0;
-      aph ^= 1;
+    if (++stage == G::kStages) {
+      stage = 0;
+      sph ^= 1;
     }
     const bool piece_end = (kk == KI - 1) || (it == it_end - 1);
     if (++kk == KI) kk = 0;
@@ -535,7 +535,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      auto bbytes = [](const Unit& w) { return G::kBHalves * (((w.ntok + 15) >> 4) * 8) * 128; };
       auto issue_a = [&](int stg, const Unit& w, int kk) {
         uint8_t* st = smem + stg * G::kStage;
         const int row0 = w.rb * 256 + 128 * static_cast<int>(rank);
@@ -551,11 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_b = [&](int stg, const Unit& w, int kk) {
         uint8_t* sb = smem + stg * G::kStage + G::kWBytes;
-        const int half_rows = ((w.ntok + 15) >> 4) * 8;  // this CTA's token rows: npad / 2
-        const int t0 = w.tok0 + half_rows * static_cast<int>(rank);
+        const int t0 = w.tok0 + G::kBRows * static_cast<int>(rank);  // this CTA's kN / 2 token rows
         const int kx = (kk < KQ ? kk : kk - KQ) * G::kKStage;  // both parts meet the same tokens
+#pragma unroll
         for (int h = 0; h < G::kBHalves; ++h)
-          for (int j = 0; j < half_rows; j += 8)
+#pragma unroll
+          for (int j = 0; j < G::kBRows; j += 8)
             tma_load_2d(sb + h * G::kBHalf + j * 128, &tmB, &full[stg], kx + 64 * h, t0 + j);
       };
       int64_t u = it_beg / KI;
@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pk = kk0;
         Unit pun = un;
         for (int64_t q = 0; q < npre; ++q) {
-          mbar_arrive_expect_tx(&full[q], G::kWBytes + bbytes(pun));
+          mbar_arrive_expect_tx(&full[q], G::kWBytes + G::kBBytes);
           issue_a(static_cast<int>(q), pun, pk);
           if (++pk == KI && q + 1 < npre) {
             pk = 0;
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[stage], G::kWBytes + bbytes(un));
+        mbar_arrive_expect_tx(&full[stage], G::kWBytes + G::kBBytes);
         issue_a(stage, un, kk0);
         issue_b(stage, un, kk0);
         ++issued;
@@ -632,13 +632,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp == kIssuer1Warp) {
     // =========================== MMA issuers (even CTA) ===========================
     if (rank == 0) {
-      issue<G>(smem, empty, a_full, a_empty, mma_done, tmem_base, args, it_beg, it_end, KI, decode);
+      issue<G>(smem, empty, a_full, a_empty, mma_done, tmem_base, args, it_beg, it_end);
     } else {
       pdl_wait_predecessor();
       pdl_allow_successor();
     }
   } else if (warp < kConvWarp0) {
-    promote<G>(smem, a_empty, d_empty, tmem_base, args, it_beg, it_end, KI, W, NC, pair_id, rank, s_misc, decode);
+    promote<G>(smem, empty, d_empty, tmem_base, args, it_beg, it_end, KI, W, NC, pair_id, rank, s_misc, decode);
   } else {
     convert<G>(smem, full, empty, a_full, a_empty, d_empty, tmem_base, rank, args, it_beg, it_end);
   }

@@ -384,7 +384,6 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
     int64_t piece = 0;
     const int64_t first_unit = it_beg / KI;
     int64_t u = first_unit;
-    int kk = static_cast<int>(it_beg - u * KI);
     for (int64_t it = it_beg; it < it_end;) {
       // one piece: stages [it, pe) of unit u
       const int64_t ub = u * KI;
