@@ -55,6 +55,52 @@ constexpr int kScaleLook = 4;      // group scales are fetched this many stages 
 // accumulator buffers, which leaves TMEM room for a third one: a stage's MMAs then wait for the
 // promotion of the stage three back instead of two, which shortens the stage period when experts
 // see a few tokens each; experts with more tokens than a pass take several passes.
+// The unit list: pass np of the a-th active expert (passes t_pp[a] .. t_pp[a + 1] - 1 of the
+// flattened list q) and 256-row block rb form unit q * RB + rb. A role finds its first unit with
+// one division and a binary search, then steps through the list without either: a lookup per
+// unit cost the single issuing thread several percent when it sat on its path.
+struct Units {
+  const int* e;
+  const int* tok0;
+  const int* ntok;
+  const int* pp;  // prefix sums of the passes per active expert, A + 1 entries
+  int A, RB, kN;
+  struct Cursor {
+    int a, np, rb;
+  };
+  __device__ __forceinline__ Cursor seek(int64_t u) const {
+    const int q = static_cast<int>(u / RB);
+    Cursor c;
+    c.rb = static_cast<int>(u - static_cast<int64_t>(q) * RB);
+    int lo = 0, hi = A - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pp[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    c.a = lo;
+    c.np = q - pp[lo];
+    return c;
+  }
+  __device__ __forceinline__ void next(Cursor& c) const {
+    if (++c.rb < RB) return;
+    c.rb = 0;
+    ++c.np;
+    while (c.a + 1 < A && c.np >= pp[c.a + 1] - pp[c.a]) {  // also skips experts without passes
+      c.np = 0;
+      ++c.a;
+    }
+  }
+  __device__ __forceinline__ Unit unit(const Cursor& c) const {
+    Unit r;
+    r.rb = c.rb;
+    r.e = e[c.a];
+    r.tok0 = tok0[c.a] + c.np * kN;
+    const int left = ntok[c.a] - c.np * kN;
+    r.ntok = left < kN ? left : kN;
+    return r;
+  }
+};
+
 template <bool kGateUp, int kN>
 struct Geo {
   static constexpr bool kGU = kGateUp;
@@ -214,11 +260,11 @@ __device__ __forceinline__ void issue(const uint8_t* smem, uint64_t* empty, uint
 // read the group sums, multiply by the row's group scale(s), accumulate in fp32 registers; at the
 // end of each unit write h = SiLU(g) * u or Y, or publish the partial of a unit another pair
 // finishes (the last arriver reduces, in pair order).
-template <typename G, typename Decode>
+template <typename G>
 __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* empty, uint64_t* d_empty, uint32_t tmem_base,
                                         const Args& args, int64_t it_beg, int64_t it_end, int KI, int64_t W,
                                         int64_t NC, int64_t pair_id, uint32_t rank, int* s_misc,
-                                        const Decode& decode) {
+                                        const Units& units) {
   constexpr int N = G::kNMax;
   pdl_wait_predecessor();
   pdl_allow_successor();
@@ -233,14 +279,14 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* empty, uint64_t
 
   float* ring = reinterpret_cast<float*>(smem + G::kScaleOff) + etid;
   constexpr int kRing = kScaleLook + 1;
-  int64_t lu = it_beg / KI;  // unit and stage of the next scale to fetch
-  int lk = static_cast<int>(it_beg - lu * KI);
+  Units::Cursor lc = units.seek(it_beg / KI);  // unit and stage of the next scale to fetch
+  int lk = static_cast<int>(it_beg % KI);
   int64_t off = -1;  // the row's first scale in [E, rows, K/128] (the same in every scale array)
   int put = 0, get = 0;
   auto fetch_next = [&](int64_t stage_index) {
     if (stage_index < it_end) {
       if (off < 0 || lk == 0) {
-        const Unit w = decode(lu);
+        const Unit w = units.unit(lc);
         int row = w.rb * 256 + row_off;
         row = row < args.rows ? row : args.rows - 1;  // rows past the end are zero-filled by TMA
         off = (static_cast<int64_t>(w.e) * args.rows + row) * KG;
@@ -257,7 +303,7 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* empty, uint64_t
       }
       if (++lk == KI) {
         lk = 0;
-        ++lu;
+        units.next(lc);
       }
     }
     cp_async_commit();  // one group per stage, empty past the end
@@ -277,8 +323,9 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* empty, uint64_t
   const int64_t first_unit = it_beg / KI;
   int64_t u = first_unit;
   int kk = static_cast<int>(it_beg - u * KI);
+  Units::Cursor uc = units.seek(first_unit);
   Unit un{};
-  if (it_beg < it_end) un = decode(u);
+  if (it_beg < it_end) un = units.unit(uc);
 
   auto emit = [&]() {
     const int row = un.rb * 256 + row_off;
@@ -304,7 +351,8 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* empty, uint64_t
   for (int64_t it = it_beg; it < it_end; ++it) {
     if (kk == 0 && it != it_beg) {
       ++u;
-      un = decode(u);
+      units.next(uc);
+      un = units.unit(uc);
       zero();
     }
     fetch_next(it + kScaleLook);
@@ -510,22 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t it_beg = pair_id < NC ? pair_id * W / NC : 0;
   const int64_t it_end = pair_id < NC ? (pair_id + 1) * W / NC : 0;
 
-  auto decode = [&](int64_t u) -> Unit {
-    const int q = static_cast<int>(u / RB);
-    Unit r;
-    r.rb = static_cast<int>(u % RB);
-    int lo = 0, hi = A - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (t_pp[mid] <= q) lo = mid; else hi = mid - 1;
-    }
-    const int np = q - t_pp[lo];
-    r.e = t_e[lo];
-    r.tok0 = t_tok0[lo] + np * G::kNMax;
-    const int left = t_ntok[lo] - np * G::kNMax;
-    r.ntok = left < G::kNMax ? left : G::kNMax;
-    return r;
-  };
+  const Units units{t_e, t_tok0, t_ntok, t_pp, A, RB, G::kNMax};
 
   if (warp == 0) {
     // =========================== TMA producer (this CTA's rows and token half) ==============
@@ -558,13 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < G::kBRows; j += 8)
             tma_load_2d(sb + h * G::kBHalf + j * 128, &tmB, &full[stg], kx + 64 * h, t0 + j);
       };
-      int64_t u = it_beg / KI;
-      int kk0 = static_cast<int>(it_beg - u * KI);
-      Unit un = it_beg < it_end ? decode(u) : Unit{};
+      int kk0 = static_cast<int>(it_beg % KI);
+      Units::Cursor uc = units.seek(it_beg / KI);
+      Unit un = it_beg < it_end ? units.unit(uc) : Unit{};
       // weights first (they do not depend on the preceding kernel), token tiles after the wait
       const int64_t npre = (it_end - it_beg) < G::kStages ? (it_end - it_beg) : G::kStages;
       {
-        int64_t pu = u;
+        Units::Cursor pc = uc;
         int pk = kk0;
         Unit pun = un;
         for (int64_t q = 0; q < npre; ++q) {
@@ -572,7 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_a(static_cast<int>(q), pun, pk);
           if (++pk == KI && q + 1 < npre) {
             pk = 0;
-            pun = decode(++pu);
+            units.next(pc);
+            pun = units.unit(pc);
           }
         }
       }
@@ -587,8 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (++kk0 == KI) {
           kk0 = 0;
-          ++u;
-          if (it_beg + q + 1 < it_end) un = decode(u);
+          units.next(uc);
+          if (it_beg + q + 1 < it_end) un = units.unit(uc);
         }
       }
       for (int64_t it = it_beg + npre; it < it_end; ++it) {
@@ -606,8 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (++kk0 == KI && it + 1 < it_end) {
           kk0 = 0;
-          ++u;
-          un = decode(u);
+          units.next(uc);
+          un = units.unit(uc);
         }
       }
       // never leave copies in flight
@@ -638,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pdl_allow_successor();
     }
   } else if (warp < kConvWarp0) {
-    promote<G>(smem, empty, d_empty, tmem_base, args, it_beg, it_end, KI, W, NC, pair_id, rank, s_misc, decode);
+    promote<G>(smem, empty, d_empty, tmem_base, args, it_beg, it_end, KI, W, NC, pair_id, rank, s_misc, units);
   } else {
     convert<G>(smem, full, empty, a_full, a_empty, d_empty, tmem_base, rank, args, it_beg, it_end);
   }
