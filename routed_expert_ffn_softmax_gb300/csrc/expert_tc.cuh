@@ -170,9 +170,26 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       t_pp[1 + lane * 8 + i] = run;
     }
     if (lane == 0) t_pp[0] = 0;
+    // One token-tile shape for the whole launch: the largest pass's token count, rounded up to 16.
+    // Every stage loads that many token rows and every MMA takes that many columns; columns past a
+    // pass's own tokens meet the following rows (or TMA's zero fill) and are never read. Measured
+    // on GB300, a shape per pass made stages of different passes cost different times, which the
+    // equal-stage stream-K split turned into CTAs finishing apart (4-5% at 16 tokens per expert).
+    int m = 16;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int a = lane * 8 + i;
+      if (a < A) {
+        const int n = t_ntok[a] < G::kNMax ? t_ntok[a] : G::kNMax;
+        m = n > m ? n : m;
+      }
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) s_misc[12] = ((m + 15) >> 4) * 16;
   }
   __syncthreads();
   const uint32_t tmem_base = *tmem_slot;
+  const int n_tile = s_misc[12];  // token rows per stage and MMA columns, 16..kNMax
 
   const int RB = (args.rows + 127) / 128;
   const int KI = (args.K + G::kKStage - 1) / G::kKStage;
@@ -209,7 +226,7 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
     int64_t u = it_beg / KI;
     int kk0 = static_cast<int>(it_beg - u * KI);
     Unit un = it_beg < it_end ? decode(u) : Unit{};
-    auto bbytes = [](const Unit& w) { return ((w.ntok + 15) >> 4) * 16 * 128; };
+    const int bbytes = n_tile * 128;
     auto issue_a = [&](int stg, const Unit& w, int kk) {
       uint8_t* st = smem + stg * G::kStage;
       if (kGateUp) {
@@ -221,8 +238,7 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
     };
     auto issue_b = [&](int stg, const Unit& w, int kk) {
       uint8_t* sb = smem + stg * G::kStage + G::kWBytes;
-      const int n16 = (w.ntok + 15) >> 4;
-      for (int j = 0; j < n16; ++j) tma_load_2d(sb + j * 2048, &tmB, &full[stg], kk * G::kKStage, w.tok0 + 16 * j);
+      for (int j = 0; j < n_tile; j += 16) tma_load_2d(sb + j * 128, &tmB, &full[stg], kk * G::kKStage, w.tok0 + j);
     };
     // weights first (they do not depend on the preceding kernel), token tiles after the wait
     const int64_t npre = (it_end - it_beg) < G::kStages ? (it_end - it_beg) : G::kStages;
@@ -232,7 +248,7 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       Unit pun = un;
       for (int64_t q = 0; q < npre; ++q) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[q], G::kWBytes + bbytes(pun));
+          mbar_arrive_expect_tx(&full[q], G::kWBytes + bbytes);
           issue_a(static_cast<int>(q), pun, pk);
         }
         if (++pk == KI && q + 1 < npre) {
@@ -279,7 +295,7 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       }
       for (int64_t q = 0; q < n; ++q) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], G::kWBytes + bbytes(un));
+          mbar_arrive_expect_tx(&full[stage], G::kWBytes + bbytes);
           issue_a(stage, un, kk0 + static_cast<int>(q));
           issue_b(stage, un, kk0 + static_cast<int>(q));
         }
@@ -322,13 +338,10 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int64_t piece = 0;
-      int64_t u = it_beg / KI;
-      int kk = static_cast<int>(it_beg - u * KI);
-      Unit un{};
-      if (it_beg < it_end) un = decode(u);
+      int kk = static_cast<int>(it_beg % KI);
       const uint32_t smem_base = smem_addr(smem);
+      const uint32_t idesc = umma_idesc_bf16_m128(n_tile);
       for (int64_t it = it_beg; it < it_end; ++it) {
-        if (kk == 0 && it != it_beg) un = decode(++u);
         const bool first = (it == it_beg) || (kk == 0);
         const bool last = (kk == KI - 1) || (it == it_end - 1);
         const int b = static_cast<int>(piece & 1);
@@ -345,10 +358,8 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
         }
         if (ok) {
           tc_fence_after_sync();
-          const int npad = ((un.ntok + 15) >> 4) * 16;
           const uint32_t st = smem_base + stage * G::kStage;
           const uint32_t d = tmem_base + b * G::kAccCols;
-          const uint32_t idesc = umma_idesc_bf16_m128(npad);
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
             const uint64_t db = umma_desc_sw128(st + G::kWBytes + 32 * s);
