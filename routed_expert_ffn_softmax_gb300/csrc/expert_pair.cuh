@@ -498,25 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
 
   // schedule tables, read before waiting for the preceding kernel (see expert_tc.cuh)
-  int A = *args.num_active;
-  A = A < 0 ? 0 : (A > args.E ? args.E : A);
-  for (int a = tid; a < kTable; a += kThreads) {
-    int passes = 0;
-    if (a < A) {
-      const int e = args.active[a];
-      int tok0 = 0, ntok = 0;
-      if (e >= 0 && e < args.E) {
-        tok0 = args.offsets[e];
-        ntok = args.offsets[e + 1] - tok0;
-      }
-      if (tok0 < 0 || ntok < 0 || static_cast<int64_t>(tok0) + ntok > args.P) ntok = 0;
-      t_e[a] = e;
-      t_tok0[a] = tok0;
-      t_ntok[a] = ntok;
-      passes = (ntok + G::kNMax - 1) / G::kNMax;
-    }
-    t_pp[a + 1] = passes;
-  }
+  const int A = tc::load_schedule<kThreads, G::kNMax>(args, t_e, t_tok0, t_ntok, t_pp);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();

@@ -81,6 +81,53 @@ struct Unit {
   int e, tok0, ntok, rb;
 };
 
+// The schedule table of the active experts: expert, first token row and token count per active
+// expert, and its pass count in pp[a + 1] (the caller forms the prefix sums). The active count,
+// the active list and the offsets are loaded together, the offsets staged in pp (E + 1 <=
+// kTable + 1 entries), so the table costs one round trip to memory instead of three dependent
+// ones. Every thread of the block calls it (it synchronises the block).
+template <int kThreads, int kPassTokens>
+__device__ __forceinline__ int load_schedule(const Args& args, int* t_e, int* t_tok0, int* t_ntok, int* pp) {
+  constexpr int kPer = (kTable + kThreads - 1) / kThreads;
+  const int tid = threadIdx.x;
+  int A = *args.num_active;
+  int ev[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int a = tid + i * kThreads;
+    ev[i] = a < args.E ? args.active[a] : -1;
+  }
+  for (int j = tid; j <= args.E; j += kThreads) pp[j] = args.offsets[j];
+  A = A < 0 ? 0 : (A > args.E ? args.E : A);
+  __syncthreads();
+  int passes[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int a = tid + i * kThreads;
+    passes[i] = 0;
+    if (a < A) {
+      const int e = ev[i];
+      int tok0 = 0, ntok = 0;
+      if (e >= 0 && e < args.E) {
+        tok0 = pp[e];
+        ntok = pp[e + 1] - tok0;
+      }
+      if (tok0 < 0 || ntok < 0 || static_cast<int64_t>(tok0) + ntok > args.P) ntok = 0;
+      t_e[a] = e;
+      t_tok0[a] = tok0;
+      t_ntok[a] = ntok;
+      passes[i] = (ntok + kPassTokens - 1) / kPassTokens;
+    }
+  }
+  __syncthreads();  // every thread has read the staged offsets
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int a = tid + i * kThreads;
+    if (a < kTable) pp[a + 1] = passes[i];
+  }
+  return A;
+}
+
 template <bool kGateUp>
 __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -123,29 +170,12 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
   }
   if (warp == 1) tmem_alloc(tmem_slot, G::kTmemCols);
 
-  // ---- schedule tables (threads 0..191 cover experts 0..191; experts 192..255 by the loop)
-  // They are read before waiting for the preceding kernel: every kernel of this library waits
-  // for its predecessor before it lets its successor start, so all work two launches back has
-  // completed, and the routing tables are always at least that far back.
-  int A = *args.num_active;
-  A = A < 0 ? 0 : (A > args.E ? args.E : A);
-  for (int a = tid; a < kTable; a += kThreads) {
-    int passes = 0;
-    if (a < A) {
-      const int e = args.active[a];
-      int tok0 = 0, ntok = 0;
-      if (e >= 0 && e < args.E) {
-        tok0 = args.offsets[e];
-        ntok = args.offsets[e + 1] - tok0;
-      }
-      if (tok0 < 0 || ntok < 0 || static_cast<int64_t>(tok0) + ntok > args.P) ntok = 0;
-      t_e[a] = e;
-      t_tok0[a] = tok0;
-      t_ntok[a] = ntok;
-      passes = (ntok + G::kNMax - 1) / G::kNMax;
-    }
-    t_pp[a + 1] = passes;
-  }
+  // ---- schedule tables. They are read before waiting for the preceding kernel: every kernel of
+  // this library waits for its predecessor before it lets its successor start, so all work two
+  // launches back has completed, and the routing tables are always at least that far back (a
+  // standalone call begins with a memset, after which its first kernel starts only once all
+  // earlier work has completed).
+  const int A = load_schedule<kThreads, G::kNMax>(args, t_e, t_tok0, t_ntok, t_pp);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();

@@ -30,9 +30,11 @@ __device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib)
 // Top-k of one token by the calling warp. Each lane sorts its (up to 8) logits once, best first
 // (odd-even merge network, 19 compare-exchanges); every round the lanes' heads meet in an xor
 // butterfly, which leaves the winner in all lanes, and the winning lane drops its head.
-// Past E a lane holds (-inf, none), which loses to every real expert.
+// Past E a lane holds (-inf, none), which loses to every real expert. Round j's winner goes to
+// sel_v[j] / sel_i[j] (shared memory, k entries): per-lane arrays indexed by the round would live
+// in local memory.
 __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int tok, int E, int k, int32_t* ids,
-                                           float* w, int* s_ids = nullptr) {
+                                           float* w, float* sel_v, int* sel_i) {
   const int lane = threadIdx.x & 31;
   const float* l = logits + static_cast<int64_t>(tok) * E;
   constexpr int kNone = 0x7fffffff;
@@ -63,14 +65,6 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
   MOE_CX(2, 4); MOE_CX(3, 5);
   MOE_CX(1, 2); MOE_CX(3, 4); MOE_CX(5, 6);
 #undef MOE_CX
-  // selection round j stays with lane j % 32, slot j / 32 (k <= E <= 256)
-  float sv[8];
-  int si[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    sv[q] = 0.0f;
-    si[q] = 0;
-  }
   float m = -INFINITY;  // the largest kept logit
   for (int j = 0; j < k; ++j) {
     float bv = cv[0];
@@ -94,22 +88,19 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
       ci[7] = kNone;
     }
     if (j == 0) m = bv;
-    if ((j & 31) == lane) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q == (j >> 5)) {
-          sv[q] = bv;
-          si[q] = bi;
-        }
+    if (lane == 0) {
+      sel_v[j] = bv;
+      sel_i[j] = bi;
     }
   }
+  __syncwarp();
   // renormalised softmax over the kept logits: exp(l_j - m) / sum of them
   float ex[8];
   float part = 0.0f;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int j = lane + 32 * q;
-    ex[q] = j < k ? expf(__fsub_rn(sv[q], m)) : 0.0f;
+    ex[q] = j < k ? expf(__fsub_rn(sel_v[j], m)) : 0.0f;
     part = __fadd_rn(part, ex[q]);
   }
 #pragma unroll
@@ -118,9 +109,8 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
   for (int q = 0; q < 8; ++q) {
     const int j = lane + 32 * q;
     if (j < k) {
-      ids[static_cast<int64_t>(tok) * k + j] = si[q];
+      ids[static_cast<int64_t>(tok) * k + j] = sel_i[j];
       w[static_cast<int64_t>(tok) * k + j] = __fdiv_rn(ex[q], part);
-      if (s_ids != nullptr) s_ids[tok * k + j] = si[q];
     }
   }
 }
@@ -130,8 +120,10 @@ __global__ void __launch_bounds__(kTopkWarpsPerBlock * 32)
                       int32_t* __restrict__ ids, float* __restrict__ w) {
   pdl_wait_predecessor();
   pdl_allow_successor();
+  __shared__ float s_sv[kTopkWarpsPerBlock][256];
+  __shared__ int s_si[kTopkWarpsPerBlock][256];
   const int tok = blockIdx.x * kTopkWarpsPerBlock + (threadIdx.x >> 5);
-  if (tok < T) topk_token(logits, tok, E, k, ids, w);
+  if (tok < T) topk_token(logits, tok, E, k, ids, w, s_sv[threadIdx.x >> 5], s_si[threadIdx.x >> 5]);
 }
 
 // ---------------------------------------------------------------------------------
@@ -259,12 +251,12 @@ __global__ void __launch_bounds__(kScanThreads)
                        int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_pos,
                        int32_t* __restrict__ active, int32_t* __restrict__ num_active,
                        int32_t* __restrict__ zero_words, int n_zero) {
-  __shared__ int s_ids[kFusedRouteMaxP];
+  __shared__ int s_ids[kFusedRouteMaxP];  // token t's experts at t * k .. t * k + k - 1
+  __shared__ float s_val[kFusedRouteMaxP];
   __shared__ int s_cnt[256];
   __shared__ int s_off[256];
   __shared__ unsigned long long s_tok[256];  // bit t: token t routed to the expert
   pdl_wait_predecessor();
-  pdl_allow_successor();
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   for (int i = tid; i < n_zero; i += kScanThreads) zero_words[i] = 0;
@@ -273,7 +265,8 @@ __global__ void __launch_bounds__(kScanThreads)
     s_tok[tid] = 0ull;
   }
   __syncthreads();
-  for (int tok = tid >> 5; tok < T; tok += kScanWarps) topk_token(logits, tok, E, k, ids, w, s_ids);
+  for (int tok = tid >> 5; tok < T; tok += kScanWarps)
+    topk_token(logits, tok, E, k, ids, w, s_val + tok * k, s_ids + tok * k);
   __syncthreads();
   const int P = T * k;
   for (int a = tid; a < P; a += kScanThreads) {
@@ -318,6 +311,9 @@ __global__ void __launch_bounds__(kScanThreads)
     sorted_token[p] = t;
     inv_pos[a] = p;
   }
+  // the successor is let go only now: launched early, its blocks could do nothing but wait
+  // (measured on GB300 together with the shared-memory selection above: routing 1 µs shorter)
+  pdl_allow_successor();
 }
 
 // ---------------------------------------------------------------------------------
