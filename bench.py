@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -109,13 +110,22 @@ EXPERT_SOURCES = ("expert_tc.cuh", "expert_pair.cuh", "moe_device.cuh", "expert_
 ATTN_SOURCES = ("gqa_decode.cu", "moe_device.cuh")
 
 
+def _code_only(text: str) -> str:
+    """Source text without // and /* */ comments, trailing blanks and empty lines (the sources hold
+    no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash(sources=EXPERT_SOURCES) -> str:
-    """Hash of a kernel's sources; a recorded DRAM-traffic figure is used only while it matches."""
+    """Hash of a kernel's sources, comments left out; a recorded DRAM-traffic figure is used only
+    while it matches (a change of code, not of comments, voids it)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "routed_expert_ffn_softmax_gb300", "csrc")
     for n in sources:
-        with open(os.path.join(csrc, n), "rb") as f:
-            h.update(n.encode() + f.read())
+        with open(os.path.join(csrc, n), encoding="utf-8") as f:
+            h.update((n + "\n" + _code_only(f.read())).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,10 +8,11 @@
 // Per CTA (one per SM, persistent, stream-K over (expert pass, 128-row block) x 64-element
 // reduction stages; 6 warps):
 //   warp 0      TMA producer: per stage the weight tile(s) (gate and up: 2 x 128 rows x 128 B;
-//               down: 128 rows x 128 B) and the stage's token tile (up to 64 rows, 16 at a time);
-//   warp 1      owns the TMEM allocation; its lane 0 issues tcgen05.mma (M = 128, N = tokens of
-//               the pass rounded up to 16, K = 16 per instruction) and commits each stage back to
-//               the producer and each finished unit to the epilogue;
+//               down: 128 rows x 128 B) and the stage's token tile (the launch's largest pass
+//               rounded up to 16 rows, at most 64, 16 at a time);
+//   warp 1      owns the TMEM allocation; its lane 0 issues tcgen05.mma (M = 128, N = that tile's
+//               rows, K = 16 per instruction) and commits each stage back to the producer and
+//               each finished unit to the epilogue;
 //   warps 2-5   epilogue: TMEM -> registers (thread = weight row), SiLU(g)*u -> h (gate+up) or
 //               Y (down), or the fp32 partial of a unit that another CTA finishes.
 // Accumulators are double buffered in TMEM per unit, so the epilogue of one unit overlaps the MMAs
