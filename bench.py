@@ -111,10 +111,10 @@ ATTN_SOURCES = ("gqa_decode.cu", "moe_device.cuh")
 
 
 def _code_only(text: str) -> str:
-    """Source text without // and /* */ comments, trailing blanks and empty lines (the sources hold
-    no comment markers inside string literals)."""
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    """Source text without // and /* */ comments, with each line's whitespace runs collapsed and
+    empty lines dropped (the sources hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    lines = (re.sub(r"\s+", " ", re.sub(r"//.*$", "", ln)).strip() for ln in text.splitlines())
     return "\n".join(ln for ln in lines if ln)
 
 
