@@ -105,9 +105,16 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# the sources of the roofline kernels and of their launches: the expert kernels, the attention kernel
+# the sources of the roofline kernels and of their launches: the expert kernels (all of them, and
+# the BF16 family alone, whose captures an INT8-only change leaves valid), the attention kernel
 EXPERT_SOURCES = ("expert_tc.cuh", "expert_pair.cuh", "moe_device.cuh", "expert_launch.cu")
+BF16_SOURCES = ("expert_tc.cuh", "moe_device.cuh", "expert_launch.cu")
 ATTN_SOURCES = ("gqa_decode.cu", "moe_device.cuh")
+
+
+def expert_sources(wtype: str):
+    """The sources a workload's expert kernels are built from."""
+    return BF16_SOURCES if wtype == "bf16" else EXPERT_SOURCES
 
 
 def _code_only(text: str) -> str:
@@ -368,7 +375,7 @@ def bench_ours(args, cfg, T):
         peak, peak_kind = hbm_peak()
         peak_kind = f"{peak_kind} (hbm_gbs, copy bandwidth)"
     workload_name = f"{cfg.name}_T{T}" + ("_hostweights" if host else "")
-    traffic = recorded_traffic(workload_name)
+    traffic = recorded_traffic(workload_name, expert_sources(cfg.wtype))
 
     # ---- end to end through the C ABI: host inputs in, host result out, every step
     x_h = [t[0].cpu().pin_memory() for t in wl.tokens]

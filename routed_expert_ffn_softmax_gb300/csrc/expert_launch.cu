@@ -321,12 +321,13 @@ cudaError_t launch_pair_int8_n(const ExpertFfnPlan& p, cudaStream_t s) {
                           td, td, dn);
 }
 
-// Passes of 16 tokens (three accumulator buffers) while the experts see at most about eleven tokens
-// each on average, passes of 32 above: measured on GB300 (Qwen3-235B shapes), the shorter passes
-// are 6-10% faster up to 8 assignments per expert, 3% faster at 10, 1% slower at 12 and 19% slower at 16
-// (experts past 16 tokens take two passes and stream their weights twice).
+// Passes of 16 tokens (three TMEM operand buffers instead of two, half the promotion work) while
+// the experts see at most about nine tokens each on average, passes of 32 above: measured on GB300
+// (Qwen3-235B shapes), the shorter passes are 2-10% faster up to 8 assignments per expert, 1%
+// slower at 10, 5% slower at 12 (experts past 16 tokens take two passes and stream their weights
+// twice).
 cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
-  if (static_cast<int64_t>(p.P) <= 11LL * p.E) return launch_pair_int8_n<16>(p, s);
+  if (static_cast<int64_t>(p.P) <= 9LL * p.E) return launch_pair_int8_n<16>(p, s);
   return launch_pair_int8_n<32>(p, s);
 }
 

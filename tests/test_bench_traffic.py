@@ -5,6 +5,7 @@ import json
 import os
 
 import bench
+import moe_workloads as mw
 
 
 def test_code_only_drops_comments_and_blank_lines():
@@ -43,8 +44,9 @@ def test_committed_captures_match_the_current_kernels():
     """Every committed expert and attention capture was taken on the kernels now in the tree."""
     with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
-    want = {"EXPERT": bench.kernel_source_hash(bench.EXPERT_SOURCES),
-            "ATTN": bench.kernel_source_hash(bench.ATTN_SOURCES)}
     for name, e in rec.items():
-        kind = "ATTN" if name.endswith("_attn") else "EXPERT"
-        assert e["kernel_source_hash"] == want[kind], name
+        if name.endswith("_attn"):
+            sources = bench.ATTN_SOURCES
+        else:
+            sources = bench.expert_sources(mw.CONFIGS[name.rsplit("_T", 1)[0]].wtype)
+        assert e["kernel_source_hash"] == bench.kernel_source_hash(sources), name

@@ -158,8 +158,8 @@ SMALL = [
     (12, 256, 256, 32, 1, "bf16", ()),      # top_k = 1
     (4, 256, 384, 8, 2, "int8", ()),
     (70, 384, 256, 8, 4, "int8", (2,)),
-    (40, 256, 384, 8, 2, "int8", (3,)),     # 16-token passes (P <= 11 E), expert 3 past one pass
-    (56, 256, 256, 8, 2, "int8", (6,)),     # 32-token passes (P > 11 E): 2 for expert 6, 1 for the rest
+    (36, 256, 384, 8, 2, "int8", (3,)),     # 16-token passes (P <= 9 E), expert 3 past one pass
+    (56, 256, 256, 8, 2, "int8", (6,)),     # 32-token passes (P > 9 E): 2 for expert 6, 1 for the rest
     (60, 256, 256, 8, 2, "bf16", (1,)),     # one tile shape for the launch, set by expert 1's pass
     # about one token per expert (P = T * k <= E)
     (3, 264, 200, 8, 2, "bf16", ()),        # H, I not multiples of 64
