@@ -332,7 +332,7 @@ moe_status_t ffn_forward_impl(const uint16_t* x, const float* logits, const void
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const bool int8 = wtype == MOE_W_INT8_G128;
   if (int8)  // the INT8 kernels read only the fp16 copy of the gathered rows: write it directly
-    e = moe::launch_gather_f16(x, H, P, sorted_token, reinterpret_cast<uint16_t*>(ws + L.xg16),
+    e = moe::launch_gather_f16(x, T, H, P, sorted_token, reinterpret_cast<uint16_t*>(ws + L.xg16),
                                reinterpret_cast<float*>(ws + L.xg_scale), sms, s);
   else
     e = moe::launch_gather(x, T, H, top_k, sorted_token, xg, sms, s);

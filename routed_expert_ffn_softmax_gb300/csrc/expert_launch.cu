@@ -70,8 +70,10 @@ constexpr int kRowThreads = 256;
 
 __global__ void __launch_bounds__(kRowThreads)
     rows_to_f16_kernel(const uint4* __restrict__ src, int K8, int64_t P, uint4* __restrict__ dst,
-                       float* __restrict__ row_scale, const int32_t* __restrict__ src_rows) {
+                       float* __restrict__ row_scale, const int32_t* __restrict__ src_rows,
+                       int64_t src_prefetch_bytes) {
   __shared__ float s_max[kRowThreads / 32];
+  prefetch_l2_grid(src, src_prefetch_bytes);
   pdl_wait_predecessor();
   pdl_allow_successor();
   const int tid = threadIdx.x;
@@ -121,11 +123,12 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 cudaError_t launch_rows_to_f16(const uint16_t* src, int K, int P, uint16_t* dst, float* row_scale, int num_sms,
-                               cudaStream_t s, const int32_t* src_rows = nullptr) {
+                               cudaStream_t s, const int32_t* src_rows = nullptr, int64_t src_prefetch_bytes = 0) {
   int blocks = P < num_sms * 4 ? P : num_sms * 4;
   if (blocks < 1) blocks = 1;
   return launch_pdl(rows_to_f16_kernel, dim3(blocks), dim3(kRowThreads), 0, s, reinterpret_cast<const uint4*>(src),
-                    K / 8, static_cast<int64_t>(P), reinterpret_cast<uint4*>(dst), row_scale, src_rows);
+                    K / 8, static_cast<int64_t>(P), reinterpret_cast<uint4*>(dst), row_scale, src_rows,
+                    src_prefetch_bytes);
 }
 
 template <bool kGateUp>
@@ -333,9 +336,12 @@ cudaError_t launch_pair_int8(const ExpertFfnPlan& p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_gather_f16(const uint16_t* x, int H, int P, const int32_t* sorted_token, uint16_t* xg16,
+cudaError_t launch_gather_f16(const uint16_t* x, int T, int H, int P, const int32_t* sorted_token, uint16_t* xg16,
                               float* xg_scale, int num_sms, cudaStream_t stream) {
-  return launch_rows_to_f16(x, H, P, xg16, xg_scale, num_sms, stream, sorted_token);
+  // a decode batch's token rows (at most a few MB) are warmed in L2 before the wait for routing
+  const int64_t x_bytes = static_cast<int64_t>(T) * H * 2;
+  return launch_rows_to_f16(x, H, P, xg16, xg_scale, num_sms, stream, sorted_token,
+                            x_bytes <= kPrefetchMaxBytes ? x_bytes : int64_t{0});
 }
 
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream) {

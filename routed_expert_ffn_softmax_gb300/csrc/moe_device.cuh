@@ -82,6 +82,16 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
+// Warm L2 with inputs a kernel reads right after waiting for its predecessor. Safe before the wait:
+// a line the predecessor still writes is updated in L2 by that write (L2 is where it lands).
+// Lines are 128 bytes; [base, base + bytes) is prefetched by the grid's threads together.
+__device__ __forceinline__ void prefetch_l2_grid(const void* base, int64_t bytes) {
+  const int64_t lines = (bytes + 127) / 128;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines; i += step)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(base) + i * 128));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -31,6 +31,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
                          int32_t* offsets, int32_t* sorted_token, int32_t* inv_pos, int32_t* active,
                          int32_t* num_active, int32_t* zero_words, int n_zero, cudaStream_t stream);
 
+// The gathers warm the token rows in L2 before waiting for routing when they are at most this size.
+constexpr int64_t kPrefetchMaxBytes = int64_t{4} << 20;
+
 cudaError_t launch_gather(const uint16_t* x, int T, int H, int k, const int32_t* sorted_token, uint16_t* xg,
                           int num_sms, cudaStream_t stream);
 
@@ -38,7 +41,7 @@ cudaError_t launch_combine(const float* Y, const int32_t* inv_pos, const float* 
                            uint16_t* out, int num_sms, cudaStream_t stream);
 
 // INT8 forward path: gather the token rows straight into their fp16 copy (see ExpertFfnPlan::xg16).
-cudaError_t launch_gather_f16(const uint16_t* x, int H, int P, const int32_t* sorted_token, uint16_t* xg16,
+cudaError_t launch_gather_f16(const uint16_t* x, int T, int H, int P, const int32_t* sorted_token, uint16_t* xg16,
                               float* xg_scale, int num_sms, cudaStream_t stream);
 
 // fp32 slots per CTA the expert kernels' stream-K partials need (the larger of the two kernel

@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(kScanThreads)
   __shared__ int s_cnt[256];
   __shared__ int s_off[256];
   __shared__ unsigned long long s_tok[256];  // bit t: token t routed to the expert
+  prefetch_l2_grid(logits, static_cast<int64_t>(T) * E * 4);
   pdl_wait_predecessor();
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -320,7 +321,8 @@ __global__ void __launch_bounds__(kScanThreads)
 // xg[p, :] = x[sorted_token[p], :], 16 bytes per thread.
 __global__ void __launch_bounds__(256)
     gather_kernel(const uint4* __restrict__ x, int H8, const int32_t* __restrict__ sorted_token,
-                  int64_t P, uint4* __restrict__ xg) {
+                  int64_t P, uint4* __restrict__ xg, int64_t x_prefetch_bytes) {
+  prefetch_l2_grid(x, x_prefetch_bytes);
   pdl_wait_predecessor();
   pdl_allow_successor();
   const int64_t n = P * H8;
@@ -388,8 +390,11 @@ cudaError_t launch_gather(const uint16_t* x, int T, int H, int k, const int32_t*
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  // a decode batch's token rows (at most a few MB) are warmed in L2 before the wait for routing
+  const int64_t x_bytes = static_cast<int64_t>(T) * H * 2;
   return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
-                    reinterpret_cast<const uint4*>(x), H8, sorted_token, P, reinterpret_cast<uint4*>(xg));
+                    reinterpret_cast<const uint4*>(x), H8, sorted_token, P, reinterpret_cast<uint4*>(xg),
+                    x_bytes <= kPrefetchMaxBytes ? x_bytes : int64_t{0});
 }
 
 cudaError_t launch_combine(const float* Y, const int32_t* inv_pos, const float* w, int T, int k, int H,
