@@ -150,6 +150,38 @@ def recorded_traffic(workload: str, sources=EXPERT_SOURCES):
     return None
 
 
+def run_pipelined(n_steps, h2d_fn, compute_fn, d2h_fn, stream, dev):
+    """n_steps end-to-end steps through the C ABI: step i's inputs are copied in from pinned host
+    memory (h2d_fn(i, b), on a copy stream), the step runs (compute_fn(i, b), on `stream`) and its
+    result is copied back (d2h_fn(i, b), on a second copy stream). Two buffer sets, b = i % 2, so
+    that a step's copies overlap its neighbours' compute, as a serving loop overlaps them; every
+    copy of every step lies between the two returned events."""
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_read = [torch.cuda.Event() for _ in range(2)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(h2d)
+    for i in range(n_steps):
+        b = i & 1
+        if i >= 2:
+            h2d.wait_event(done[b])  # step i - 2 has read this input buffer
+        with torch.cuda.stream(h2d):
+            h2d_fn(i, b)
+        in_ready[b].record(h2d)
+        stream.wait_event(in_ready[b])
+        if i >= 2:
+            stream.wait_event(out_read[b])  # step i - 2's result has been read back
+        compute_fn(i, b)
+        done[b].record(stream)
+        d2h.wait_event(done[b])
+        with torch.cuda.stream(d2h):
+            d2h_fn(i, b)
+        out_read[b].record(d2h)
+    end.record(d2h)  # after the last read-back, which waited for the last step and its inputs
+    return start, end
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled in the background."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -377,28 +409,28 @@ def bench_ours(args, cfg, T):
     workload_name = f"{cfg.name}_T{T}" + ("_hostweights" if host else "")
     traffic = recorded_traffic(workload_name, expert_sources(cfg.wtype))
 
-    # ---- end to end through the C ABI: host inputs in, host result out, every step
+    # ---- end to end through the C ABI: host inputs in, host result out, every step (the copies
+    # overlap the neighbouring steps' compute, double-buffered)
     x_h = [t[0].cpu().pin_memory() for t in wl.tokens]
     lg_h = [t[1].cpu().pin_memory() for t in wl.tokens]
-    out_h = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(wl.tokens[0][0])
-    lg_d = torch.empty_like(wl.tokens[0][1])
+    out_h = [torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(wl.tokens[0][0]) for _ in range(2)]
+    lg_d = [torch.empty_like(wl.tokens[0][1]) for _ in range(2)]
+    out_d = [out, torch.empty_like(out)]
 
-    def e2e_step(c):
-        L = wl.layers[c]
-        x_d.copy_(x_h[c], non_blocking=True)
-        lg_d.copy_(lg_h[c], non_blocking=True)
-        ffn_forward(moe, cfg, L, x_d, lg_d, out, ws, stream)
-        out_h.copy_(out, non_blocking=True)
+    def e2e_in(i, b):
+        x_d[b].copy_(x_h[i % copies], non_blocking=True)
+        lg_d[b].copy_(lg_h[i % copies], non_blocking=True)
 
-    for i in range(3):
-        e2e_step(i % copies)
+    def e2e_step(i, b):
+        ffn_forward(moe, cfg, wl.layers[i % copies], x_d[b], lg_d[b], out_d[b], ws, stream)
+
+    def e2e_out(i, b):
+        out_h[b].copy_(out_d[b], non_blocking=True)
+
+    run_pipelined(3, e2e_in, e2e_step, e2e_out, stream, dev)
     barrier_sync()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(args.steps):
-        e2e_step(i % copies)
-    b.record(stream)
+    a, b = run_pipelined(args.steps, e2e_in, e2e_step, e2e_out, stream, dev)
     barrier_sync()
     e2e_ms, e2e_value, _ = aggregate_over_ranks(a.elapsed_time(b), bytes_timed, T * args.steps, ws_n, dev)
 
@@ -659,26 +691,27 @@ def bench_attention_ours(args, acfg):
     workload_name = acfg.name
 
     # ---- end to end through the C ABI: query and lengths in from pinned host memory, output back
+    # (the copies overlap the neighbouring calls' compute, double-buffered)
     q_h = wl.q.cpu().pin_memory()
     lens_h = wl.lens.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_d = torch.empty_like(wl.q)
-    lens_d = torch.empty_like(wl.lens)
+    out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    q_d = [torch.empty_like(wl.q) for _ in range(2)]
+    lens_d = [torch.empty_like(wl.lens) for _ in range(2)]
+    out_d = [out, torch.empty_like(out)]
 
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        lens_d.copy_(lens_h, non_blocking=True)
-        moe.moe_gqa_decode(q_d, wl.k, wl.v, lens_d, acfg.scale, out, ws, stream)
-        out_h.copy_(out, non_blocking=True)
+    def e2e_in(i, b):
+        q_d[b].copy_(q_h, non_blocking=True)
+        lens_d[b].copy_(lens_h, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_step(i, b):
+        moe.moe_gqa_decode(q_d[b], wl.k, wl.v, lens_d[b], acfg.scale, out_d[b], ws, stream)
+
+    def e2e_out(i, b):
+        out_h[b].copy_(out_d[b], non_blocking=True)
+
+    run_pipelined(3, e2e_in, e2e_step, e2e_out, stream, dev)
     barrier_sync()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    b.record(stream)
+    a, b = run_pipelined(args.steps, e2e_in, e2e_step, e2e_out, stream, dev)
     barrier_sync()
     _, e2e_value, _ = aggregate_over_ranks(a.elapsed_time(b), wl.kv_bytes * args.steps, acfg.B * args.steps, ws_n,
                                            dev)
