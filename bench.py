@@ -1,11 +1,13 @@
 """Benchmark of the routed-expert FFN decode step on GB300 (and of decode GQA attention).
 
 One step = one pass of the whole path (route -> gather -> gate+up -> down -> combine)
-through the C ABI over one decode batch of synthetic tokens. Default workload: the
-Mixtral-8x7B-shaped expert layer (H=4096, I=14336, E=8, top-2, BF16 weights) at
-T=16 tokens (about 4 tokens per expert). The metric is the weight-stream bandwidth:
-bytes of the active experts' weights (each read once) per second; tokens/s is
-reported beside it.
+through the C ABI over one decode batch of synthetic tokens. Default workload: the largest
+of the expert shapes, DeepSeek-V3 (H=7168, I=2048, E=256, top-8, BF16 weights, 22.5 GB per
+layer) at T=512 tokens (16 tokens per expert). The metric is the weight-stream bandwidth:
+bytes of the active experts' weights (each read once) per second; tokens/s is reported
+beside it. The same JSON line carries a sweep over every (config, T) point of the five
+expert workloads (Mixtral-8x7B, Mixtral-8x22B and its skewed variant, DeepSeek-V3, Qwen3-235B
+INT8), each with its GB/s, % of peak, tokens/s and the expert call's roofline fraction.
 
 `--op attention` measures decode-phase GQA attention instead (moe_gqa_decode, one new
 token per sequence against its key/value cache): one step = one call over the batch;
@@ -14,7 +16,7 @@ sequences/s beside it. Default workload: Qwen3-30B-A3B-shaped heads (32 query he
 4 key/value heads, d = 128), 64 sequences of 512..8192 tokens.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
-        [--config NAME] [--T T] [--sweep] [--no-cpu-baseline]
+        [--config NAME] [--T T] [--no-sweep] [--sweep-configs A,B] [--no-cpu-baseline]
         [--op attention [--attn-config NAME]]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path is not sharded); value = all ranks' bytes / the slowest rank's time.
@@ -24,14 +26,16 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import re
 import json
+import math
 import os
+import re
 import statistics
 import subprocess
 import sys
 import time
 
+import numpy as np
 import torch
 import torch.distributed as dist
 
@@ -266,17 +270,34 @@ def expert_ffn(moe, cfg, L, xg, r, Y, ws, stream):
 
 
 # ------------------------------------------------------------------ workload
-class Workload:
-    """Weights (several distinct layer copies, so consecutive steps do not re-read the previous
-    step's experts from L2) and one decode batch per copy. The weights live in HBM, or with
-    host_weights in pinned host memory (Grace LPDDR5X on a GB300 node), which the same kernels
-    read over NVLink-C2C. The number of active experts per batch (which sets the weight bytes a
-    step must stream) is read from the library's own routing kernel."""
+# The (config, T) points of the sweep: every expert shape and token count of the five workloads.
+SWEEP_CONFIGS = ("mixtral8x7b", "mixtral8x22b", "mixtral8x22b_skew", "dsv3", "qwen3_int8")
+L2_BYTES = 129e6
 
-    def __init__(self, cfg: mw.MoEConfig, T: int, copies: int, device, moe, seed: int = 0,
-                 host_weights: bool = False):
-        self.cfg, self.T, self.device = cfg, T, device
-        self.layers, self.tokens = [], []
+
+def auto_copies(cfg: mw.MoEConfig, Ts, max_bytes: float = 120e9) -> int:
+    """Distinct weight copies rotated across steps: enough that the active experts of all copies
+    together exceed 4x L2 at the smallest T (so a step never finds the previous steps' experts in
+    L2), at least 2, at most 8 and at most `max_bytes` of weights."""
+    per_copy = min(mw.expected_active(cfg, T) for T in Ts) * cfg.weight_bytes_per_expert
+    n = max(2, math.ceil(4 * L2_BYTES / per_copy))
+    fit = int(max_bytes // (cfg.E * cfg.weight_bytes_per_expert))
+    return max(2, min(n, 8, fit))
+
+
+def weights_key(cfg: mw.MoEConfig):
+    """Configs that differ only in their router logits (the skewed variant) share one set of weights."""
+    return (cfg.H, cfg.I, cfg.E, cfg.wtype, cfg.seed)
+
+
+class Layers:
+    """Several distinct copies of one layer's expert weights (so that consecutive steps do not re-read
+    the previous steps' experts from L2). The weights live in HBM, or with host_weights in pinned host
+    memory (Grace LPDDR5X on a GB300 node), which the same kernels read over NVLink-C2C."""
+
+    def __init__(self, cfg: mw.MoEConfig, copies: int, device, seed: int = 0, host_weights: bool = False):
+        self.cfg, self.key, self.copies = cfg, weights_key(cfg), copies
+        self.layers = []
         for c in range(copies):
             layer = mw.make_layer(cfg, seed=seed + 1000 * c, device=device)
             if host_weights:
@@ -284,7 +305,16 @@ class Workload:
                              else None) for n, v in layer.items()}
                 torch.cuda.synchronize()
             self.layers.append(layer)
-            self.tokens.append(mw.make_tokens(cfg, T, seed=seed + 1000 * c, device=device))
+
+
+class Workload:
+    """One decode batch of T tokens per weight copy. The number of active experts per batch (which
+    sets the weight bytes a step must stream) is read from the library's own routing kernel."""
+
+    def __init__(self, cfg: mw.MoEConfig, T: int, layers: Layers, device, moe, seed: int = 0):
+        self.cfg, self.T, self.device = cfg, T, device
+        self.layers = layers.layers
+        self.tokens = [mw.make_tokens(cfg, T, seed=seed + 1000 * c, device=device) for c in range(layers.copies)]
         self.active = []
         k = cfg.top_k
         for x, lg in self.tokens:
@@ -296,11 +326,15 @@ class Workload:
             self.active.append(int(outs[-1].item()))
         self.wt = 0 if cfg.wtype == "bf16" else 1  # the residual split uses the INT8 workspace
 
+    @property
+    def copies(self) -> int:
+        return len(self.layers)
+
     def weight_bytes(self, c: int) -> int:
         return self.active[c] * self.cfg.weight_bytes_per_expert
 
     def mean_weight_bytes(self) -> float:
-        return sum(self.weight_bytes(c) for c in range(len(self.layers))) / len(self.layers)
+        return sum(self.weight_bytes(c) for c in range(self.copies)) / self.copies
 
     def step_other_bytes(self) -> int:
         """Bytes of a whole step besides the weights: x and logits read, routing tables, the
@@ -315,6 +349,44 @@ class Workload:
         """Token-side algorithmic bytes of the expert kernels: xg read, h write + read, Y write."""
         cfg, P = self.cfg, self.T * self.cfg.top_k
         return P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 4
+
+
+def expert_call_roofline(moe, wl: Workload, ws, stream, n: int, peak: float):
+    """The expert-FFN call (moe_expert_ffn: the expert kernels, which stream the weights) timed alone
+    with events on the launching stream; routing and gather run outside the events. Returns
+    (achieved GB/s of algorithmic bytes, frac of peak, average ms per call, algorithmic bytes)."""
+    cfg, T, dev = wl.cfg, wl.T, wl.device
+    r = {nm: torch.empty(sz, dtype=dt, device=dev) for nm, sz, dt in (
+        ("ids", (T, cfg.top_k), torch.int32), ("w", (T, cfg.top_k), torch.float32), ("counts", (cfg.E,), torch.int32),
+        ("offsets", (cfg.E + 1,), torch.int32), ("st", (T * cfg.top_k,), torch.int32),
+        ("inv", (T, cfg.top_k), torch.int32), ("act", (cfg.E,), torch.int32), ("na", (1,), torch.int32))}
+    xg = torch.empty(T * cfg.top_k, cfg.H, dtype=torch.bfloat16, device=dev)
+    Y = torch.empty(T * cfg.top_k, cfg.H, dtype=torch.float32, device=dev)
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+    evs, nbytes = [], []
+    for i in range(n + 3):
+        c = i % wl.copies
+        L = wl.layers[c]
+        x, lg = wl.tokens[c]
+        moe.moe_route_topk(lg, cfg.top_k, r["ids"], r["w"], r["counts"], r["offsets"], r["st"], r["inv"], r["act"],
+                           r["na"], stream)
+        moe.moe_gather(x, cfg.top_k, r["st"], xg, stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        expert_ffn(moe, cfg, L, xg, r, Y, ws, stream)
+        b.record(stream)
+        moe.moe_combine(Y, r["inv"], r["w"], cfg.top_k, out, stream)
+        if i >= 3:
+            evs.append((a, b))
+            nbytes.append(wl.weight_bytes(c) + wl.act_bytes())
+    torch.cuda.synchronize()
+    if moe.workspace_status(ws) != 0:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    t = [a.elapsed_time(b) for a, b in evs]
+    avg_ms = sum(t) / len(t)
+    alg = sum(nbytes) / len(nbytes)
+    achieved = alg / (avg_ms * 1e-3) / 1e9
+    return achieved, achieved / peak, avg_ms, alg
 
 
 # ------------------------------------------------------------------ our implementation
@@ -334,9 +406,10 @@ def bench_ours(args, cfg, T):
         dist.barrier()
     moe.load()
 
-    copies = args.copies
     host = args.weights == "host"
-    wl = Workload(cfg, T, copies, dev, moe, host_weights=host)
+    copies = args.copies if args.copies > 0 else auto_copies(cfg, [T])
+    layers = Layers(cfg, copies, dev, host_weights=host)
+    wl = Workload(cfg, T, layers, dev, moe)
     stream = torch.cuda.current_stream()
     ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wl.wt, dev)
     out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
@@ -367,45 +440,20 @@ def bench_ours(args, cfg, T):
         barrier_sync()
     clocks = clk.summary()
     total_ms = ev0.elapsed_time(ev1)
-    per_step = per_step_times(lambda i: step(i % copies), min(args.steps, 100), stream)
+    per_step = per_step_times(lambda i: step(i % copies), max(min(args.steps, 100), 20), stream)
     if moe.workspace_status(ws) != 0:
         raise RuntimeError("a kernel reported a timed-out wait")
     bytes_timed = sum(wl.weight_bytes(i % copies) for i in range(args.steps))
     total_ms, value, tokens_s = aggregate_over_ranks(total_ms, bytes_timed, T * args.steps, ws_n, dev)
 
     # ---- dominant kernels: the expert FFN pair (gate+up, down), timed alone with events
-    r = {n: torch.empty(s, dtype=dt, device=dev) for n, s, dt in (
-        ("ids", (T, cfg.top_k), torch.int32), ("w", (T, cfg.top_k), torch.float32), ("counts", (cfg.E,), torch.int32),
-        ("offsets", (cfg.E + 1,), torch.int32), ("st", (T * cfg.top_k,), torch.int32),
-        ("inv", (T, cfg.top_k), torch.int32), ("act", (cfg.E,), torch.int32), ("na", (1,), torch.int32))}
-    xg = torch.empty(T * cfg.top_k, cfg.H, dtype=torch.bfloat16, device=dev)
-    Y = torch.empty(T * cfg.top_k, cfg.H, dtype=torch.float32, device=dev)
-    ffn_ev, ffn_bytes = [], []
-    n_ffn = max(min(args.steps, 200), 20)
-    for i in range(n_ffn + 3):
-        c = i % copies
-        L = wl.layers[c]
-        x, lg = wl.tokens[c]
-        moe.moe_route_topk(lg, cfg.top_k, r["ids"], r["w"], r["counts"], r["offsets"], r["st"], r["inv"], r["act"],
-                           r["na"], stream)
-        moe.moe_gather(x, cfg.top_k, r["st"], xg, stream)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        expert_ffn(moe, cfg, L, xg, r, Y, ws, stream)
-        b.record(stream)
-        moe.moe_combine(Y, r["inv"], r["w"], cfg.top_k, out, stream)
-        if i >= 3:
-            ffn_ev.append((a, b))
-            ffn_bytes.append(wl.weight_bytes(c) + wl.act_bytes())
-    torch.cuda.synchronize()
-    ffn_t = [a.elapsed_time(b) for a, b in ffn_ev]
-    ffn_avg_ms = sum(ffn_t) / len(ffn_t)
-    ffn_achieved = (sum(ffn_bytes) / len(ffn_bytes)) / (ffn_avg_ms * 1e-3) / 1e9
     if host:
         peak, peak_kind = round(c2c_copy_peak(dev), 1), "measured in this run (pinned host -> device copy, NVLink-C2C)"
     else:
         peak, peak_kind = hbm_peak()
         peak_kind = f"{peak_kind} (hbm_gbs, copy bandwidth)"
+    ffn_achieved, ffn_frac, ffn_avg_ms, ffn_alg = expert_call_roofline(moe, wl, ws, stream,
+                                                                        max(min(args.steps, 200), 20), peak)
     workload_name = f"{cfg.name}_T{T}" + ("_hostweights" if host else "")
     traffic = recorded_traffic(workload_name, expert_sources(cfg.wtype))
 
@@ -447,8 +495,7 @@ def bench_ours(args, cfg, T):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {"bf16": "bf16", "int8": "int8 weights, bf16 activations",
-                  "int8_residual": "int8 + int8 residual gate/up, int8 down, bf16 activations"}[cfg.wtype],
+        "dtype": DTYPE[cfg.wtype],
         "data": "synthetic (seeded N(0,1) tokens and logits, N(0,0.02) weights)",
         "pct_of_peak": round(100.0 * value / ws_n / peak, 2),
         "tokens_per_s": round(tokens_s, 1),
@@ -475,79 +522,121 @@ def bench_ours(args, cfg, T):
             "peak": peak,
             "peak_kind": peak_kind,
             "unit": "GB/s",
-            "frac": round(ffn_achieved / peak, 4),
+            "frac": round(ffn_frac, 4),
             "traffic": traffic,
             "avg_launch_ms": round(ffn_avg_ms, 5),
-            "algorithmic_bytes_per_launch": int(sum(ffn_bytes) / len(ffn_bytes)),
+            "algorithmic_bytes_per_launch": int(ffn_alg),
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 2},
         "gpu_launches": kernels_per_step(cfg, T) * args.steps,
         "clocks": clocks,
     }
-    if args.sweep and rank == 0:
-        result["sweep"] = sweep(cfg, dev, moe, copies, host)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(cfg, T, wl, budget_s=args.cpu_budget)
+    held = [layers]  # the sweep reuses these weights for its points of the same config, then frees them
+    del x_h, lg_h, out_h, x_d, lg_d, out_d, ws, wl, layers
+    if rank == 0 and not args.no_sweep and not host:
+        result["sweep"] = sweep(moe, dev, peak, held, args.sweep_configs.split(","))
+    held.clear()
     if ws_n > 1:
         dist.barrier()
         dist.destroy_process_group()
     return result if rank == 0 else None
 
 
-def sweep(cfg, dev, moe, copies, host=False):
-    """GB/s and tokens/s at every T of the workload (same method, fewer steps)."""
-    rows = []
-    for T in cfg.T:
-        wl = Workload(cfg, T, copies, dev, moe, host_weights=host)
-        ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wl.wt, dev)
-        out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
-        s = torch.cuda.current_stream()
+DTYPE = {"bf16": "bf16", "int8": "int8 weights, bf16 activations",
+         "int8_residual": "int8 + int8 residual gate/up, int8 down, bf16 activations"}
 
-        def step(c):
-            x, lg = wl.tokens[c]
-            ffn_forward(moe, cfg, wl.layers[c], x, lg, out, ws, s)
-        for i in range(10):
-            step(i % copies)
-        torch.cuda.synchronize()
-        n = 100
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s)
-        for i in range(n):
-            step(i % copies)
-        b.record(s)
-        torch.cuda.synchronize()
-        if moe.workspace_status(ws) != 0:
-            raise RuntimeError("a kernel reported a timed-out wait")
-        ms = a.elapsed_time(b) / n
-        wb = sum(wl.weight_bytes(i % copies) for i in range(n)) / n
-        rows.append({"T": T, "active_experts": round(sum(wl.active) / len(wl.active), 2),
-                     "us_per_step": round(ms * 1e3, 2), "GB_s": round(wb / (ms * 1e-3) / 1e9, 1),
-                     "tokens_per_s": round(T / (ms * 1e-3), 1)})
-        del wl, ws
-        torch.cuda.empty_cache()
-    return rows
+
+def measure_point(moe, cfg, T, layers: Layers, dev, peak, steps=60, warmup=5, n_roof=40):
+    """GB/s and tokens/s of whole steps at one (config, T) point (two events around `steps` steps),
+    and the expert call's roofline fraction."""
+    wl = Workload(cfg, T, layers, dev, moe)
+    ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wl.wt, dev)
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream()
+
+    def step(c):
+        x, lg = wl.tokens[c]
+        ffn_forward(moe, cfg, wl.layers[c], x, lg, out, ws, s)
+    for i in range(warmup):
+        step(i % wl.copies)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for i in range(steps):
+        step(i % wl.copies)
+    b.record(s)
+    torch.cuda.synchronize()
+    if moe.workspace_status(ws) != 0:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    ms = a.elapsed_time(b) / steps
+    wb = sum(wl.weight_bytes(i % wl.copies) for i in range(steps)) / steps
+    gbs = wb / (ms * 1e-3) / 1e9
+    ach, frac, avg_ms, _ = expert_call_roofline(moe, wl, ws, s, n_roof, peak)
+    row = {"workload": f"{cfg.name}_T{T}", "weights": cfg.wtype, "T": T,
+           "active_experts": round(sum(wl.active) / len(wl.active), 2),
+           "tokens_per_expert": round(T * cfg.top_k * len(wl.active) / sum(wl.active), 2),
+           "us_per_step": round(ms * 1e3, 2), "GB_s": round(gbs, 1), "pct_of_peak": round(100 * gbs / peak, 2),
+           "tokens_per_s": round(T / (ms * 1e-3), 1), "launches_per_step": kernels_per_step(cfg, T),
+           "roofline": {"kernel": "expert FFN call (moe_expert_ffn), timed alone", "achieved": round(ach, 1),
+                        "frac": round(frac, 4), "avg_launch_us": round(avg_ms * 1e3, 2)},
+           "copies": wl.copies}
+    del wl, ws
+    return row
+
+
+def sweep(moe, dev, peak, held, names):
+    """Every (config, T) point of the named workloads, measured the same way as the headline with
+    fewer steps (weights rotate over distinct copies at every point). `held` may hold the headline's
+    Layers; configs sharing its weights go first and reuse them."""
+    have = held.pop() if held else None
+    if have is not None:
+        names = sorted(names, key=lambda n: weights_key(mw.CONFIGS[n]) != have.key)
+    rows = []
+    with ClockSampler(dev.index or 0) as clk:
+        for name in names:
+            cfg = mw.CONFIGS[name]
+            if have is None or have.key != weights_key(cfg):
+                have = None
+                torch.cuda.empty_cache()
+                have = Layers(cfg, auto_copies(cfg, cfg.T), dev)
+            for T in cfg.T:
+                rows.append(measure_point(moe, cfg, T, have, dev, peak))
+                torch.cuda.empty_cache()
+    have = None
+    torch.cuda.empty_cache()
+    return {"points": rows, "peak_gbs": peak, "clocks": clk.summary(),
+            "method": "per point: 5 warm-up steps, 60 timed steps between two events (GB/s = active-expert "
+                      "weight bytes / time), then the expert call alone for 40 calls (roofline frac = its "
+                      "algorithmic bytes / time / peak); weights rotate over distinct copies"}
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline leg)
-def oracle_rate(cfg, T, budget_s, layer_cpu, x, lg):
-    """Run the oracle token by token over the batch (cycling) until the time budget is spent,
-    at least one token; return (weight GB/s for the whole batch, tokens/s, tokens run, seconds)."""
+def oracle_rate(cfg, T, budget_s, experts, x, lg):
+    """Run the oracle token by token over the batch's first tokens (cycling) until the time budget is
+    spent, at least one token. `experts` maps an expert id to its CPU weights (W_gate, W_up, W_down,
+    s_*). Returns (weight GB/s for the whole batch, tokens/s, tokens run, seconds)."""
     import oracle
     ro = oracle.route(lg, cfg.top_k)
     full_bytes = ro["num_active"] * cfg.weight_bytes_per_expert
+    sample = sample_tokens(ro, T, cfg.top_k, len(experts))
     t0 = time.perf_counter()
     n = 0
     while True:
-        t = n % T
-        L = layer_cpu
-        if cfg.wtype == "int8_residual":
-            oracle.forward_residual(x[t:t + 1], lg[t:t + 1], L["W_gate"], L["s_gate"], L["Wr_gate"], L["sr_gate"],
-                                    L["W_up"], L["s_up"], L["Wr_up"], L["sr_up"], L["W_down"], L["s_down"],
-                                    top_k=cfg.top_k)
-        else:
-            oracle.forward(x[t:t + 1], lg[t:t + 1], L["W_gate"], L["W_up"], L["W_down"], L["s_gate"], L["s_up"],
-                           L["s_down"], wtype=cfg.wtype, top_k=cfg.top_k)
+        t = sample[n % len(sample)]
+        ys = []
+        for j in range(cfg.top_k):
+            W = experts[int(ro["ids"][t, j])]
+            if cfg.wtype == "int8_residual":
+                h, _, _ = oracle.gateup_token_residual(x[t], W["W_gate"], W["s_gate"], W["Wr_gate"], W["sr_gate"],
+                                                       W["W_up"], W["s_up"], W["Wr_up"], W["sr_up"])
+                ys.append(oracle.down_token(h, W["W_down"], W["s_down"], "int8"))
+            else:
+                h, _, _ = oracle.gateup_token(x[t], W["W_gate"], W["W_up"], W["s_gate"], W["s_up"], cfg.wtype)
+                ys.append(oracle.down_token(h, W["W_down"], W["s_down"], cfg.wtype))
+        oracle.combine_token(np.stack(ys), ro["w"][t])
         n += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -555,6 +644,24 @@ def oracle_rate(cfg, T, budget_s, layer_cpu, x, lg):
     per_token = dt / n
     # the oracle's cost is linear in tokens: the whole batch takes T * per_token
     return full_bytes / (T * per_token) / 1e9, 1.0 / per_token, n, dt
+
+
+def sample_tokens(ro, T, k, max_experts):
+    """The batch's first tokens whose experts together number at most max_experts (at least one)."""
+    seen, out = set(), []
+    for t in range(T):
+        e = set(int(v) for v in ro["ids"][t])
+        if out and len(seen | e) > max_experts:
+            break
+        seen |= e
+        out.append(t)
+    return out
+
+
+def sample_experts(cfg, ro, T, max_experts, fetch):
+    """CPU weights of the experts of sample_tokens(...): fetch(e) returns one expert's tensors."""
+    need = sorted({int(v) for t in sample_tokens(ro, T, cfg.top_k, max_experts) for v in ro["ids"][t]})
+    return {e: fetch(e) for e in need}
 
 
 def cores_used():
@@ -566,15 +673,29 @@ def cores_used():
     return int(omp) if omp and omp.isdigit() else n
 
 
+CPU_SAMPLE_EXPERTS = 32
+
+
 def cpu_baseline(cfg, T, wl, budget_s):
-    layer = {n: (v.cpu() if v is not None else None) for n, v in wl.layers[0].items()}
+    import oracle
     x, lg = (t.cpu() for t in wl.tokens[0])
-    gbs, tok_s, n, dt = oracle_rate(cfg, T, budget_s, layer, x, lg)
+    ro = oracle.route(lg, cfg.top_k)
+    L = wl.layers[0]
+    experts = sample_experts(cfg, ro, T, CPU_SAMPLE_EXPERTS,
+                             lambda e: {n: (v[e].cpu() if v is not None else None) for n, v in L.items()})
+    gbs, tok_s, n, dt = oracle_rate(cfg, T, budget_s, experts, x, lg)
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
             "tokens_per_s": round(tok_s, 3),
-            "sample": f"{n} token evaluations cycling over the {T} tokens of the same batch ({dt:.1f} s of CPU "
-                      f"time); the oracle's time is linear in tokens, so GB/s = active-expert weight bytes of "
-                      f"the batch / ({T} x time per token)"}
+            "sample": f"{n} token evaluations cycling over the batch's first tokens whose experts number at most "
+                      f"{CPU_SAMPLE_EXPERTS} ({dt:.1f} s of CPU time); the oracle's time is linear in tokens and the "
+                      f"same for every token, so GB/s = active-expert weight bytes of the {T}-token batch / "
+                      f"({T} x time per token)"}
+
+
+def cpu_expert(cfg, e, seed=0):
+    """One expert's weights drawn on the CPU (the same draws make_layer makes for it)."""
+    L = mw.make_layer(cfg, seed=seed, device="cpu", experts=[e])
+    return {n: (v[0] if v is not None else None) for n, v in L.items()}
 
 
 def bench_reference(args, cfg, T):
@@ -586,12 +707,12 @@ def bench_reference(args, cfg, T):
     oracle.build()
     x, lg = mw.make_tokens(cfg, T, device="cpu")
     ro = oracle.route(lg, cfg.top_k)
-    layer = mw.make_layer(cfg, device="cpu")
+    experts = sample_experts(cfg, ro, T, CPU_SAMPLE_EXPERTS, lambda e: cpu_expert(cfg, e))
     nsteps = args.steps + args.warmup
     per_step_budget = max(0.02, args.cpu_budget * 4 / nsteps)
     vals, times = [], []
     for i in range(nsteps):
-        gbs, tok_s, n, dt = oracle_rate(cfg, T, per_step_budget, layer, x, lg)
+        gbs, tok_s, n, dt = oracle_rate(cfg, T, per_step_budget, experts, x, lg)
         if i >= args.warmup:
             vals.append(gbs)
             times.append(T / tok_s)
@@ -615,9 +736,10 @@ def bench_reference(args, cfg, T):
         "config": {"workload": f"{cfg.name}_T{T}", "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
                    "weights": cfg.wtype, "T": T, "active_experts": ro["num_active"]},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
-                         "sample": f"each step runs the oracle token by token over the T={T} batch for about "
-                                   f"{per_step_budget:.2f} s (at least one token) and scales to the whole batch "
-                                   f"(time is linear in tokens)"},
+                         "sample": f"each step runs the oracle token by token over the batch's first tokens whose "
+                                   f"experts number at most {CPU_SAMPLE_EXPERTS} (cycling) for about "
+                                   f"{per_step_budget:.2f} s (at least one token) and scales to the whole {T}-token "
+                                   f"batch (time is linear in tokens and the same for every token)"},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -847,12 +969,16 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--config", default="mixtral8x7b", choices=sorted(mw.CONFIGS))
-    ap.add_argument("--T", type=int, default=16)
-    ap.add_argument("--copies", type=int, default=3, help="distinct weight copies rotated across steps")
+    ap.add_argument("--config", default="dsv3", choices=sorted(mw.CONFIGS))
+    ap.add_argument("--T", type=int, default=512)
+    ap.add_argument("--copies", type=int, default=0,
+                    help="distinct weight copies rotated across steps (0: enough to exceed 4x L2, at least 2)")
     ap.add_argument("--weights", choices=("device", "host"), default="device",
                     help="where the expert weights live: HBM, or pinned host memory read over NVLink-C2C")
-    ap.add_argument("--sweep", action="store_true", help="also measure every T of the workload")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sweep over every (config, T) point of the expert workloads")
+    ap.add_argument("--sweep-configs", default=",".join(SWEEP_CONFIGS),
+                    help="comma-separated workloads the sweep covers (every T of each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--op", choices=("ffn", "attention"), default="ffn",

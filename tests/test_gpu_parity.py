@@ -249,35 +249,59 @@ def test_forward_zero_tokens_is_noop():
     torch.cuda.synchronize()
 
 
-# ------------------------------------------------------------------ full-size workloads, sampled
-def sampled_oracle_rows(cfg, Lg, x, lg, tokens):
-    """Oracle output rows for the sampled tokens; expert weights copied from the device."""
-    ro = oracle.route(lg.cpu(), cfg.top_k)
+# ------------------------------------------------------------------ full-size workloads, every token
+def oracle_rows(cfg, Lc, x, lg, tokens=None):
+    """Oracle output rows (fp32 values of the bf16 outputs) for `tokens` (default: all), computed
+    one token-expert assignment at a time from the CPU copy of the layer, and the oracle's routing."""
+    ro = oracle.route(lg, cfg.top_k)
+    tokens = range(x.shape[0]) if tokens is None else tokens
     rows = {}
-    cache = {}
     for t in tokens:
         ys = []
         for j in range(cfg.top_k):
             e = int(ro["ids"][t, j])
-            if e not in cache:
-                cache[e] = {n: (v[e].cpu() if v is not None else None) for n, v in Lg.items()}
-            W = cache[e]
-            h, _, _ = oracle.gateup_token(x[t].cpu(), W["W_gate"], W["W_up"], W["s_gate"], W["s_up"], cfg.wtype)
-            ys.append(oracle.down_token(h, W["W_down"], W["s_down"], cfg.wtype))
+            sc = (lambda n: Lc[n][e] if Lc[n] is not None else None)
+            h, _, _ = oracle.gateup_token(x[t], Lc["W_gate"][e], Lc["W_up"][e], sc("s_gate"), sc("s_up"), cfg.wtype)
+            ys.append(oracle.down_token(h, Lc["W_down"][e], sc("s_down"), cfg.wtype))
         out, _ = oracle.combine_token(np.stack(ys), ro["w"][t])
         rows[t] = oracle.bf16_bits_to_f32(out)
     return ro, rows
 
 
-FULL = [("mixtral8x7b", 1), ("mixtral8x7b", 16), ("mixtral8x7b", 64), ("mixtral8x22b", 4),
-        ("mixtral8x22b_skew", 64), ("dsv3", 1), ("dsv3", 16), ("dsv3", 512), ("qwen3_int8", 1), ("qwen3_int8", 8),
-        ("qwen3_int8", 256)]
+# Every (config, T) point of the four full-size expert shapes (HiNa-MoE §8.1 Table 3 at 1-16
+# tokens per expert), in config order so that one config's layer serves all its T.
+FULL = [(name, T) for name in ("mixtral8x7b", "mixtral8x22b", "mixtral8x22b_skew", "dsv3", "qwen3_int8")
+        for T in mw.CONFIGS[name].T]
+
+_LAYERS = {}
+
+
+def full_layer(name):
+    """The config's layer on the device and its CPU copy; one config is held at a time (the skewed
+    8x22B variant shares the 8x22B weights: only its router logits differ)."""
+    key = "mixtral8x22b" if name == "mixtral8x22b_skew" else name
+    if key not in _LAYERS:
+        _LAYERS.clear()
+        torch.cuda.empty_cache()
+        Lg = mw.make_layer(mw.CONFIGS[key], device=DEV)
+        Lc = {n: (v.cpu() if v is not None else None) for n, v in Lg.items()}
+        _LAYERS[key] = (Lg, Lc)
+    return _LAYERS[key]
+
+
+@pytest.fixture(scope="module")
+def _release_layers():
+    yield
+    _LAYERS.clear()
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("name,T", FULL)
-def test_full_size_sampled(name, T):
+def test_full_size_every_token(name, T, _release_layers):
+    """moe_ffn_forward on the full-size layer; every token's output row against the oracle, and the
+    whole batch's routing bit-exact."""
     cfg = mw.CONFIGS[name]
-    Lg = mw.make_layer(cfg, device=DEV)
+    Lg, Lc = full_layer(name)
     x, lg = mw.make_tokens(cfg, T, device=DEV)
     wt = moe.MOE_W_INT8_G128 if cfg.wtype == "int8" else moe.MOE_W_BF16
     ws = moe.alloc_workspace(T, cfg.H, cfg.I, cfg.E, cfg.top_k, wt, DEV)
@@ -288,11 +312,7 @@ def test_full_size_sampled(name, T):
     assert moe.workspace_status(ws) == 0
     got = to_np_f32(out)
     assert np.all(np.isfinite(got))
-    tokens = sorted({0, T - 1, T // 2})
-    ro, rows = sampled_oracle_rows(cfg, Lg, x.cpu(), lg, tokens)
-    for t in tokens:
+    ro, rows = oracle_rows(cfg, Lc, x.cpu(), lg.cpu())
+    for t in range(T):
         assert_moe_close(got[t], rows[t], cfg.wtype, f"{name} T={T} token {t}")
-    # routing of the whole batch is bit-exact (read back from the workspace via a separate call)
     check_route(gpu_route(lg, cfg.top_k), ro)
-    del Lg
-    torch.cuda.empty_cache()

@@ -10,8 +10,8 @@ import torch
 import moe_workloads as mw
 import oracle
 import routed_expert_ffn_softmax_gb300 as moe
-from test_gpu_parity import (DEV, assert_moe_close, check_route, gpu_route, run_forward_ws, sampled_oracle_rows,
-                             small_case, to_np_f32)
+from test_gpu_parity import (DEV, assert_moe_close, check_route, gpu_route, oracle_rows, run_forward_ws, small_case,
+                             to_np_f32)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,16 +59,15 @@ def test_host_weights_match_oracle_and_device_run(T, H, I, E, k, wtype, skew):
 
 
 @pytest.mark.parametrize("name,T", [("mixtral8x7b", 16), ("qwen3_int8", 8)])
-def test_host_weights_full_size_sampled(name, T):
+def test_host_weights_full_size_every_token(name, T):
     cfg = mw.CONFIGS[name]
     Lg = mw.make_layer(cfg, device=DEV)
     Lh = pinned(Lg)
     x, lg = mw.make_tokens(cfg, T, device=DEV)
     got = to_np_f32(forward(Lh, x, lg, cfg.top_k, cfg))
     assert np.all(np.isfinite(got))
-    tokens = sorted({0, T - 1, T // 2})
-    ro, rows = sampled_oracle_rows(cfg, Lg, x.cpu(), lg, tokens)
-    for t in tokens:
+    ro, rows = oracle_rows(cfg, Lh, x.cpu(), lg.cpu())  # the pinned copy is the oracle's CPU layer
+    for t in range(T):
         assert_moe_close(got[t], rows[t], cfg.wtype, f"{name} T={T} token {t} (host weights)")
     check_route(gpu_route(lg, cfg.top_k), ro)
     del Lg, Lh

@@ -115,8 +115,8 @@ def test_residual_reaches_below_int8_error():
     assert np.abs(res - ref).mean() < np.abs(i8 - ref).mean()
 
 
-@pytest.mark.parametrize("T", [8, 64])
-def test_full_size_sampled(T):
+@pytest.mark.parametrize("T", [1, 8, 64, 256])
+def test_full_size_every_token(T):
     cfg = mw.CONFIGS["qwen3_int8_residual"]
     Lg = mw.make_layer(cfg, device=DEV)
     x, lg = mw.make_tokens(cfg, T, device=DEV)
@@ -129,15 +129,17 @@ def test_full_size_sampled(T):
     assert np.all(np.isfinite(got))
     ro = oracle.route(lg.cpu(), cfg.top_k)
     check_route(gpu_route(lg, cfg.top_k), ro)
-    for t in sorted({0, T // 2, T - 1}):
+    Lc = {n: Lg[n].cpu() for n in RES}
+    xc = x.cpu()
+    for t in range(T):
         ys = []
         for j in range(cfg.top_k):
             e = int(ro["ids"][t, j])
-            W = {n: Lg[n][e].cpu() for n in RES}
-            h, _, _ = oracle.gateup_token_residual(x[t].cpu(), W["W_gate"], W["s_gate"], W["Wr_gate"], W["sr_gate"],
+            W = {n: Lc[n][e] for n in RES}
+            h, _, _ = oracle.gateup_token_residual(xc[t], W["W_gate"], W["s_gate"], W["Wr_gate"], W["sr_gate"],
                                                    W["W_up"], W["s_up"], W["Wr_up"], W["sr_up"])
             ys.append(oracle.down_token(h, W["W_down"], W["s_down"], "int8"))
         row, _ = oracle.combine_token(np.stack(ys), ro["w"][t])
         assert_moe_close(got[t], oracle.bf16_bits_to_f32(row), "int8", f"residual full size T={T} token {t}")
-    del Lg
+    del Lg, Lc
     torch.cuda.empty_cache()
