@@ -51,10 +51,12 @@ METRIC_ATTN = "decode GQA attention key/value-cache read GB/s (% of peak) and se
 FALLBACK_HBM_GBS = 6800.0
 
 
-def kernels_per_step(cfg, T: int) -> int:
-    """Launches of one moe_ffn_forward: routing (one fused launch for T <= 64 and T*k <= 1024,
-    else top-k and scan), gather (INT8: straight into the fp16 copy), the expert kernels (INT8
-    adds the fp16 copy of h), combine."""
+def kernels_per_step(cfg, T: int, moe=None) -> int:
+    """Launches of one moe_ffn_forward under the library's current policy: 1 for the one-launch decode
+    step; otherwise routing (one fused launch for T <= 64 and T*k <= 1024, else top-k and scan), gather
+    (INT8: straight into the fp16 copy), the expert kernels (INT8 adds the fp16 copy of h), combine."""
+    if moe is not None and cfg.wtype != "int8_residual":
+        return moe.moe_ffn_forward_launches(T, cfg.H, cfg.I, cfg.E, cfg.top_k, 0 if cfg.wtype == "bf16" else 1)
     route = 1 if (T <= 64 and T * cfg.top_k <= 1024) else 2
     experts = 2 if cfg.wtype == "bf16" else 3
     return route + 1 + experts + 1
@@ -351,6 +353,42 @@ class Workload:
         return P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 4
 
 
+def decode_step_roofline(moe, wl: Workload, ws, stream, n: int, peak: float):
+    """The one-launch decode step is the whole step: its kernel timed per launch with events on the
+    launching stream (an event pair around every call). Algorithmic bytes = every array of the step,
+    each once. Returns (achieved GB/s, frac of peak, average ms per launch, algorithmic bytes)."""
+    cfg, T = wl.cfg, wl.T
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=wl.device)
+    evs, nbytes = [], []
+    for i in range(n + 3):
+        c = i % wl.copies
+        x, lg = wl.tokens[c]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ffn_forward(moe, cfg, wl.layers[c], x, lg, out, ws, stream)
+        b.record(stream)
+        if i >= 3:
+            evs.append((a, b))
+            nbytes.append(wl.weight_bytes(c) + wl.step_other_bytes())
+    torch.cuda.synchronize()
+    if moe.workspace_status(ws) != 0:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    t = [a.elapsed_time(b) for a, b in evs]
+    avg_ms = sum(t) / len(t)
+    alg = sum(nbytes) / len(nbytes)
+    achieved = alg / (avg_ms * 1e-3) / 1e9
+    return achieved, achieved / peak, avg_ms, alg
+
+
+def roofline_for(moe, wl: Workload, ws, stream, n: int, peak: float):
+    """(kernel description, achieved, frac, avg ms, algorithmic bytes) of the step's dominant kernel(s)."""
+    if kernels_per_step(wl.cfg, wl.T, moe) == 1:
+        return ("decode_step_kernel: the whole step in one launch (routing, gate+up with SiLU*up, down, "
+                "combine), timed per launch",) + decode_step_roofline(moe, wl, ws, stream, n, peak)
+    return ("expert FFN stream kernels (gate+up with SiLU*up, then down), timed together",) + \
+        expert_call_roofline(moe, wl, ws, stream, n, peak)
+
+
 def expert_call_roofline(moe, wl: Workload, ws, stream, n: int, peak: float):
     """The expert-FFN call (moe_expert_ffn: the expert kernels, which stream the weights) timed alone
     with events on the launching stream; routing and gather run outside the events. Returns
@@ -405,6 +443,7 @@ def bench_ours(args, cfg, T):
     if ws_n > 1:
         dist.barrier()
     moe.load()
+    moe.moe_set_decode_step_policy(args.decode_step_policy)
 
     host = args.weights == "host"
     copies = args.copies if args.copies > 0 else auto_copies(cfg, [T])
@@ -452,8 +491,8 @@ def bench_ours(args, cfg, T):
     else:
         peak, peak_kind = hbm_peak()
         peak_kind = f"{peak_kind} (hbm_gbs, copy bandwidth)"
-    ffn_achieved, ffn_frac, ffn_avg_ms, ffn_alg = expert_call_roofline(moe, wl, ws, stream,
-                                                                        max(min(args.steps, 200), 20), peak)
+    roof_kernel, ffn_achieved, ffn_frac, ffn_avg_ms, ffn_alg = roofline_for(moe, wl, ws, stream,
+                                                                             max(min(args.steps, 200), 20), peak)
     workload_name = f"{cfg.name}_T{T}" + ("_hostweights" if host else "")
     traffic = recorded_traffic(workload_name, expert_sources(cfg.wtype))
 
@@ -516,7 +555,7 @@ def bench_ours(args, cfg, T):
                   f"rotating over {copies} distinct weight copies",
         },
         "roofline": {
-            "kernel": "expert FFN stream kernels (gate+up with SiLU*up, then down), timed together",
+            "kernel": roof_kernel,
             "bound": "c2c" if host else "hbm",
             "achieved": round(ffn_achieved, 1),
             "peak": peak,
@@ -529,7 +568,7 @@ def bench_ours(args, cfg, T):
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 2},
-        "gpu_launches": kernels_per_step(cfg, T) * args.steps,
+        "gpu_launches": kernels_per_step(cfg, T, moe) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -574,13 +613,13 @@ def measure_point(moe, cfg, T, layers: Layers, dev, peak, steps=60, warmup=5, n_
     ms = a.elapsed_time(b) / steps
     wb = sum(wl.weight_bytes(i % wl.copies) for i in range(steps)) / steps
     gbs = wb / (ms * 1e-3) / 1e9
-    ach, frac, avg_ms, _ = expert_call_roofline(moe, wl, ws, s, n_roof, peak)
+    kernel, ach, frac, avg_ms, _ = roofline_for(moe, wl, ws, s, n_roof, peak)
     row = {"workload": f"{cfg.name}_T{T}", "weights": cfg.wtype, "T": T,
            "active_experts": round(sum(wl.active) / len(wl.active), 2),
            "tokens_per_expert": round(T * cfg.top_k * len(wl.active) / sum(wl.active), 2),
            "us_per_step": round(ms * 1e3, 2), "GB_s": round(gbs, 1), "pct_of_peak": round(100 * gbs / peak, 2),
-           "tokens_per_s": round(T / (ms * 1e-3), 1), "launches_per_step": kernels_per_step(cfg, T),
-           "roofline": {"kernel": "expert FFN call (moe_expert_ffn), timed alone", "achieved": round(ach, 1),
+           "tokens_per_s": round(T / (ms * 1e-3), 1), "launches_per_step": kernels_per_step(cfg, T, moe),
+           "roofline": {"kernel": kernel, "achieved": round(ach, 1),
                         "frac": round(frac, 4), "avg_launch_us": round(avg_ms * 1e3, 2)},
            "copies": wl.copies}
     del wl, ws
@@ -609,8 +648,10 @@ def sweep(moe, dev, peak, held, names):
     torch.cuda.empty_cache()
     return {"points": rows, "peak_gbs": peak, "clocks": clk.summary(),
             "method": "per point: 5 warm-up steps, 60 timed steps between two events (GB/s = active-expert "
-                      "weight bytes / time), then the expert call alone for 40 calls (roofline frac = its "
-                      "algorithmic bytes / time / peak); weights rotate over distinct copies"}
+                      "weight bytes / time), then the dominant kernel(s) for 40 calls with an event pair around "
+                      "each: the expert call (moe_expert_ffn) for the staged path, the whole step for the "
+                      "one-launch decode step (roofline frac = algorithmic bytes / time / peak); weights rotate "
+                      "over distinct copies"}
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline leg)
@@ -981,6 +1022,9 @@ def main():
                     help="comma-separated workloads the sweep covers (every T of each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--decode-step-policy", type=int, choices=(0, 1, 2), default=0,
+                    help="moe_ffn_forward's path: 0 by batch shape (default), 1 never the one-launch decode step, "
+                         "2 the one-launch decode step whenever the sizes allow")
     ap.add_argument("--op", choices=("ffn", "attention"), default="ffn",
                     help="ffn: the routed-expert FFN (default); attention: decode GQA attention")
     ap.add_argument("--attn-config", default="qwen3_30b_attn",

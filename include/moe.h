@@ -21,7 +21,9 @@
  *
  * Conventions shared by every entry point:
  *   - Every array pointer is a DEVICE pointer owned by the caller. The library
- *     allocates no memory and keeps no device state between calls.
+ *     allocates no memory and keeps no device state between calls, with one
+ *     exception: moe_expert_ffn_noalloc uses a fixed scratch array inside the
+ *     library (see there), which persists from load until the process exits.
  *   - Exception: the expert weights and scales (W_gate, W_up, W_down, s_gate,
  *     s_up, s_down) may also live in host memory the GPU can address (pinned or
  *     registered; on a GB300 node the Grace LPDDR5X), passed by that memory's
@@ -81,10 +83,15 @@ const char* moe_status_string(moe_status_t status);
  * these sizes (the same figure serves both). Returns 0 when the sizes are
  * invalid. Pure host computation; touches no device.
  *
+ * A workspace must be zero-filled before its first use (cudaMemset to 0); every
+ * call leaves its counters zero again, so it stays usable call after call.
+ *
  * The first 4 bytes of a workspace are a status word: a kernel that gives up
  * on a bounded wait (which does not happen in correct operation) writes a
  * nonzero code there and returns early, leaving the outputs undefined. Each
- * moe_ffn_forward / moe_expert_ffn call clears it at its start.
+ * moe_ffn_forward / moe_expert_ffn call clears it at its start. After a
+ * nonzero status, zero the whole workspace again before the next call (a call
+ * that gave up may leave counters behind).
  */
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, moe_wtype_t wtype);
 
@@ -162,7 +169,11 @@ moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets,
  *   All calls share that array and it keeps the last call's contents: calls whose kernels
  *   overlap on one GPU (several streams or host threads) race and give wrong results.
  *   The first call on a device looks up the array's device address with that device
- *   current; make it before any stream capture starts on that device.
+ *   current and keeps it for the life of the process: make that first call before any
+ *   stream capture starts on the device, and do not reset the device (cudaDeviceReset)
+ *   or switch it to another context between calls.
+ *   A kernel that gives up on a bounded wait records a nonzero code in the array's status
+ *   word; read it with moe_expert_ffn_noalloc_status. Each call clears it at its start.
  *   Calls no cudaMalloc/cudaFree and no allocating library routine.
  */
 moe_status_t moe_expert_ffn_noalloc(const uint16_t* xg, const int32_t* expert_offsets,
@@ -171,6 +182,14 @@ moe_status_t moe_expert_ffn_noalloc(const uint16_t* xg, const int32_t* expert_of
                                     const float* s_gate, const float* s_up, const float* s_down,
                                     moe_wtype_t wtype, int H, int I, int E, int P, float* Y,
                                     moe_stream_t stream);
+
+/*
+ * The status word of moe_expert_ffn_noalloc's scratch, as the last call on `stream` left it:
+ * waits until the stream's work so far is done, then copies the 4-byte word to *status_out
+ * (0 = no kernel gave up a wait). Allocates nothing. The paper has no counterpart.
+ * Returns MOE_ERR_INVALID_ARG for a null status_out, MOE_ERR_CUDA if the copy fails.
+ */
+moe_status_t moe_expert_ffn_noalloc_status(int32_t* status_out, moe_stream_t stream);
 
 /*
  * Routing-weighted combine back to row-major token order (HiNa-MoE §4.1, third
@@ -188,12 +207,44 @@ moe_status_t moe_combine(const float* Y, const int32_t* inv_pos, const float* to
  *   out [T, H] bf16;  workspace >= moe_workspace_size(T, H, I, E, top_k, wtype).
  * The routing, the gathered block, h and Y live in the workspace; the host never
  * learns the routing, so the call is free of host synchronisation.
+ * Small decode batches (by default when T * top_k <= 2 E, with T <= 32, T * top_k <= 256,
+ * H and I multiples of 128, for INT8 multiples of 512) run as ONE cooperative kernel that
+ * routes, streams both projections on CUDA-core FMAs and combines; larger batches run
+ * the routing, gather, tensor-core expert kernels and combine as separate launches.
+ * Both give results within the same tolerance of the definition; the routing tables in
+ * the workspace are the same. moe_set_decode_step_policy chooses between them.
  */
 moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void* W_gate,
                              const void* W_up, const void* W_down, const float* s_gate,
                              const float* s_up, const float* s_down, moe_wtype_t wtype, int T,
                              int H, int I, int E, int top_k, uint16_t* out, void* workspace,
                              size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Which implementation moe_ffn_forward uses (process-wide; the default is 0):
+ *   0  by batch shape (the rule above);
+ *   1  never the one-launch decode step;
+ *   2  the one-launch decode step whenever the sizes allow it.
+ * Returns MOE_ERR_INVALID_ARG for any other value. Affects only later calls.
+ */
+moe_status_t moe_set_decode_step_policy(int policy);
+
+/*
+ * Failure-detection test hook; the paper has no counterpart. While enabled (enable = 1), the
+ * one-launch decode step's grid-wide barrier waits for one more CTA than the launch has, so it
+ * never opens: every CTA gives up after wait_ns nanoseconds (1 us .. 2 s), records status 5 in
+ * the workspace status word, and the kernel runs to its end and returns (outputs undefined; the
+ * GPU and the context stay usable). Zero the workspace before its next use, as after any nonzero
+ * status. enable = 0 restores the normal barrier and its 2 s limit. Process-wide; affects only
+ * later calls. Returns MOE_ERR_INVALID_ARG for other values.
+ */
+moe_status_t moe_test_expire_grid_barrier(int enable, uint64_t wait_ns);
+
+/*
+ * Kernels one moe_ffn_forward call launches for these sizes under the current policy
+ * (1 for the one-launch decode step), or -1 when the sizes are invalid. Host only.
+ */
+int moe_ffn_forward_launches(int T, int H, int I, int E, int top_k, moe_wtype_t wtype);
 
 /*
  * Residual-split INT8 experts (RapidMoE, arXiv 2610.01265, "Residual-Split Representation" and

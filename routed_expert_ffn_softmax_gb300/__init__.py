@@ -25,8 +25,9 @@ __all__ = [
     "MoeError", "MOE_W_BF16", "MOE_W_INT8_G128", "load", "lib_path",
     "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
     "moe_expert_ffn", "moe_combine", "moe_ffn_forward", "alloc_workspace", "workspace_status",
-    "moe_expert_ffn_noalloc", "moe_gqa_workspace_size", "moe_gqa_decode", "alloc_gqa_workspace",
-    "moe_expert_ffn_residual", "moe_ffn_forward_residual",
+    "moe_expert_ffn_noalloc", "moe_expert_ffn_noalloc_status", "moe_gqa_workspace_size", "moe_gqa_decode", "alloc_gqa_workspace",
+    "moe_expert_ffn_residual", "moe_ffn_forward_residual", "moe_set_decode_step_policy", "moe_ffn_forward_launches",
+    "moe_test_expire_grid_barrier",
 ]
 
 MOE_W_BF16 = 0
@@ -73,6 +74,10 @@ def load() -> ctypes.CDLL:
         lib.moe_gqa_workspace_size.argtypes = [i, i, i, i, i]
         lib.moe_gqa_workspace_size.restype = z
         lib.moe_gqa_decode.argtypes = [P, P, P, P, i, i, i, i, i, ctypes.c_float, P, P, z, P]
+        lib.moe_set_decode_step_policy.argtypes = [i]
+        lib.moe_ffn_forward_launches.argtypes = [i, i, i, i, i, i]
+        for f in ("moe_set_decode_step_policy", "moe_ffn_forward_launches"):
+            getattr(lib, f).restype = i
         for f in ("moe_route_topk", "moe_gather", "moe_expert_ffn", "moe_combine", "moe_ffn_forward",
                   "moe_gqa_decode", "moe_expert_ffn_residual", "moe_ffn_forward_residual"):
             getattr(lib, f).restype = i
@@ -116,10 +121,11 @@ def moe_workspace_size(T: int, H: int, I: int, E: int, top_k: int, wtype: int = 
 
 
 def alloc_workspace(T, H, I, E, top_k, wtype=MOE_W_BF16, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (it must start zeroed; calls leave it reusable)."""
     n = moe_workspace_size(T, H, I, E, top_k, wtype)
     if n == 0:
         raise ValueError("invalid sizes for moe_workspace_size")
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def workspace_status(workspace: torch.Tensor) -> int:
@@ -166,6 +172,25 @@ def moe_ffn_forward(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, top_k
         _stream(stream)))
 
 
+def moe_set_decode_step_policy(policy: int) -> None:
+    """0: by batch shape (default); 1: never the one-launch decode step; 2: whenever the sizes allow."""
+    _check("moe_set_decode_step_policy", load().moe_set_decode_step_policy(policy))
+
+
+def moe_test_expire_grid_barrier(enable: bool, wait_ns: int = 2_000_000_000) -> None:
+    """Failure-detection test hook: the one-launch decode step's grid barrier never opens while enabled
+    and every CTA gives up after wait_ns (status 5 in the workspace; see include/moe.h)."""
+    f = load().moe_test_expire_grid_barrier
+    f.argtypes = [ctypes.c_int, ctypes.c_uint64]
+    f.restype = ctypes.c_int
+    _check("moe_test_expire_grid_barrier", f(1 if enable else 0, int(wait_ns)))
+
+
+def moe_ffn_forward_launches(T, H, I, E, top_k, wtype=MOE_W_BF16) -> int:
+    """Kernels one moe_ffn_forward call launches for these sizes under the current policy."""
+    return int(load().moe_ffn_forward_launches(T, H, I, E, top_k, wtype))
+
+
 def moe_expert_ffn_noalloc(xg, expert_offsets, active_experts, num_active, W_gate, W_up, W_down, s_gate, s_up,
                            s_down, Y, stream=None) -> None:
     """moe_expert_ffn for callers that cannot allocate: no workspace argument; the library's
@@ -181,6 +206,18 @@ def moe_expert_ffn_noalloc(xg, expert_offsets, active_experts, num_active, W_gat
     _check("moe_expert_ffn_noalloc", f(
         _ptr(xg), _ptr(expert_offsets), _ptr(active_experts), _ptr(num_active), _ptr(W_gate), _ptr(W_up),
         _ptr(W_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _wtype(W_gate), H, I, E, P, _ptr(Y), _stream(stream)))
+
+
+def moe_expert_ffn_noalloc_status(stream=None) -> int:
+    """The status word moe_expert_ffn_noalloc's scratch holds after the stream's work so far (0 = no
+    kernel gave up a wait)."""
+    lib = load()
+    f = lib.moe_expert_ffn_noalloc_status
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    word = ctypes.c_int32(-1)
+    _check("moe_expert_ffn_noalloc_status", f(ctypes.addressof(word), _stream(stream)))
+    return int(word.value)
 
 
 def moe_gqa_workspace_size(B: int, h_q: int, h_kv: int, d: int, L_cap: int) -> int:

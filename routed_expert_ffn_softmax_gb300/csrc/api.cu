@@ -21,18 +21,24 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Workspace layout, in order (each section 256-byte aligned):
-//   ctrl      status word (byte 0) + stream-K counters at byte 256
+//   ctrl      status word (byte 0), the fused decode step's grid barrier (bytes 8..15), stream-K
+//             counters at byte 256, the fused decode step's row-block counters at byte 2048
 //   partials  stream-K partial slots
 //   h         [P, I] bf16 (gate+up output)
 //   INT8 only: h16 [P, I] fp16, xg16 [P, H] fp16, h_scale [P], xg_scale [P] f32
 //   --- moe_ffn_forward only ---
-//   ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg [P,H] bf16, Y [P,H] f32
-constexpr size_t kCtrlBytes = 2048;
+//   ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg [P,H] bf16, Y [P,H] f32,
+//   INT8 only: hrec [P, I/128] records of 272 bytes (the fused decode step's fp16 h)
+constexpr size_t kCtrlBytes = 4096;
+constexpr size_t kGridBarrierOffset = 8;
 constexpr size_t kCountersOffset = 256;
+constexpr size_t kRowCountersOffset = 2048;
+constexpr int kMaxRowBlocks = static_cast<int>((kCtrlBytes - kRowCountersOffset) / 4);  // H <= 65536
 constexpr int kZeroWords = static_cast<int>((kCountersOffset + 4 * kMaxCtas) / 4);
 
 struct Layout {
-  size_t ctrl, partials, h, h16, xg16, h_scale, xg_scale, ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg, Y, total;
+  size_t ctrl, partials, h, h16, xg16, h_scale, xg_scale, ids, w, counts, offsets, sorted_token, inv_pos, active,
+      num_active, xg, Y, hrec, total;
 };
 
 Layout layout(int64_t P, int H, int I, int E, bool int8) {
@@ -75,6 +81,8 @@ Layout layout(int64_t P, int H, int I, int E, bool int8) {
   o = align_up(o + 2 * static_cast<size_t>(P) * H);
   L.Y = o;
   o = align_up(o + 4 * static_cast<size_t>(P) * H);
+  L.hrec = o;
+  if (int8) o = align_up(o + 272 * static_cast<size_t>(P) * (I / 128));
   L.total = o;
   return L;
 }
@@ -109,6 +117,21 @@ int sm_count() {
 }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// moe_set_decode_step_policy: 0 = by batch shape, 1 = never, 2 = whenever the sizes allow it.
+std::atomic<int> g_decode_policy{0};
+// moe_test_expire_grid_barrier: extra arrivals the decode step's grid barrier waits for, and its wait limit.
+std::atomic<int> g_grid_extra{0};
+std::atomic<unsigned long long> g_grid_wait_ns{2000000000ull};
+
+// Whether moe_ffn_forward runs the fused one-launch decode step for these sizes.
+bool use_decode_step(int T, int H, int I, int E, int top_k, moe_wtype_t wtype, bool residual) {
+  const int policy = g_decode_policy.load(std::memory_order_relaxed);
+  if (policy == 1 || residual) return false;
+  if (!moe::decode_step_supported(T, H, I, E, top_k, wtype == MOE_W_INT8_G128)) return false;
+  if (H / 128 > kMaxRowBlocks) return false;
+  return policy == 2;
+}
 
 // Residual-split parts of gate and up (INT8 only); all null when the weights are not split.
 struct Residual {
@@ -327,10 +350,52 @@ moe_status_t ffn_forward_impl(const uint16_t* x, const float* logits, const void
   uint16_t* xg = reinterpret_cast<uint16_t*>(ws + L.xg);
   float* Y = reinterpret_cast<float*>(ws + L.Y);
 
+  const bool int8 = wtype == MOE_W_INT8_G128;
+  if (use_decode_step(T, H, I, E, top_k, wtype, res.Wg != nullptr)) {
+    moe::DecodePlan plan{};
+    moe::DecodeArgs& a = plan.args;
+    a.x = x;
+    a.logits = logits;
+    a.out = out;
+    a.x16 = reinterpret_cast<uint16_t*>(ws + L.xg16);
+    a.h = int8 ? static_cast<void*>(ws + L.hrec) : static_cast<void*>(ws + L.h);
+    a.Y = Y;
+    a.partials = reinterpret_cast<float*>(ws + L.partials);
+    a.counters = I32(L.ctrl + kCountersOffset);
+    a.ccount = I32(L.ctrl + kRowCountersOffset);
+    a.gbar = I32(L.ctrl + kGridBarrierOffset);
+    a.status = I32(L.ctrl);
+    a.ids = ids;
+    a.w = w;
+    a.counts = I32(L.counts);
+    a.offsets = offsets;
+    a.sorted_token = sorted_token;
+    a.inv_pos = inv_pos;
+    a.active = active;
+    a.num_active = num_active;
+    a.T = T;
+    a.H = H;
+    a.I = I;
+    a.E = E;
+    a.k = top_k;
+    a.grid_extra = g_grid_extra.load(std::memory_order_relaxed);
+    a.grid_wait_ns = g_grid_wait_ns.load(std::memory_order_relaxed);
+    plan.W_gate = W_gate;
+    plan.W_up = W_up;
+    plan.W_down = W_down;
+    plan.s_gate = s_gate;
+    plan.s_up = s_up;
+    plan.s_down = s_down;
+    plan.int8 = int8;
+    plan.H = H;
+    plan.I = I;
+    plan.E = E;
+    plan.max_ctas = sms < kMaxCtas ? sms : kMaxCtas;
+    return cuda_status(moe::launch_decode_step(plan, s));
+  }
   cudaError_t e = moe::launch_route(logits, T, E, top_k, ids, w, I32(L.counts), offsets, sorted_token, inv_pos,
                                     active, num_active, I32(L.ctrl), kZeroWords, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  const bool int8 = wtype == MOE_W_INT8_G128;
   if (int8)  // the INT8 kernels read only the fp16 copy of the gathered rows: write it directly
     e = moe::launch_gather_f16(x, T, H, P, sorted_token, reinterpret_cast<uint16_t*>(ws + L.xg16),
                                reinterpret_cast<float*>(ws + L.xg_scale), sms, s);
@@ -353,6 +418,28 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
                              void* workspace, size_t ws_bytes, moe_stream_t stream) {
   return ffn_forward_impl(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, wtype, T, H, I, E, top_k, out,
                           workspace, ws_bytes, stream, Residual{});
+}
+
+moe_status_t moe_set_decode_step_policy(int policy) {
+  if (policy < 0 || policy > 2) return MOE_ERR_INVALID_ARG;
+  g_decode_policy.store(policy, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_test_expire_grid_barrier(int enable, uint64_t wait_ns) {
+  if (enable != 0 && enable != 1) return MOE_ERR_INVALID_ARG;
+  if (enable && (wait_ns < 1000ull || wait_ns > 2000000000ull)) return MOE_ERR_INVALID_ARG;
+  g_grid_wait_ns.store(enable ? wait_ns : 2000000000ull, std::memory_order_relaxed);
+  g_grid_extra.store(enable, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+int moe_ffn_forward_launches(int T, int H, int I, int E, int top_k, moe_wtype_t wtype) {
+  if (check_sizes(T, H, I, E, top_k, wtype) != MOE_OK) return -1;
+  if (T == 0) return 0;
+  if (use_decode_step(T, H, I, E, top_k, wtype, false)) return 1;
+  const int route = (T <= 64 && static_cast<int64_t>(T) * top_k <= 1024) ? 1 : 2;
+  return route + 1 + (wtype == MOE_W_INT8_G128 ? 3 : 2) + 1;
 }
 
 moe_status_t moe_ffn_forward_residual(const uint16_t* x, const float* logits, const void* W_gate, const void* W_up,

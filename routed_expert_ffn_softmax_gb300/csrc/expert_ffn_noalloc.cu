@@ -22,8 +22,12 @@
 //     kernels overlap on the GPU (different streams, or different host threads, on the same
 //     device) race on it and produce wrong results; serialise them.
 //   * The first call on each device looks up the array's device address
-//     (cudaGetSymbolAddress) with that device current; make that first call before any
-//     stream capture begins on the device.
+//     (cudaGetSymbolAddress) with that device current and keeps it until the process exits;
+//     make that first call before any stream capture begins on the device, and keep the
+//     device's primary context alive (no cudaDeviceReset) between calls.
+//   * A kernel that gives up on a bounded wait writes a nonzero code into the status word at
+//     the start of the array; moe_expert_ffn_noalloc_status copies it out. Every call clears
+//     it first.
 // The paper has no counterpart of this entry point: it concerns memory ownership only.
 #include <cuda_runtime.h>
 
@@ -152,4 +156,17 @@ extern "C" moe_status_t moe_expert_ffn_noalloc(const uint16_t* xg, const int32_t
   plan.status = reinterpret_cast<int32_t*>(scratch);
   plan.num_ctas = sms < kCtas ? sms : kCtas;
   return moe::launch_expert_ffn(plan, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status_t moe_expert_ffn_noalloc_status(int32_t* status_out, moe_stream_t stream) {
+  if (status_out == nullptr) return MOE_ERR_INVALID_ARG;
+  char* scratch = nullptr;
+  int sms = 0;
+  if (scratch_for_current_device(&scratch, &sms) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t word = 0;  // pageable host memory: the copy completes before cudaStreamSynchronize returns
+  if (cudaMemcpyAsync(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status_out = word;
+  return MOE_OK;
 }

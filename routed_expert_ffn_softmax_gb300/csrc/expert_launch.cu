@@ -28,8 +28,6 @@ TensorMapEncodeFn tensor_map_encoder() {
   return fn;
 }
 
-namespace {
-
 // Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = one stage's 128 bytes of
 // `box_rows` rows of one expert (64 bf16 or 128 int8 elements, one INT8 scale group), with the
 // 128-byte swizzle the MMA descriptors and the converters expect.
@@ -45,6 +43,8 @@ bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 // Token block {K (contiguous), P rows} bf16 or fp16; box = 64 elements x `box_rows` rows;
 // 128-byte swizzle.

@@ -101,6 +101,56 @@ struct GqaPlan {
 };
 cudaError_t launch_gqa_decode(const GqaPlan& plan, cudaStream_t stream);
 
+// The whole decode step (routing, gate+up, down, combine) in one cooperative persistent launch
+// (decode_step.cu), for small batches: at most kDecodeMaxT tokens and kDecodeMaxP assignments.
+constexpr int kDecodeMaxT = 32;
+constexpr int kDecodeMaxP = 256;
+struct DecodeArgs {
+  const uint16_t* x;     // [T, H] bf16
+  const float* logits;   // [T, E]
+  uint16_t* out;         // [T, H] bf16
+  uint16_t* x16;         // INT8: [T, H] fp16 copies of the token rows (scratch)
+  void* h;               // BF16: [P, I] bf16; INT8: [P, I / 128] records of 272 bytes (scratch)
+  float* Y;              // [P, H] (scratch)
+  float* partials;       // stream-K partial slots, [num CTAs][2][kPartialSlotFloats]
+  int32_t* counters;     // stream-K counters, zero on entry, left zero
+  int32_t* ccount;       // per 128-row block of H: units done, zero on entry, left zero
+  int32_t* gbar;         // grid barrier: [0] arrivals (zero on entry, left zero), [1] release word
+  int32_t* status;
+  // the grid barrier opens after gridDim.x + grid_extra arrivals (grid_extra > 0 only in the
+  // failure-detection test: it never opens, and every CTA's wait gives up after grid_wait_ns)
+  int grid_extra;
+  unsigned long long grid_wait_ns;
+  // the routing tables (written by CTA 0)
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_token;
+  int32_t* inv_pos;
+  int32_t* active;
+  int32_t* num_active;
+  int T, H, I, E, k;
+};
+struct DecodePlan {
+  DecodeArgs args;
+  const void* W_gate;
+  const void* W_up;
+  const void* W_down;
+  const float* s_gate;
+  const float* s_up;
+  const float* s_down;
+  bool int8;
+  int H, I, E;
+  int max_ctas;  // partial-slot capacity of the workspace
+};
+bool decode_step_supported(int T, int H, int I, int E, int k, bool int8);
+cudaError_t launch_decode_step(const DecodePlan& plan, cudaStream_t stream);
+
+// Weights of all experts as a 3-D tensor {K (contiguous), rows, E}; box = 128 bytes of `box_rows` rows
+// of one expert (64 bf16 or 128 int8 elements), 128-byte swizzle.
+bool encode_weights(CUtensorMap* map, const void* W, bool int8, int K, int rows, int E, int box_rows);
+
 // Resolves cuTensorMapEncodeTiled through the runtime (no link-time libcuda).
 using TensorMapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                        const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,

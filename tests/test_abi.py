@@ -47,8 +47,9 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "moe_status_string", "moe_workspace_size", "moe_route_topk", "moe_gather",
-        "moe_expert_ffn", "moe_expert_ffn_noalloc", "moe_combine", "moe_ffn_forward",
-        "moe_gqa_workspace_size", "moe_gqa_decode", "moe_expert_ffn_residual", "moe_ffn_forward_residual"])
+        "moe_expert_ffn", "moe_expert_ffn_noalloc", "moe_expert_ffn_noalloc_status", "moe_combine", "moe_ffn_forward",
+        "moe_gqa_workspace_size", "moe_gqa_decode", "moe_expert_ffn_residual", "moe_ffn_forward_residual",
+        "moe_set_decode_step_policy", "moe_ffn_forward_launches", "moe_test_expire_grid_barrier"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -199,3 +200,46 @@ def test_residual_entry_points_reject_bad_arguments(lib):
     assert f(ws=64) == WORKSPACE
     assert f(T=0, rg=None) == OK           # T = 0 is a no-op
     assert lib.moe_expert_ffn_residual(*([F] * 10), None, F, F, F, 256, 256, 8, 8, F, F, ws, None) == INVALID
+
+
+def test_decode_step_policy_and_launch_count(lib):
+    """The one-launch decode step is chosen by batch shape (P <= 2 E, T <= 32, P <= 256, H and I multiples of
+    128, INT8 of 512); the policy forces either path; host-only queries, no GPU needed."""
+    lib.moe_set_decode_step_policy.argtypes = [ctypes.c_int]
+    lib.moe_set_decode_step_policy.restype = ctypes.c_int
+    f = lib.moe_ffn_forward_launches
+    f.argtypes = [ctypes.c_int] * 6
+    f.restype = ctypes.c_int
+    try:
+        assert lib.moe_set_decode_step_policy(0) == OK
+        assert f(64, 7168, 2048, 256, 8, BF16) == 5         # staged: route, gather, gate+up, down, combine
+        assert f(512, 7168, 2048, 256, 8, BF16) == 6        # routing in two launches above 64 tokens
+        assert f(64, 4096, 1536, 128, 8, INT8) == 6         # staged INT8: + the fp16 copy of h
+        assert f(16, 4096, 14336, 8, 2, BF16) == 5          # Mixtral-8x7B, 4 tokens per expert
+        assert f(0, 256, 512, 8, 2, BF16) == 0
+        assert f(1, 256, 512, 8, 9, BF16) == -1
+        assert lib.moe_set_decode_step_policy(1) == OK
+        assert f(1, 7168, 2048, 256, 8, BF16) == 5
+        assert lib.moe_set_decode_step_policy(2) == OK
+        assert f(1, 7168, 2048, 256, 8, BF16) == 1          # DeepSeek-V3, one token
+        assert f(1, 4096, 1536, 128, 8, INT8) == 1          # Qwen3-235B INT8
+        assert f(16, 4096, 14336, 8, 2, BF16) == 1
+        assert f(1, 264, 200, 8, 2, BF16) == 5              # H, I not multiples of 128
+        assert f(4, 384, 256, 8, 2, INT8) == 6              # INT8 with H not a multiple of 512
+        assert f(33, 4096, 14336, 8, 2, BF16) == 5          # more than 32 tokens
+        assert lib.moe_set_decode_step_policy(3) == INVALID
+    finally:
+        lib.moe_set_decode_step_policy(0)
+
+
+def test_grid_barrier_test_hook_arguments(lib):
+    f = lib.moe_test_expire_grid_barrier
+    f.argtypes = [ctypes.c_int, ctypes.c_uint64]
+    f.restype = ctypes.c_int
+    try:
+        assert f(2, 10**6) == INVALID
+        assert f(1, 10) == INVALID             # below 1 us
+        assert f(1, 3 * 10**9) == INVALID      # above the normal 2 s limit
+        assert f(1, 10**6) == OK
+    finally:
+        assert f(0, 0) == OK
