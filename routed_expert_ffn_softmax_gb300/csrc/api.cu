@@ -28,7 +28,8 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 //   INT8 only: h16 [P, I] fp16, xg16 [P, H] fp16, h_scale [P], xg_scale [P] f32
 //   --- moe_ffn_forward only ---
 //   ids, w, counts, offsets, sorted_token, inv_pos, active, num_active, xg [P,H] bf16, Y [P,H] f32,
-//   INT8 only: hrec [P, I/128] records of 272 bytes (the fused decode step's fp16 h)
+//   INT8 only: hrec: the fused decode step's token records of 400 bytes (digit planes), [P, H/128] for
+//   the token rows (T <= P of them used) then [P, I/128] for h
 constexpr size_t kCtrlBytes = 4096;
 constexpr size_t kGridBarrierOffset = 8;
 constexpr size_t kCountersOffset = 256;
@@ -82,7 +83,7 @@ Layout layout(int64_t P, int H, int I, int E, bool int8) {
   L.Y = o;
   o = align_up(o + 4 * static_cast<size_t>(P) * H);
   L.hrec = o;
-  if (int8) o = align_up(o + 272 * static_cast<size_t>(P) * (I / 128));
+  if (int8) o = align_up(o + 400 * static_cast<size_t>(P) * (H / 128 + I / 128));
   L.total = o;
   return L;
 }
@@ -357,8 +358,9 @@ moe_status_t ffn_forward_impl(const uint16_t* x, const float* logits, const void
     a.x = x;
     a.logits = logits;
     a.out = out;
-    a.x16 = reinterpret_cast<uint16_t*>(ws + L.xg16);
-    a.h = int8 ? static_cast<void*>(ws + L.hrec) : static_cast<void*>(ws + L.h);
+    a.x16 = reinterpret_cast<uint16_t*>(ws + L.hrec);
+    a.h = int8 ? static_cast<void*>(ws + L.hrec + 400 * static_cast<size_t>(P) * (H / 128))
+               : static_cast<void*>(ws + L.h);
     a.Y = Y;
     a.partials = reinterpret_cast<float*>(ws + L.partials);
     a.counters = I32(L.ctrl + kCountersOffset);

@@ -49,23 +49,31 @@
 namespace moe {
 namespace dec {
 
-constexpr int kNE = 8;                                // tokens per pass of an expert
+// Tokens per pass of an expert: a template parameter of the kernel (1, 4 or 8, chosen per launch);
+// the slots and shared arrays are sized for the largest.
+constexpr int kMaxNEAll = 8;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = 32 * kComputeWarps;  // 128 rows x 4 quarters
 constexpr int kProducerWarp = kComputeWarps;
 constexpr int kThreads = kComputeThreads + 32;
-constexpr int kRec = 272;  // INT8 h record: 128 fp16 values, the fp32 group scale, padding to 16 B
+// INT8 token record of one 128-element group (x for gate+up, h for down): the group's values as 24-bit
+// fixed-point integers X = round(v * 2^-e), e chosen so that the group's largest |v| * 2^-e lies in
+// [2^22, 2^23), split into three int8 digit planes of 128 bytes (X = d2 * 2^16 + d1 * 2^8 + d0, d0 and d1
+// unsigned, d2 signed), then the fp32 2^e and padding to 16 bytes.
+constexpr int kRec = 400;
+constexpr int kRecScale = 384;
 
 template <bool kInt8>
 struct Geo {
+  static constexpr int kMaxNE = kInt8 ? 4 : 8;          // tokens per pass at most
   static constexpr int kKt = kInt8 ? 128 : 64;          // reduction elements per 128-byte tile row
   static constexpr int kWBytes = 32768;                 // two 128-row x 128-byte weight boxes
   static constexpr int kScaleBytes = kInt8 ? 4096 : 0;  // INT8: two {4 groups x 128 rows} fp32 boxes
-  static constexpr int kSliceGU = kInt8 ? 256 : 128;    // token bytes per slot, gate+up (x)
+  static constexpr int kSliceGU = kInt8 ? kRec : 128;   // token bytes per slot, gate+up (x)
   static constexpr int kSliceDN = kInt8 ? 2 * kRec : 256;  // and down (h: two reduction slices)
   static constexpr int kSliceMax = kSliceGU > kSliceDN ? kSliceGU : kSliceDN;
   static constexpr int kTokOff = kWBytes + kScaleBytes;
-  static constexpr int kSlot = (kTokOff + kNE * kSliceMax + 1023) / 1024 * 1024;
+  static constexpr int kSlot = (kTokOff + kMaxNE * kSliceMax + 1023) / 1024 * 1024;
   static constexpr int kStages = kInt8 ? 5 : 6;
   static_assert(kSlot % 1024 == 0, "slots keep the 1024-byte alignment of the 128B swizzle");
 };
@@ -76,7 +84,6 @@ struct Shared {
   uint64_t gbar_arrived;  // compute -> producer: this CTA has arrived at the grid barrier
   int gbar_epoch;         // the barrier's release word as read before arriving
   int flag;               // broadcast word of the epilogues
-  float xs[kDecodeMaxT];  // INT8: the power of two each token's fp16 copy was divided by
   uint32_t need;          // INT8: tokens this CTA converts (bit t)
   int A;                  // active experts
   int ids[kDecodeMaxP];   // token t's experts at t * k .. t * k + k - 1 (slot order)
@@ -90,7 +97,9 @@ struct Shared {
   uint32_t tokmask[256];
   int act_e[256];
   int pp[257];            // prefix sums of the passes of the active experts
-  float red[2][kComputeWarps][kNE];
+  int qc[kDecodeMaxP];    // cost of one tile of pass q (tile_cost of its tokens)
+  int pc[kDecodeMaxP + 1];  // prefix sums of qc
+  float red[2][kComputeWarps][kMaxNEAll];
 };
 
 template <bool kInt8>
@@ -99,12 +108,24 @@ constexpr int smem_bytes() {
 }
 static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "dynamic shared memory per CTA");
 
+// Stream-K by cost: a tile of a pass with n tokens costs max(kCostMem, kCostBase + kCostTok * n), its
+// HBM time or its compute warps' time, whichever is longer (the compute grows with the tokens: on GB300
+// a BF16 tile is bound by HBM up to about two tokens, an INT8 tile up to about one), so CTAs whose
+// tiles carry more tokens get fewer tiles.
+constexpr int kCostMem = 10;
+constexpr int kCostBase = 4;
+template <bool kInt8>
+__host__ __device__ constexpr int tile_cost(int n) {
+  return kCostBase + (kInt8 ? 5 : 3) * n > kCostMem ? kCostBase + (kInt8 ? 5 : 3) * n : kCostMem;
+}
+
 // One unit: pass `np` of the a-th active expert (tokens at sorted positions p0 .. p0 + n - 1) and a
 // 128-row block of the output rows.
 struct Unit {
   int e, p0, n, rb;
 };
 
+template <int kNE>
 __device__ __forceinline__ Unit unit_of(const Shared& S, int q, int rb) {
   int lo = 0, hi = S.A - 1;
   while (lo < hi) {
@@ -158,7 +179,53 @@ __device__ __forceinline__ int f16_exponent(float m) {
   return k;
 }
 
-template <bool kInt8>
+// e with max * 2^-e in [2^22, 2^23) (the 24-bit fixed point of an INT8 token record), kept where 2^e
+// and the conversions stay finite in fp32; 0 for an all-zero or non-finite group.
+__device__ __forceinline__ int fixed_exponent(float m) {
+  int k = 0;
+  if (m > 0.0f && m <= 3.0e38f) {
+    int e = 0;
+    frexpf(m, &e);  // m = f * 2^e, 0.5 <= f < 1
+    k = e - 23;
+    k = k < -140 ? -140 : k;
+  }
+  return k;
+}
+
+// The three digit bytes of round(v * 2^-e) (|.| < 2^23): d0 = bits 0..7, d1 = bits 8..15 (unsigned),
+// d2 = bits 16..23 with the sign (an arithmetic shift).
+__device__ __forceinline__ int fixed_value(float v, int e) { return __float2int_rn(ldexpf(v, -e)); }
+
+// dp4a of four unsigned digit bytes (a) with four signed weights (b), or of signed bytes with signed.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Sum over one 16-byte chunk pair of a token record's planes: sum_k X_k * q_k for the 32 elements whose
+// weights are in w[0..7] (chunk ca, then chunk cb) and whose digits are at chunk offsets ca and cb of
+// the record at `rec` (a shared-memory address). Exact in int32 per plane; returned as fp32.
+__device__ __forceinline__ float record_dot(uint32_t rec, int ca, int cb, const uint32_t (&w)[8]) {
+  int s[3];
+#pragma unroll
+  for (int p = 0; p < 3; ++p) {
+    const uint4 xa = lds128(rec + p * 128 + ca * 16), xb = lds128(rec + p * 128 + cb * 16);
+    const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    int acc = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc = p == 2 ? dp4a_ss(xw[j], w[j], acc) : dp4a_us(xw[j], w[j], acc);
+    s[p] = acc;
+  }
+  return fmaf(static_cast<float>(s[2]), 65536.0f, fmaf(static_cast<float>(s[1]), 256.0f, static_cast<float>(s[0])));
+}
+
+template <bool kInt8, int kNE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_step_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmU,
                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSG,
@@ -196,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warm the logits in L2 (a line still being written by the predecessor is updated there)
   for (int i = tid; i * 32 < T * E; i += kThreads)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(a.logits + i * 32));
+  prefetch_l2_grid(a.x, static_cast<int64_t>(T) * H * 2);  // the token rows, spread over the grid
   for (int i = tid; i < 256; i += kThreads) {
     S.cnt[i] = 0;
     S.tokmask[i] = 0u;
@@ -223,16 +291,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicOr(&S.tokmask[e], 1u << (i / k));
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive offsets, active list and pass counts, 32 experts at a time
-    int run = 0, nact = 0;
+  if (warp == 0) {  // exclusive offsets, active list and the prefix of pass counts, 32 experts at a time
+    int run = 0, nact = 0, prun = 0;
     for (int b = 0; b < E; b += 32) {
       const int e = b + lane;
       const int c = e < E ? S.cnt[e] : 0;
-      int incl = c;
+      const int pc = (c + kNE - 1) / kNE;
+      int incl = c, pin = pc;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+        const int m = __shfl_up_sync(0xffffffffu, pin, o);
+        if (lane >= o) {
+          incl += n;
+          pin += m;
+        }
       }
       const uint32_t act = __ballot_sync(0xffffffffu, c > 0);
       if (e < E) {
@@ -240,17 +313,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c > 0) {
           const int ai = nact + __popc(act & ((1u << lane) - 1u));
           S.act_e[ai] = e;
-          S.pp[ai + 1] = (c + kNE - 1) / kNE;
+          S.pp[ai + 1] = prun + pin;
         }
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
+      prun += __shfl_sync(0xffffffffu, pin, 31);
       nact += __popc(act);
     }
     if (lane == 0) {
       S.off[E] = run;
       S.A = nact;
       S.pp[0] = 0;
-      for (int i = 1; i <= nact; ++i) S.pp[i] += S.pp[i - 1];
     }
   }
   __syncthreads();
@@ -283,28 +356,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ============================ schedule ============================
+  for (int q = tid; q < NU; q += kThreads) S.qc[q] = tile_cost<kInt8>(unit_of<kNE>(S, q, 0).n);
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix of the pass costs, eight passes per lane
+    int v[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = lane * 8 + j;
+      v[j] = q < NU ? S.qc[q] : 0;
+      sum += v[j];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = lane * 8 + j;
+      if (q <= NU) S.pc[q] = run;
+      run += v[j];
+    }
+  }
+  __syncthreads();
   const int RBg = I / 128, KIg = H / G::kKt;        // gate+up: rows of I, reduction H
   const int RBd = H / 128, KId = I / (2 * G::kKt);  // down: rows of H, reduction I (two slices per slot)
-  const int64_t Wg = static_cast<int64_t>(NU) * RBg * KIg;
+  const int64_t TPg = static_cast<int64_t>(RBg) * KIg;  // gate+up tiles of one pass
+  const int64_t Wg = static_cast<int64_t>(NU) * TPg;
   const int64_t Wd = static_cast<int64_t>(NU) * RBd * KId;
-  const int64_t NCg = Wg < N ? Wg : N, NCd = Wd < N ? Wd : N;
-  const int64_t g_beg = cta < NCg ? cta * Wg / NCg : 0, g_end = cta < NCg ? (cta + 1) * Wg / NCg : 0;
-  const int64_t d_beg = cta < NCd ? cta * Wd / NCd : 0, d_end = cta < NCd ? (cta + 1) * Wd / NCd : 0;
+  const int64_t PC = S.pc[NU];
+  const int64_t Cg = PC * TPg, Rd = PC * KId, Cd = Rd * RBd;  // total costs; Rd: one row block of down
+  // CTAs taking part: each range is at least one tile's cost wide, so every one holds a tile
+  constexpr int kMaxCost = tile_cost<kInt8>(kNE);
+  const int64_t Ng = Cg / kMaxCost < N ? (Cg / kMaxCost > 0 ? Cg / kMaxCost : 1) : N;
+  const int64_t Nd = Cd / kMaxCost < N ? (Cd / kMaxCost > 0 ? Cd / kMaxCost : 1) : N;
+  auto pass_at = [&](int64_t X) -> int {  // the last pass q with pc[q] <= X
+    int lo = 0, hi = NU - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (S.pc[mid] <= X) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  // cost position of a tile, and the first tile at or past a cost position (gate+up: tiles of pass
+  // q at q * TPg .., each costing qc[q]; down: row block rb, then pass q, KId tiles each)
+  auto pos_gu = [&](int64_t i) -> int64_t {
+    const int q = static_cast<int>(i / TPg);
+    return S.pc[q] * TPg + (i - q * TPg) * S.qc[q];
+  };
+  auto first_gu = [&](int64_t X) -> int64_t {
+    if (X >= Cg) return Wg;
+    const int q = pass_at(X / TPg);
+    const int64_t base = S.pc[q] * TPg;
+    return q * TPg + (X - base + S.qc[q] - 1) / S.qc[q];
+  };
+  auto pos_dn = [&](int64_t i) -> int64_t {
+    const int64_t u = i / KId;
+    const int64_t rb = u / NU;
+    const int q = static_cast<int>(u - rb * NU);
+    return rb * Rd + static_cast<int64_t>(S.pc[q]) * KId + (i - u * KId) * S.qc[q];
+  };
+  auto first_dn = [&](int64_t X) -> int64_t {
+    if (X >= Cd) return Wd;
+    const int64_t rb = X / Rd, rem = X - rb * Rd;
+    const int q = pass_at(rem / KId);
+    const int64_t base = static_cast<int64_t>(S.pc[q]) * KId;
+    return (rb * NU + q) * KId + (rem - base + S.qc[q] - 1) / S.qc[q];
+  };
+  const int64_t g_beg = cta < Ng ? first_gu(cta * Cg / Ng) : Wg, g_end = cta < Ng ? first_gu((cta + 1) * Cg / Ng) : Wg;
+  const int64_t d_beg = cta < Nd ? first_dn(cta * Cd / Nd) : Wd, d_end = cta < Nd ? first_dn((cta + 1) * Cd / Nd) : Wd;
   // gate+up units are pass-major (q * RBg + rb): a CTA's range touches few experts' tokens;
   // down units are row-block-major (rb * NU + q): a row block's combine becomes ready as soon as
   // its last unit is done, spread over the step instead of all at its end.
-  auto gu_unit = [&](int64_t u) { return unit_of(S, static_cast<int>(u / RBg), static_cast<int>(u % RBg)); };
-  auto dn_unit = [&](int64_t u) { return unit_of(S, static_cast<int>(u % NU), static_cast<int>(u / NU)); };
+  auto gu_unit = [&](int64_t u) { return unit_of<kNE>(S, static_cast<int>(u / RBg), static_cast<int>(u % RBg)); };
+  auto dn_unit = [&](int64_t u) { return unit_of<kNE>(S, static_cast<int>(u % NU), static_cast<int>(u / NU)); };
 
-  // INT8: fp16 copies of the token rows this CTA's gate+up tiles read, each divided by a power of
-  // two that brings its largest value into [2^14, 2^15). CTAs that share a token write the same
-  // bytes; each CTA reads only rows it has written itself.
+  // INT8: records (the digit planes above) of the token rows this CTA's gate+up tiles read, one per
+  // 128-element scale group, the same layout as h's. CTAs that share a token write the same bytes;
+  // each CTA reads only records it has written itself.
   if (kInt8) {
     if (tid == 0) {
       uint32_t need = 0u;
       if (g_beg < g_end) {
         const int q0 = static_cast<int>((g_beg / KIg) / RBg), q1 = static_cast<int>(((g_end - 1) / KIg) / RBg);
-        const Unit u0 = unit_of(S, q0, 0), u1 = unit_of(S, q1, 0);
+        const Unit u0 = unit_of<kNE>(S, q0, 0), u1 = unit_of<kNE>(S, q1, 0);
         for (int p = u0.p0; p < u1.p0 + u1.n; ++p) need |= 1u << S.sorted[p];
       }
       S.need = need;
@@ -312,48 +449,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp < kComputeWarps) {
       const uint32_t need = S.need;
-      const int nn = __popc(need);
-      for (int j = warp; j < nn; j += kComputeWarps) {
+      const int ng = H / 128;
+      const int nrec = __popc(need) * ng;
+      for (int w = warp; w < nrec; w += kComputeWarps) {  // a warp per (token, group) record
+        const int j = w / ng, g = w - j * ng;
         uint32_t m = need;
         for (int z = 0; z < j; ++z) m &= m - 1u;
         const int t = __ffs(m) - 1;
-        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * H);
-        float mx = 0.0f;
-        for (int c = lane; c < H / 8; c += 32) {
-          const uint4 v = src[c];
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        const uint2 v = *reinterpret_cast<const uint2*>(a.x + static_cast<int64_t>(t) * H + g * 128 + lane * 4);
+        const float f0 = __uint_as_float(v.x << 16), f1 = __uint_as_float(v.x & 0xffff0000u);
+        const float f2 = __uint_as_float(v.y << 16), f3 = __uint_as_float(v.y & 0xffff0000u);
+        const float mx = warp_max_abs(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+        const int kx = fixed_exponent(mx);
+        const int X0 = fixed_value(f0, kx), X1 = fixed_value(f1, kx), X2 = fixed_value(f2, kx), X3 = fixed_value(f3, kx);
+        uint8_t* rec = reinterpret_cast<uint8_t*>(a.x16) + (static_cast<int64_t>(t) * ng + g) * kRec;
+        // plane p, elements 4 lane .. 4 lane + 3: bytes of (X >> 8 p)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            mx = fmaxf(mx, fabsf(__uint_as_float(wv[i] << 16)));
-            mx = fmaxf(mx, fabsf(__uint_as_float(wv[i] & 0xffff0000u)));
-          }
+        for (int p = 0; p < 3; ++p) {
+          const uint32_t word = ((X0 >> (8 * p)) & 0xff) | (((X1 >> (8 * p)) & 0xff) << 8) |
+                                (((X2 >> (8 * p)) & 0xff) << 16) | (static_cast<uint32_t>((X3 >> (8 * p)) & 0xff) << 24);
+          *reinterpret_cast<uint32_t*>(rec + p * 128 + lane * 4) = word;
         }
-        mx = warp_max_abs(mx);
-        const int kx = f16_exponent(mx);
-        const float down = ldexpf(1.0f, -kx);
-        uint4* dst = reinterpret_cast<uint4*>(a.x16 + static_cast<int64_t>(t) * H);
-        for (int c = lane; c < H / 8; c += 32) {
-          const uint4 v = src[c];
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __half2 h2 = __floats2half2_rn(__uint_as_float(wv[i] << 16) * down,
-                                                 __uint_as_float(wv[i] & 0xffff0000u) * down);
-            o[i] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (lane == 0) S.xs[t] = ldexpf(1.0f, kx);
+        if (lane == 0) *reinterpret_cast<float*>(rec + kRecScale) = ldexpf(1.0f, kx);
       }
-      fence_proxy_async_global();  // the producer's bulk copies of these rows come after the barrier
+      fence_proxy_async_global();  // the producer's bulk copies of these records come after the barrier
+      named_bar_sync(1, kThreads);
     }
-    named_bar_sync(1, kThreads);
   }
 
   if (warp == kProducerWarp) {
     // ================================ producer ================================
-    if (lane == 0) {
+    // Lane 0 issues everything; the warp's other lanes only take part in barrier 1 (INT8).
+    {
       const uint64_t pol = l2_policy_evict_first();
       uint8_t* const slots = smem;
       int slot = 0;
@@ -367,50 +494,115 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph ^= 1u;
         }
       };
-      // ---- gate+up tiles
-      for (int64_t i = g_beg; i < g_end && ok; ++i) {
-        const int64_t u = i / KIg;
-        const int kk = static_cast<int>(i - u * KIg);
-        const Unit un = gu_unit(u);
+      // The tiles are stepped through with cursors: one division and one unit lookup per range (and a
+      // lookup per unit), none per tile. The single issuing thread shares the SM's issue slots with
+      // sixteen compute warps, and per-tile arithmetic on its path held back every copy behind it.
+      // ---- gate+up tiles (pass-major units q * RBg + rb, KIg reduction slices each)
+      // The first ring's weight tiles go out at once; their token slices follow when the token rows
+      // are ready (INT8: the compute warps' fp16 copies, signalled by barrier 1).
+      struct GuCursor {
+        int kk, q, rb;
+        Unit un;
+      };
+      GuCursor cur{};
+      // token t's row: bf16 x, or its INT8 records (H / 128 of kRec bytes)
+      const uint8_t* xrow[kNE];
+      const int64_t xrow_bytes = kInt8 ? static_cast<int64_t>(H / 128) * kRec : static_cast<int64_t>(H) * 2;
+      const uint8_t* const xbase = kInt8 ? reinterpret_cast<const uint8_t*>(a.x16) : reinterpret_cast<const uint8_t*>(a.x);
+      auto rows_of = [&](const Unit& un) {
+#pragma unroll
+        for (int t = 0; t < kNE; ++t) xrow[t] = xbase + S.sorted[un.p0 + (t < un.n ? t : 0)] * xrow_bytes;
+      };
+      auto step = [&](GuCursor& c, int64_t i) {  // to tile i + 1
+        if (++c.kk == KIg) {
+          c.kk = 0;
+          if (++c.rb == RBg) {
+            c.rb = 0;
+            ++c.q;
+          }
+          if (i + 1 < g_end) c.un = unit_of<kNE>(S, c.q, c.rb);
+        }
+      };
+      auto weights_gu = [&](int sl, const GuCursor& c) {
+        uint8_t* st = slots + sl * G::kSlot;
+        mbar_arrive_expect_tx(&S.full[sl], G::kWBytes + G::kScaleBytes + c.un.n * G::kSliceGU);
+        tma_load_3d(st, &tmG, &S.full[sl], c.kk * G::kKt, c.un.rb * 128, c.un.e, pol);
+        tma_load_3d(st + 16384, &tmU, &S.full[sl], c.kk * G::kKt, c.un.rb * 128, c.un.e, pol);
+        if (kInt8) {
+          tma_load_3d_plain(st + G::kWBytes, &tmSG, &S.full[sl], c.kk & ~3, c.un.rb * 128, c.un.e);
+          tma_load_3d_plain(st + G::kWBytes + 2048, &tmSU, &S.full[sl], c.kk & ~3, c.un.rb * 128, c.un.e);
+        }
+      };
+      auto tokens_gu = [&](int sl, const GuCursor& c) {
+        uint8_t* st = slots + sl * G::kSlot;
+#pragma unroll
+        for (int t = 0; t < kNE; ++t)
+          if (t < c.un.n)
+            bulk_g2s(st + G::kTokOff + t * G::kSliceGU, xrow[t] + c.kk * G::kSliceGU, G::kSliceGU, &S.full[sl]);
+      };
+      const int64_t npre = (g_end - g_beg) < G::kStages ? (g_end - g_beg) : G::kStages;
+      if (g_beg < g_end) {
+        const int64_t u0 = g_beg / KIg;
+        cur.kk = static_cast<int>(g_beg - u0 * KIg);
+        cur.q = static_cast<int>(u0 / RBg);
+        cur.rb = static_cast<int>(u0 - static_cast<int64_t>(cur.q) * RBg);
+        cur.un = unit_of<kNE>(S, cur.q, cur.rb);
+      }
+      const GuCursor first = cur;
+      if (lane == 0) {
+        rows_of(cur.un);
+        for (int64_t j = 0; j < npre; ++j) {  // a fresh ring: no slot to wait for
+          weights_gu(static_cast<int>(j), cur);
+          if (!kInt8) tokens_gu(static_cast<int>(j), cur);  // BF16 reads x itself: each slot whole, in order
+          const int q0 = cur.q, rb0 = cur.rb;
+          step(cur, g_beg + j);
+          if (!kInt8 && (cur.q != q0 || cur.rb != rb0)) rows_of(cur.un);
+        }
+      }
+      __syncwarp();
+      if (kInt8) named_bar_sync(1, kThreads);
+      if (lane == 0) {
+      if (kInt8) {  // the records are written: the first ring's token slices
+        GuCursor c = first;
+        rows_of(c.un);
+        for (int64_t j = 0; j < npre; ++j) {
+          tokens_gu(static_cast<int>(j), c);
+          const int q0 = c.q, rb0 = c.rb;
+          step(c, g_beg + j);
+          if (c.q != q0 || c.rb != rb0) rows_of(c.un);
+        }
+        rows_of(cur.un);
+      }
+      for (int64_t j = 0; j < npre; ++j) advance();
+      for (int64_t i = g_beg + npre; i < g_end && ok; ++i) {
         if (!mbar_wait(&S.empty[slot], ph ^ 1u)) {
           ok = false;
           atomicExch(a.status, kStatusWaitEmptyTimeout);
           break;
         }
-        uint8_t* st = slots + slot * G::kSlot;
-        mbar_arrive_expect_tx(&S.full[slot], G::kWBytes + G::kScaleBytes + un.n * G::kSliceGU);
-        tma_load_3d(st, &tmG, &S.full[slot], kk * G::kKt, un.rb * 128, un.e, pol);
-        tma_load_3d(st + 16384, &tmU, &S.full[slot], kk * G::kKt, un.rb * 128, un.e, pol);
-        if (kInt8) {
-          tma_load_3d_plain(st + G::kWBytes, &tmSG, &S.full[slot], kk & ~3, un.rb * 128, un.e);
-          tma_load_3d_plain(st + G::kWBytes + 2048, &tmSU, &S.full[slot], kk & ~3, un.rb * 128, un.e);
-        }
-        for (int t = 0; t < un.n; ++t) {
-          const int tok = S.sorted[un.p0 + t];
-          const uint16_t* src = (kInt8 ? a.x16 : a.x) + static_cast<int64_t>(tok) * H + kk * G::kKt;
-          bulk_g2s(st + G::kTokOff + t * G::kSliceGU, src, G::kSliceGU, &S.full[slot]);
-        }
+        weights_gu(slot, cur);
+        tokens_gu(slot, cur);
         advance();
+        const int q0 = cur.q, rb0 = cur.rb;
+        step(cur, i);
+        if (cur.q != q0 || cur.rb != rb0) rows_of(cur.un);
       }
-      // ---- down tiles: weights as slots free up; the h slices once the grid barrier is passed
+      // ---- down tiles (row-block-major units rb * NU + q, KId slots of two reduction slices each):
+      // weights as slots free up; the h slices of a slot once the grid barrier is passed
       int pend_slot[8];
-      int64_t pend_i[8];
+      int pend_kk2[8];
+      const uint8_t* pend_src[8];
+      int pend_n[8];
       int npend = 0;
       bool passed = false;
-      auto issue_h = [&](int sl, int64_t i) {
-        const int64_t u = i / KId;
-        const int kk2 = static_cast<int>(i - u * KId);
-        const Unit un = dn_unit(u);
+      auto issue_h = [&](int sl, const uint8_t* src, int n, int kk2) {
         uint8_t* st = slots + sl * G::kSlot;
-        for (int t = 0; t < un.n; ++t) {
-          const int p = un.p0 + t;
-          const void* src;
-          if (kInt8)
-            src = static_cast<const uint8_t*>(a.h) + (static_cast<int64_t>(p) * (I / 128) + 2 * kk2) * kRec;
-          else
-            src = static_cast<const uint16_t*>(a.h) + static_cast<int64_t>(p) * I + kk2 * 128;
-          bulk_g2s(st + G::kTokOff + t * G::kSliceDN, src, G::kSliceDN, &S.full[sl]);
-        }
+        // h rows of the unit's tokens are consecutive (sorted positions p0 ..): I * 2 bytes apart in
+        // bf16, I / 128 records apart for INT8
+        const int64_t row_bytes = kInt8 ? static_cast<int64_t>(I / 128) * kRec : static_cast<int64_t>(I) * 2;
+        const int64_t off = kInt8 ? static_cast<int64_t>(2 * kk2) * kRec : static_cast<int64_t>(kk2) * 256;
+        for (int t = 0; t < n; ++t)
+          bulk_g2s(st + G::kTokOff + t * G::kSliceDN, src + t * row_bytes + off, G::kSliceDN, &S.full[sl]);
       };
       // the grid barrier has been passed: every CTA's h is written (acquire, then order the async
       // proxy's later reads after it)
@@ -421,12 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto release_pending = [&]() {
         fence_proxy_async_global();
         passed = true;
-        for (int j = 0; j < npend; ++j) issue_h(pend_slot[j], pend_i[j]);
+        for (int j = 0; j < npend; ++j) issue_h(pend_slot[j], pend_src[j], pend_n[j], pend_kk2[j]);
         npend = 0;
       };
       // wait for a free slot, issuing the pending h slices as soon as the barrier opens (the slots
       // they complete are the ones the compute warps wait for)
       auto wait_slot = [&]() -> bool {
+        if (mbar_try_wait(&S.empty[slot], ph ^ 1u)) return true;
         const uint64_t t0 = global_timer_ns();
         uint64_t tb = t0;
         for (;;) {
@@ -447,28 +640,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((passed || npend == 0) && global_timer_ns() - t0 > 2 * kWaitLimitNs) return false;
         }
       };
-      for (int64_t i = d_beg; i < d_end && ok; ++i) {
-        if (!wait_slot()) {
-          ok = false;
-          atomicExch(a.status, kStatusWaitEmptyTimeout);
-          break;
+      if (d_beg < d_end && ok) {
+        const int64_t u0 = d_beg / KId;
+        int kk2 = static_cast<int>(d_beg - u0 * KId);
+        int rb = static_cast<int>(u0 / NU), q = static_cast<int>(u0 - static_cast<int64_t>(rb) * NU);
+        Unit un = unit_of<kNE>(S, q, rb);
+        auto h_of = [&]() -> const uint8_t* {
+          return kInt8 ? static_cast<const uint8_t*>(a.h) + static_cast<int64_t>(un.p0) * (I / 128) * kRec
+                       : static_cast<const uint8_t*>(a.h) + static_cast<int64_t>(un.p0) * I * 2;
+        };
+        const uint8_t* hsrc = h_of();
+        for (int64_t i = d_beg; i < d_end; ++i) {
+          if (!wait_slot()) {
+            ok = false;
+            atomicExch(a.status, kStatusWaitEmptyTimeout);
+            break;
+          }
+          uint8_t* st = slots + slot * G::kSlot;
+          mbar_arrive_expect_tx(&S.full[slot], G::kWBytes + (kInt8 ? 2048 : 0) + un.n * G::kSliceDN);
+          tma_load_3d(st, &tmD, &S.full[slot], 2 * kk2 * G::kKt, un.rb * 128, un.e, pol);
+          tma_load_3d(st + 16384, &tmD, &S.full[slot], (2 * kk2 + 1) * G::kKt, un.rb * 128, un.e, pol);
+          if (kInt8) tma_load_3d_plain(st + G::kWBytes, &tmSD, &S.full[slot], (2 * kk2) & ~3, un.rb * 128, un.e);
+          if (passed) {
+            issue_h(slot, hsrc, un.n, kk2);
+          } else {
+            pend_slot[npend] = slot;
+            pend_src[npend] = hsrc;
+            pend_n[npend] = un.n;
+            pend_kk2[npend] = kk2;
+            ++npend;
+          }
+          advance();
+          if (++kk2 == KId) {
+            kk2 = 0;
+            if (++q == NU) {
+              q = 0;
+              ++rb;
+            }
+            if (i + 1 < d_end) {
+              un = unit_of<kNE>(S, q, rb);
+              hsrc = h_of();
+            }
+          }
         }
-        const int64_t u = i / KId;
-        const int kk2 = static_cast<int>(i - u * KId);
-        const Unit un = dn_unit(u);
-        uint8_t* st = slots + slot * G::kSlot;
-        mbar_arrive_expect_tx(&S.full[slot], G::kWBytes + (kInt8 ? 2048 : 0) + un.n * G::kSliceDN);
-        tma_load_3d(st, &tmD, &S.full[slot], 2 * kk2 * G::kKt, un.rb * 128, un.e, pol);
-        tma_load_3d(st + 16384, &tmD, &S.full[slot], (2 * kk2 + 1) * G::kKt, un.rb * 128, un.e, pol);
-        if (kInt8) tma_load_3d_plain(st + G::kWBytes, &tmSD, &S.full[slot], (2 * kk2) & ~3, un.rb * 128, un.e);
-        if (passed) {
-          issue_h(slot, i);
-        } else {
-          pend_slot[npend] = slot;
-          pend_i[npend] = i;
-          ++npend;
-        }
-        advance();
       }
       if (!passed && npend > 0) {
         const uint64_t t0 = global_timer_ns();
@@ -494,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
+      }  // lane 0
     }
     __syncwarp();
   } else {
@@ -521,15 +736,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ph ^= 1u;
       }
     };
-    auto cta_of = [](int64_t i, int64_t W, int64_t NC) -> int64_t { return ((i + 1) * NC - 1) / W; };
 
     // Split-unit hand-off: publish this CTA's partial sums (vals[t][m], m < kM) and let the last of
     // the unit's CTAs sum all pieces in CTA order. Returns true in the CTA that must finish the unit
     // (vals then holds the full sums in its quarter-0 threads).
-    auto split_unit = [&](auto& vals, auto kMc, int64_t ub, int64_t ue, int64_t beg, int64_t W, int64_t NC,
-                          int64_t KI) -> bool {
+    // pos / first: the phase's cost position of a tile and first tile at a cost position; Nc, Ct: the
+    // CTAs taking part and the total cost (the CTA of a tile: the last c with c * Ct / Nc <= pos).
+    auto split_unit = [&](auto& vals, auto kMc, int64_t ub, int64_t ue, int64_t beg, int64_t KI, auto pos,
+                          auto first, int64_t Nc, int64_t Ct) -> bool {
       constexpr int kM = decltype(kMc)::value;
-      const int64_t c_first = cta_of(ub, W, NC), c_last = cta_of(ue - 1, W, NC);
+      auto cta_of = [&](int64_t i) -> int64_t { return ((pos(i) + 1) * Nc - 1) / Ct; };
+      const int64_t c_first = cta_of(ub), c_last = cta_of(ue - 1);
       const int sl = (ub / KI == beg / KI) ? 0 : 1;
       float* mine = a.partials + (static_cast<int64_t>(cta) * 2 + sl) * kPartialSlotFloats;
       if (q == 0) {
@@ -558,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int m = 0; m < kM; ++m) vals[t][m] = 0.0f;
         for (int64_t c = c_first; c <= c_last; ++c) {
-          const int cs = (ub / KI == (c * W / NC) / KI) ? 0 : 1;
+          const int cs = (ub / KI == first(c * Ct / Nc) / KI) ? 0 : 1;
           const float* src = a.partials + (c * 2 + cs) * kPartialSlotFloats;
 #pragma unroll
           for (int t = 0; t < kNE; ++t)
@@ -581,10 +798,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; i < pe; ++i) {
         const uint32_t st = take();
         const uint32_t rowg = st + r * 128, rowu = rowg + 16384;
-        const uint32_t c0 = ((2 * q) ^ x7) << 4, c1 = ((2 * q + 1) ^ x7) << 4;
-        const uint4 g0 = lds128(rowg + c0), g1 = lds128(rowg + c1);
-        const uint4 u0 = lds128(rowu + c0), u1 = lds128(rowu + c1);
         if constexpr (!kInt8) {
+          const uint32_t c0 = ((2 * q) ^ x7) << 4, c1 = ((2 * q + 1) ^ x7) << 4;
+          const uint4 g0 = lds128(rowg + c0), g1 = lds128(rowg + c1);
+          const uint4 u0 = lds128(rowu + c0), u1 = lds128(rowu + c1);
           const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
           const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
           const uint32_t tb = st + G::kTokOff + q * 32;
@@ -606,36 +823,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
+          // chunks 2q and 2q + 1 (int8 elements 32q .. 32q + 31) of the group: the weights as they are,
+          // against the token record's digit planes (dp4a); quarters 2 and 3 take the two chunks in the
+          // other order so that, in every load, the four quarters' digit reads fall in distinct banks
+          const int ca = 2 * q + (q >> 1), cb = 2 * q + 1 - (q >> 1);
+          const uint32_t c0 = (ca ^ x7) << 4, c1 = (cb ^ x7) << 4;
+          const uint4 g0 = lds128(rowg + c0), g1 = lds128(rowg + c1);
+          const uint4 u0 = lds128(rowu + c0), u1 = lds128(rowu + c1);
           const uint32_t gq[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
           const uint32_t uq[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-          uint32_t gh[16], uh[16];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            int8x4_to_f16x2x2(gq[j], gh[2 * j], gh[2 * j + 1]);
-            int8x4_to_f16x2x2(uq[j], uh[2 * j], uh[2 * j + 1]);
-          }
           const int kk = static_cast<int>(i - ub);
           const float sg = lds_f32(st + G::kWBytes + r * 16 + (kk & 3) * 4);
           const float su = lds_f32(st + G::kWBytes + 2048 + r * 16 + (kk & 3) * 4);
-          const uint32_t tb = st + G::kTokOff + q * 64;
 #pragma unroll
           for (int t = 0; t < kNE; ++t) {
             if (t < un.n) {
-              float ga = 0.0f, gb = 0.0f, ua = 0.0f, ubb = 0.0f;
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const uint4 xv = lds128(tb + t * G::kSliceGU + h * 16);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                for (int j = 0; j < 4; j += 2) {
-                  ga = fma2_f16(gh[4 * h + j], xw[j], ga);
-                  gb = fma2_f16(gh[4 * h + j + 1], xw[j + 1], gb);
-                  ua = fma2_f16(uh[4 * h + j], xw[j], ua);
-                  ubb = fma2_f16(uh[4 * h + j + 1], xw[j + 1], ubb);
-                }
-              }
-              acc[t][0] = fmaf(ga + gb, sg, acc[t][0]);
-              acc[t][1] = fmaf(ua + ubb, su, acc[t][1]);
+              const uint32_t rec = st + G::kTokOff + t * G::kSliceGU;
+              const float xsc = lds_f32(rec + kRecScale);  // the record's 2^e
+              acc[t][0] = fmaf(record_dot(rec, ca, cb, gq), sg * xsc, acc[t][0]);
+              acc[t][1] = fmaf(record_dot(rec, ca, cb, uq), su * xsc, acc[t][1]);
             }
           }
         }
@@ -650,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[t][m] += __shfl_xor_sync(0xffffffffu, acc[t][m], 2);
         }
       bool finish = true;
-      if (!(ub >= g_beg && ue <= g_end)) finish = split_unit(acc, std::integral_constant<int, 2>{}, ub, ue, g_beg, Wg, NCg, KIg);
+      if (!(ub >= g_beg && ue <= g_end)) finish = split_unit(acc, std::integral_constant<int, 2>{}, ub, ue, g_beg, KIg, pos_gu, first_gu, Ng, Cg);
       if (finish) {
         const int i_row = un.rb * 128 + r;
         if constexpr (!kInt8) {
@@ -662,15 +868,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 h[static_cast<int64_t>(un.p0 + t) * I + i_row] = __float2bfloat16_rn(silu_mul(acc[t][0], acc[t][1]));
           }
         } else {
-          // h rounded to bf16, then its fp16 record: this unit's 128 rows are one scale group of the
-          // down projection's reduction, so the group's largest |h| sets the record's power of two
+          // h rounded to bf16, then its record: this unit's 128 rows are one scale group of the down
+          // projection's reduction, so the group's largest |h| sets the record's fixed point
           float hv[kNE];
 #pragma unroll
           for (int t = 0; t < kNE; ++t) {
             float m = 0.0f;  // only quarter 0 holds the full sums after a split unit's hand-off
             if (t < un.n) {
-              const float xsc = S.xs[S.sorted[un.p0 + t]];
-              hv[t] = __bfloat162float(__float2bfloat16_rn(silu_mul(acc[t][0] * xsc, acc[t][1] * xsc)));
+              hv[t] = __bfloat162float(__float2bfloat16_rn(silu_mul(acc[t][0], acc[t][1])));
               if (q == 0) m = fabsf(hv[t]);
             } else {
               hv[t] = 0.0f;
@@ -686,11 +891,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float m = 0.0f;
 #pragma unroll
                 for (int w = 0; w < kComputeWarps; ++w) m = fmaxf(m, S.red[red_buf][w][t]);
-                const int kh = f16_exponent(m);
+                const int kh = fixed_exponent(m);
+                const int X = fixed_value(hv[t], kh);
                 uint8_t* rec = static_cast<uint8_t*>(a.h) +
                                (static_cast<int64_t>(un.p0 + t) * (I / 128) + un.rb) * kRec;
-                reinterpret_cast<__half*>(rec)[r] = __float2half_rn(hv[t] * ldexpf(1.0f, -kh));
-                if (r == 0) *reinterpret_cast<float*>(rec + 256) = ldexpf(1.0f, kh);
+                rec[r] = static_cast<uint8_t>(X & 0xff);
+                rec[128 + r] = static_cast<uint8_t>((X >> 8) & 0xff);
+                rec[256 + r] = static_cast<uint8_t>((X >> 16) & 0xff);
+                if (r == 0) *reinterpret_cast<float*>(rec + kRecScale) = ldexpf(1.0f, kh);
               }
             }
           }
@@ -715,24 +923,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[kNE][1];
 #pragma unroll
       for (int t = 0; t < kNE; ++t) acc[t][0] = 0.0f;
-      const int box = q >> 1;  // quarters 0, 1 read the slot's first slice, 2, 3 its second
       for (; i < pe; ++i) {
         const uint32_t st = take();
-        const uint32_t row = st + box * 16384 + r * 128;
-        const int cb = 4 * (q & 1);
-        const uint4 w0 = lds128(row + (((cb + 0) ^ x7) << 4)), w1 = lds128(row + (((cb + 1) ^ x7) << 4));
-        const uint4 w2 = lds128(row + (((cb + 2) ^ x7) << 4)), w3 = lds128(row + (((cb + 3) ^ x7) << 4));
-        const uint32_t wq[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                                 w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+        // every quarter reads the same two chunks of both reduction slices of the slot (the two boxes):
+        // in every load the four quarters touch four distinct chunk pairs, i.e. distinct banks
+        const uint32_t rowa = st + r * 128, rowb = rowa + 16384;
         if constexpr (!kInt8) {
-          const uint32_t tb = st + G::kTokOff + q * 64;
+          const int ca = 2 * q, cb = 2 * q + 1;
+          const uint4 w0 = lds128(rowa + ((ca ^ x7) << 4)), w1 = lds128(rowa + ((cb ^ x7) << 4));
+          const uint4 w2 = lds128(rowb + ((ca ^ x7) << 4)), w3 = lds128(rowb + ((cb ^ x7) << 4));
+          const uint32_t wq[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                   w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+          // h elements 16q .. 16q + 15 of each 64-element slice: bytes 32q and 128 + 32q of the slot
+          const uint32_t tb = st + G::kTokOff + q * 32;
 #pragma unroll
           for (int t = 0; t < kNE; ++t) {
             if (t < un.n) {
               float ya = acc[t][0], yb = 0.0f;
 #pragma unroll
               for (int hq = 0; hq < 4; ++hq) {
-                const uint4 xv = lds128(tb + t * G::kSliceDN + hq * 16);
+                const uint4 xv = lds128(tb + t * G::kSliceDN + (hq >> 1) * 128 + (hq & 1) * 16);
                 ya = fma2_bf16(wq[4 * hq + 0], xv.x, ya);
                 yb = fma2_bf16(wq[4 * hq + 1], xv.y, yb);
                 ya = fma2_bf16(wq[4 * hq + 2], xv.z, ya);
@@ -742,26 +952,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          uint32_t wh[32];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) int8x4_to_f16x2x2(wq[j], wh[2 * j], wh[2 * j + 1]);
+          // int8 elements 32q .. 32q + 31 of each of the slot's two scale groups (one per box), against
+          // the two h records' digit planes; quarters 2 and 3 take their two chunks in the other order
+          const int ca = 2 * q + (q >> 1), cb = 2 * q + 1 - (q >> 1);
+          const uint4 w0 = lds128(rowa + ((ca ^ x7) << 4)), w1 = lds128(rowa + ((cb ^ x7) << 4));
+          const uint4 w2 = lds128(rowb + ((ca ^ x7) << 4)), w3 = lds128(rowb + ((cb ^ x7) << 4));
+          const uint32_t wa[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const uint32_t wb[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
           const int kk2 = static_cast<int>(i - ub);
-          const float sd = lds_f32(st + G::kWBytes + r * 16 + ((2 * kk2 + box) & 3) * 4);
-          const uint32_t tb = st + G::kTokOff + box * kRec;
+          const uint32_t sbox = st + G::kWBytes + r * 16;
+          const float sa = lds_f32(sbox + ((2 * kk2) & 3) * 4), sb = lds_f32(sbox + ((2 * kk2 + 1) & 3) * 4);
 #pragma unroll
           for (int t = 0; t < kNE; ++t) {
             if (t < un.n) {
-              const uint32_t rec = tb + t * G::kSliceDN;
-              float ya = 0.0f, yb = 0.0f;
-#pragma unroll
-              for (int hq = 0; hq < 8; ++hq) {
-                const uint4 xv = lds128(rec + (q & 1) * 128 + hq * 16);
-                ya = fma2_f16(wh[4 * hq + 0], xv.x, ya);
-                yb = fma2_f16(wh[4 * hq + 1], xv.y, yb);
-                ya = fma2_f16(wh[4 * hq + 2], xv.z, ya);
-                yb = fma2_f16(wh[4 * hq + 3], xv.w, yb);
-              }
-              acc[t][0] = fmaf(ya + yb, sd * lds_f32(rec + 256), acc[t][0]);
+              const uint32_t reca = st + G::kTokOff + t * G::kSliceDN, recb = reca + kRec;
+              acc[t][0] = fmaf(record_dot(reca, ca, cb, wa), sa * lds_f32(reca + kRecScale), acc[t][0]);
+              acc[t][0] = fmaf(record_dot(recb, ca, cb, wb), sb * lds_f32(recb + kRecScale), acc[t][0]);
             }
           }
         }
@@ -773,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[t][0] += __shfl_xor_sync(0xffffffffu, acc[t][0], 2);
       }
       bool finish = true;
-      if (!(ub >= d_beg && ue <= d_end)) finish = split_unit(acc, std::integral_constant<int, 1>{}, ub, ue, d_beg, Wd, NCd, KId);
+      if (!(ub >= d_beg && ue <= d_end)) finish = split_unit(acc, std::integral_constant<int, 1>{}, ub, ue, d_beg, KId, pos_dn, first_dn, Nd, Cd);
       if (!finish) continue;
       const int h_row = un.rb * 128 + r;
       if (q == 0) {
@@ -813,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 }
 
-template <bool kInt8>
+template <bool kInt8, int kNE>
 cudaError_t prepare(int* max_ctas) {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev];
@@ -827,11 +1033,11 @@ cudaError_t prepare(int* max_ctas) {
       return cudaSuccess;
     }
   }
-  e = cudaFuncSetAttribute(decode_step_kernel<kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_step_kernel<kInt8, kNE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem_bytes<kInt8>());
   if (e != cudaSuccess) return e;
   int per_sm = 0, sms = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_step_kernel<kInt8>, kThreads,
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_step_kernel<kInt8, kNE>, kThreads,
                                                     smem_bytes<kInt8>());
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -854,7 +1060,7 @@ bool encode_scales(CUtensorMap* map, const float* s, int groups, int rows, int E
                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kInt8>
+template <bool kInt8, int kNE>
 cudaError_t launch(const DecodePlan& p, cudaStream_t stream) {
   CUtensorMap tg, tu, td, tsg, tsu, tsd;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
@@ -870,7 +1076,7 @@ cudaError_t launch(const DecodePlan& p, cudaStream_t stream) {
                 !encode_scales(&tsd, p.s_down, p.I / 128, p.H, p.E)))
     return cudaErrorInvalidValue;
   int max_ctas = 0;
-  cudaError_t e = prepare<kInt8>(&max_ctas);
+  cudaError_t e = prepare<kInt8, kNE>(&max_ctas);
   if (e != cudaSuccess) return e;
   const int ctas = max_ctas < p.max_ctas ? max_ctas : p.max_ctas;
   // cooperative (all CTAs resident: the grid barrier waits on every CTA) and, where the driver
@@ -889,12 +1095,12 @@ cudaError_t launch(const DecodePlan& p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_ok.load(std::memory_order_relaxed) ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8>, tg, tu, td, tsg, tsu, tsd, p.args);
+  e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8, kNE>, tg, tu, td, tsg, tsu, tsd, p.args);
   if (e != cudaSuccess && cfg.numAttrs == 2) {
     cudaGetLastError();  // clear the launch error, then launch cooperatively alone
     pdl_ok.store(0, std::memory_order_relaxed);
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8>, tg, tu, td, tsg, tsu, tsd, p.args);
+    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8, kNE>, tg, tu, td, tsg, tsu, tsd, p.args);
   }
   return e;
 }
@@ -908,8 +1114,24 @@ bool decode_step_supported(int T, int H, int I, int E, int k, bool int8) {
   return true;
 }
 
+// Tokens per pass: exactly one per expert at T = 1; four while the batch has at most one assignment
+// per expert on average (a hotter expert takes several passes); eight above. Fewer tokens per pass
+// keep the compute loops short (instruction-cache misses were the top stall of the INT8 kernel at T = 1
+// with eight-token loops).
+template <bool kInt8>
+cudaError_t launch_ne(const DecodePlan& plan, cudaStream_t stream) {
+  const DecodeArgs& a = plan.args;
+  if (a.T == 1) return dec::launch<kInt8, 1>(plan, stream);
+  if constexpr (kInt8) {
+    return dec::launch<true, 4>(plan, stream);  // INT8: passes of at most 4 (the slots hold 4 tokens' records)
+  } else {
+    if (static_cast<int64_t>(a.T) * a.k <= a.E) return dec::launch<false, 4>(plan, stream);
+    return dec::launch<false, 8>(plan, stream);
+  }
+}
+
 cudaError_t launch_decode_step(const DecodePlan& plan, cudaStream_t stream) {
-  return plan.int8 ? dec::launch<true>(plan, stream) : dec::launch<false>(plan, stream);
+  return plan.int8 ? launch_ne<true>(plan, stream) : launch_ne<false>(plan, stream);
 }
 
 }  // namespace moe

@@ -109,8 +109,8 @@ struct DecodeArgs {
   const uint16_t* x;     // [T, H] bf16
   const float* logits;   // [T, E]
   uint16_t* out;         // [T, H] bf16
-  uint16_t* x16;         // INT8: [T, H] fp16 copies of the token rows (scratch)
-  void* h;               // BF16: [P, I] bf16; INT8: [P, I / 128] records of 272 bytes (scratch)
+  uint16_t* x16;         // INT8: [T, H / 128] records of 400 bytes, the token rows as digit planes (scratch)
+  void* h;               // BF16: [P, I] bf16; INT8: [P, I / 128] records of 400 bytes (scratch)
   float* Y;              // [P, H] (scratch)
   float* partials;       // stream-K partial slots, [num CTAs][2][kPartialSlotFloats]
   int32_t* counters;     // stream-K counters, zero on entry, left zero

@@ -16,14 +16,25 @@ __device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
+// Order-preserving 32-bit image of a logit (NaN already mapped to -inf; -0 and +0 share +0's image,
+// as they compare equal): a larger logit has a larger key. key_value inverts it (-0 comes back as +0).
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Top-k of kNT tokens by the calling warp: tokens tok0 + t * tok_step (t < kNT; those at or past T
 // are skipped). Each lane holds kPer logits of a token (experts lane, lane + 32, ...; kPer = 4 covers
 // E <= 128, 8 covers E <= 256) and sorts them once, best first (odd-even merge networks: 5
-// compare-exchanges for 4, 19 for 8); every round the lanes' heads meet in an xor butterfly, which
-// leaves the winner in all lanes, and the winning lane drops its head. Past E a lane holds
+// compare-exchanges for 4, 19 for 8); every round two warp reductions over the lanes' heads leave the
+// winner in all lanes, and the winning lane drops its head. Past E a lane holds
 // (-inf, none), which loses to every real expert. Round j's winner of token t goes to
 // sel_v[t * sel_step + j] / sel_i[...] (shared memory): per-lane arrays indexed by the round would
-// live in local memory. With kNT = 2 the two tokens' dependent shuffle chains interleave.
+// live in local memory. With kNT = 2 the two tokens' dependent reduction chains interleave.
 template <int kPer, int kNT>
 __device__ __forceinline__ void topk_tokens(const float* __restrict__ logits, int tok0, int tok_step, int T, int E,
                                             int k, int32_t* ids, float* w, float* sel_v, int* sel_i,
@@ -80,20 +91,14 @@ __device__ __forceinline__ void topk_tokens(const float* __restrict__ logits, in
     int bi[kNT];
 #pragma unroll
     for (int t = 0; t < kNT; ++t) {
-      bv[t] = cv[t][0];
-      bi[t] = ci[t][0];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-      for (int t = 0; t < kNT; ++t) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv[t], o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi[t], o);
-        if (route_better(ov, oi, bv[t], bi[t])) {
-          bv[t] = ov;
-          bi[t] = oi;
-        }
-      }
+      // the round's winner over the lanes' heads in two warp reductions: the largest key (an
+      // order-preserving 32-bit image of the logit), then the lowest expert id among the heads that
+      // hold it (equal logits go to the lower id)
+      const uint32_t key = ordered_key(cv[t][0]);
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t wi = __reduce_min_sync(0xffffffffu, key == mk ? static_cast<uint32_t>(ci[t][0]) : 0xffffffffu);
+      bv[t] = key_value(mk);
+      bi[t] = static_cast<int>(wi);
     }
 #pragma unroll
     for (int t = 0; t < kNT; ++t) {

@@ -2,7 +2,8 @@
 the CPU oracle, element by element, through the C ABI (needs a GPU).
 
 moe_ffn_forward takes this path for small decode batches; here the policy forces it (2) so that every
-shape below runs it, including skewed batches whose hot experts need several passes of 8 tokens, and
+shape below runs it (passes of 1 token at T = 1, of 4 when P <= E, of 8 above), including skewed batches
+whose hot experts need several passes, and
 checks it against the oracle and against the staged path (policy 1). The workspace's counters must be
 back at zero after every call, so that consecutive calls on one workspace need no clearing.
 """
@@ -92,6 +93,9 @@ CASES = [
     (16, 512, 1024, 32, 2, "int8", (3,)),         # expert 3 gets every token: two passes
     (32, 512, 512, 64, 8, "int8", ()),            # P = 256
     (2, 1536, 512, 8, 2, "int8", ()),
+    # passes of 4 tokens (at most one assignment per expert on average): a hot expert takes several
+    (8, 512, 512, 64, 2, "bf16", (0,)),           # expert 0 gets all 8 tokens: two passes
+    (12, 512, 512, 64, 4, "int8", (1,)),          # expert 1 gets all 12: three passes
 ]
 
 
