@@ -49,6 +49,7 @@ METRIC_HOST = ("expert-FFN decode weight-stream GB/s with the expert weights in 
                "NVLink-C2C (% of the measured host->device copy rate) and tokens/s, 1 GB300")
 METRIC_ATTN = "decode GQA attention key/value-cache read GB/s (% of peak) and sequences/s, 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 
 
 def kernels_per_step(cfg, T: int, moe=None) -> int:
@@ -109,6 +110,16 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 TFLOP/s sustained under the power cap (a kernel timed inside back-to-back steps)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured (bf16_tflops_sustained)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback (sustained)"
 
 
 # the sources of the roofline kernels and of their launches: the expert kernels (all of them, and
@@ -273,7 +284,7 @@ def expert_ffn(moe, cfg, L, xg, r, Y, ws, stream):
 
 # ------------------------------------------------------------------ workload
 # The (config, T) points of the sweep: every expert shape and token count of the five workloads.
-SWEEP_CONFIGS = ("mixtral8x7b", "mixtral8x22b", "mixtral8x22b_skew", "dsv3", "qwen3_int8")
+SWEEP_CONFIGS = ("mixtral8x7b", "mixtral8x22b", "mixtral8x22b_skew", "dsv3", "qwen3_int8", "mixtral8x7b_prefill")
 L2_BYTES = 129e6
 
 
@@ -614,6 +625,7 @@ def measure_point(moe, cfg, T, layers: Layers, dev, peak, steps=60, warmup=5, n_
     wb = sum(wl.weight_bytes(i % wl.copies) for i in range(steps)) / steps
     gbs = wb / (ms * 1e-3) / 1e9
     kernel, ach, frac, avg_ms, _ = roofline_for(moe, wl, ws, s, n_roof, peak)
+    flops = 2 * 3 * cfg.H * cfg.I * T * cfg.top_k  # routed work: 2 flops per weight per token routed to it
     row = {"workload": f"{cfg.name}_T{T}", "weights": cfg.wtype, "T": T,
            "active_experts": round(sum(wl.active) / len(wl.active), 2),
            "tokens_per_expert": round(T * cfg.top_k * len(wl.active) / sum(wl.active), 2),
@@ -621,7 +633,13 @@ def measure_point(moe, cfg, T, layers: Layers, dev, peak, steps=60, warmup=5, n_
            "tokens_per_s": round(T / (ms * 1e-3), 1), "launches_per_step": kernels_per_step(cfg, T, moe),
            "roofline": {"kernel": kernel, "achieved": round(ach, 1),
                         "frac": round(frac, 4), "avg_launch_us": round(avg_ms * 1e3, 2)},
-           "copies": wl.copies}
+           "copies": wl.copies,
+           "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
+    if cfg.wtype == "bf16" and T * cfg.top_k >= 32 * cfg.E:  # a real contraction: the tensor-core roofline
+        tp, kind = tensor_peak()
+        call = flops / (avg_ms * 1e-3) / 1e12
+        row["tensor_roofline"] = {"kernel": "expert FFN (gate+up, down), timed together", "achieved": round(call, 1),
+                                  "peak": tp, "peak_kind": kind, "unit": "TFLOP/s", "frac": round(call / tp, 4)}
     del wl, ws
     return row
 

@@ -144,8 +144,14 @@ moe_status_t moe_gather(const uint16_t* x, int T, int H, int top_k, const int32_
  *   P               = T * top_k, the number of rows of xg and Y
  *   Y               [P, H] f32 out, expert-sorted rows
  *   workspace       >= moe_workspace_size(T, H, I, E, top_k, wtype) bytes (device)
- * Only the weights of active experts are read, each once per 64 tokens routed to it.
- * The result is deterministic for a given device.
+ * Only the weights of active experts are read. BF16 weights stream once per pass of an
+ * expert's tokens: 64-token passes when the mean tokens per expert P / E is at most 40,
+ * 128 up to 96, 256 above (moe_set_expert_pass_tokens can force a size). At 128- and
+ * 256-token passes an expert with more tokens than one pass has them split evenly over up
+ * to 4 CTAs that run the same weight blocks side by side, so its weights come from HBM
+ * once and from L2 for the others (up to 4 x 256 tokens per expert; more take further
+ * rounds). INT8 weights stream once per 64 tokens.
+ * The result is deterministic for a given device and pass size.
  */
 moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets,
                             const int32_t* active_experts, const int32_t* num_active,
@@ -207,12 +213,13 @@ moe_status_t moe_combine(const float* Y, const int32_t* inv_pos, const float* to
  *   out [T, H] bf16;  workspace >= moe_workspace_size(T, H, I, E, top_k, wtype).
  * The routing, the gathered block, h and Y live in the workspace; the host never
  * learns the routing, so the call is free of host synchronisation.
- * Small decode batches (by default when T * top_k <= 2 E, with T <= 32, T * top_k <= 256,
- * H and I multiples of 128, for INT8 multiples of 512) run as ONE cooperative kernel that
- * routes, streams both projections on CUDA-core FMAs and combines; larger batches run
- * the routing, gather, tensor-core expert kernels and combine as separate launches.
- * Both give results within the same tolerance of the definition; the routing tables in
- * the workspace are the same. moe_set_decode_step_policy chooses between them.
+ * By default it runs the routing, gather, tensor-core expert kernels and combine as
+ * separate launches (linked by programmatic dependent launch). moe_set_decode_step_policy
+ * can instead run small decode batches (T <= 32, T * top_k <= 256, H and I multiples of
+ * 128, for INT8 multiples of 512) as ONE cooperative kernel that routes, streams both
+ * projections on CUDA-core FMAs and combines; measured on GB300 it is not faster than the
+ * separate launches, so it is not the default. Both give results within the same
+ * tolerance of the definition; the routing tables in the workspace are the same.
  */
 moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void* W_gate,
                              const void* W_up, const void* W_down, const float* s_gate,
@@ -222,12 +229,22 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
 
 /*
  * Which implementation moe_ffn_forward uses (process-wide; the default is 0):
- *   0  by batch shape (the rule above);
+ *   0  by batch shape (currently: the separate launches for every shape);
  *   1  never the one-launch decode step;
  *   2  the one-launch decode step whenever the sizes allow it.
  * Returns MOE_ERR_INVALID_ARG for any other value. Affects only later calls.
  */
 moe_status_t moe_set_decode_step_policy(int policy);
+
+/*
+ * Tokens per pass of the BF16 expert kernels, gate+up and down separately: 64, 128 or 256,
+ * or 0 for the rule of moe_expert_ffn (the default). A tuning and test control; the paper
+ * has no counterpart. Process-wide, affects only later calls. moe_workspace_size sizes the
+ * stream-K partial slots for the sizes in force when it is called; a call whose workspace
+ * was sized for smaller passes runs 64-token passes instead. Results differ between pass
+ * sizes only in fp32 summation order. Returns MOE_ERR_INVALID_ARG for other values.
+ */
+moe_status_t moe_set_expert_pass_tokens(int gate_up, int down);
 
 /*
  * Failure-detection test hook; the paper has no counterpart. While enabled (enable = 1), the

@@ -79,6 +79,10 @@ CONFIGS: Dict[str, MoEConfig] = {
         MoEConfig("mixtral8x22b_skew", 6144, 16384, 8, 2, "bf16", (1, 4, 16, 64),
                   skew_experts=(0, 1), skew=2.0),
         MoEConfig("dsv3", 7168, 2048, 256, 8, "bf16", (1, 16, 128, 512)),
+        # Prefill-sized batches of the Mixtral-8x7B expert shape (the pages run prefill at 2K-32K
+        # tokens, HiNa-MoE §8.2 "Prefill Phase", Table 4): 64 to 1024 tokens per expert, where the
+        # expert FFN is a real contraction and is timed in TFLOP/s.
+        MoEConfig("mixtral8x7b_prefill", 4096, 14336, 8, 2, "bf16", (256, 1024, 2048, 4096)),
         MoEConfig("qwen3_int8", 4096, 1536, 128, 8, "int8", (1, 8, 64, 256)),
         MoEConfig("qwen3_int8_residual", 4096, 1536, 128, 8, "int8_residual", (1, 8, 64, 256)),
     )

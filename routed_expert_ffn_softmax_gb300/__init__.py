@@ -27,7 +27,7 @@ __all__ = [
     "moe_expert_ffn", "moe_combine", "moe_ffn_forward", "alloc_workspace", "workspace_status",
     "moe_expert_ffn_noalloc", "moe_expert_ffn_noalloc_status", "moe_gqa_workspace_size", "moe_gqa_decode", "alloc_gqa_workspace",
     "moe_expert_ffn_residual", "moe_ffn_forward_residual", "moe_set_decode_step_policy", "moe_ffn_forward_launches",
-    "moe_test_expire_grid_barrier",
+    "moe_test_expire_grid_barrier", "moe_set_expert_pass_tokens",
 ]
 
 MOE_W_BF16 = 0
@@ -175,6 +175,15 @@ def moe_ffn_forward(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, top_k
 def moe_set_decode_step_policy(policy: int) -> None:
     """0: by batch shape (default); 1: never the one-launch decode step; 2: whenever the sizes allow."""
     _check("moe_set_decode_step_policy", load().moe_set_decode_step_policy(policy))
+
+
+def moe_set_expert_pass_tokens(gate_up: int = 0, down: int = 0) -> None:
+    """Tokens per pass of the BF16 expert kernels (64, 128 or 256; 0 = by batch shape, the default).
+    Size workspaces after setting it (see include/moe.h)."""
+    f = load().moe_set_expert_pass_tokens
+    f.argtypes = [ctypes.c_int, ctypes.c_int]
+    f.restype = ctypes.c_int
+    _check("moe_set_expert_pass_tokens", f(int(gate_up), int(down)))
 
 
 def moe_test_expire_grid_barrier(enable: bool, wait_ns: int = 2_000_000_000) -> None:

@@ -15,7 +15,6 @@
 namespace {
 
 constexpr int kMaxCtas = moe::kPartialCtas;
-constexpr int kPartialFloats = moe::kPartialSlotFloats;
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -40,15 +39,25 @@ constexpr int kZeroWords = static_cast<int>((kCountersOffset + 4 * kMaxCtas) / 4
 struct Layout {
   size_t ctrl, partials, h, h16, xg16, h_scale, xg_scale, ids, w, counts, offsets, sorted_token, inv_pos, active,
       num_active, xg, Y, hrec, total;
+  int64_t partial_slot;      // fp32 per stream-K partial slot
+  moe::PassTokens passes;    // BF16 tokens per pass the slots are sized for
 };
 
 Layout layout(int64_t P, int H, int I, int E, bool int8) {
   Layout L{};
+  L.passes = int8 ? moe::PassTokens{64, 64} : moe::pass_tokens(P, E);
+  L.partial_slot = moe::kPartialSlotFloats;
+  if (!int8) {
+    const int64_t gu = moe::partial_slot_floats(L.passes.gate_up, true);
+    const int64_t dn = moe::partial_slot_floats(L.passes.down, false);
+    L.partial_slot = gu > L.partial_slot ? gu : L.partial_slot;
+    L.partial_slot = dn > L.partial_slot ? dn : L.partial_slot;
+  }
   size_t o = 0;
   L.ctrl = o;
   o += kCtrlBytes;
   L.partials = o;
-  o = align_up(o + sizeof(float) * static_cast<size_t>(kMaxCtas) * 2 * kPartialFloats);
+  o = align_up(o + sizeof(float) * static_cast<size_t>(kMaxCtas) * 2 * static_cast<size_t>(L.partial_slot));
   L.h = o;
   o = align_up(o + 2 * static_cast<size_t>(P) * I);
   L.h16 = L.xg16 = L.h_scale = L.xg_scale = o;
@@ -183,6 +192,8 @@ moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const in
   plan.xg16_ready = xg16_ready;
   plan.Y = Y;
   plan.partials = reinterpret_cast<float*>(ws + L.partials);
+  plan.partial_slot = L.partial_slot;
+  plan.passes = L.passes;
   plan.counters = reinterpret_cast<int32_t*>(ws + L.ctrl + kCountersOffset);
   plan.status = reinterpret_cast<int32_t*>(ws + L.ctrl);
   plan.num_ctas = sms < kMaxCtas ? sms : kMaxCtas;
@@ -425,6 +436,13 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
 moe_status_t moe_set_decode_step_policy(int policy) {
   if (policy < 0 || policy > 2) return MOE_ERR_INVALID_ARG;
   g_decode_policy.store(policy, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_set_expert_pass_tokens(int gate_up, int down) {
+  auto ok = [](int n) { return n == 0 || n == 64 || n == 128 || n == 256; };
+  if (!ok(gate_up) || !ok(down)) return MOE_ERR_INVALID_ARG;
+  moe::set_pass_tokens(gate_up, down);
   return MOE_OK;
 }
 

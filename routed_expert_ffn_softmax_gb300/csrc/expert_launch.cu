@@ -131,7 +131,7 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, int K, int P, uint16_t* dst,
                     src_prefetch_bytes);
 }
 
-template <bool kGateUp>
+template <bool kGateUp, int kN>
 cudaError_t prepare_tc_kernel() {
   constexpr int kMaxDev = 64;
   static std::atomic<bool> done[kMaxDev];
@@ -139,25 +139,53 @@ cudaError_t prepare_tc_kernel() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::Geo<kGateUp>::kSmem);
+  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp, kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::Geo<kGateUp, kN>::kSmem);
   if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
-// BF16: weight boxes of 128 rows by 128 bytes, token boxes of 16 rows.
+template <bool kGateUp, int kN>
+cudaError_t launch_tc_kernel(const CUtensorMap& a0, const CUtensorMap& a1, const void* tokens, int K, int P,
+                             const tc::Args& args, int num_ctas, cudaStream_t s) {
+  using G = tc::Geo<kGateUp, kN>;
+  CUtensorMap tb;
+  if (!encode_tokens(&tb, tokens, K, P, false, G::kBoxRows)) return cudaErrorInvalidValue;
+  cudaError_t e = prepare_tc_kernel<kGateUp, kN>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tc::expert_tc_kernel<kGateUp, kN>, dim3(num_ctas), dim3(G::kThreads), G::kSmem, s, a0, a1, tb,
+                    args);
+}
+
+// Launch the kernel of `pass` tokens per pass (64, 128 or 256), or of 64 where its partial slots
+// would not fit in `slot` fp32.
+template <bool kGateUp>
+cudaError_t launch_tc_pass(int pass, int64_t slot, const CUtensorMap& a0, const CUtensorMap& a1, const void* tokens,
+                           int K, int P, tc::Args args, int num_ctas, cudaStream_t s) {
+  if (partial_slot_floats(pass, kGateUp) > slot) pass = 64;
+  args.partial_stride = partial_slot_floats(pass, kGateUp);
+  if (pass == 256) return launch_tc_kernel<kGateUp, 256>(a0, a1, tokens, K, P, args, num_ctas, s);
+  if (pass == 128) return launch_tc_kernel<kGateUp, 128>(a0, a1, tokens, K, P, args, num_ctas, s);
+  args.partial_stride = kPartialSlotFloats;
+  return launch_tc_kernel<kGateUp, 64>(a0, a1, tokens, K, P, args, num_ctas, s);
+}
+
+std::atomic<int> g_pass_gate_up{0}, g_pass_down{0};
+int pass_by_mean(int64_t P, int E) {
+  const int64_t mean = (P + E - 1) / (E > 0 ? E : 1);
+  return mean <= 40 ? 64 : (mean <= 96 ? 128 : 256);
+}
+int valid_pass(int n) { return n == 64 || n == 128 || n == 256 ? n : 0; }
+
+// BF16: weight boxes of 128 rows by 128 bytes, token boxes of 16 rows (64-token passes) or 32.
 cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
-  CUtensorMap tg, tu, td, txg, th;
+  CUtensorMap tg, tu, td;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
   if (!encode_weights(&tg, p.W_gate, false, p.H, p.I, p.E, 128) ||
       !encode_weights(&tu, p.W_up, false, p.H, p.I, p.E, 128) ||
-      !encode_weights(&td, p.W_down, false, p.I, p.H, p.E, 128) || !encode_tokens(&txg, p.xg, p.H, p.P, false, 16) ||
-      !encode_tokens(&th, p.h, p.I, p.P, false, 16))
+      !encode_weights(&td, p.W_down, false, p.I, p.H, p.E, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = prepare_tc_kernel<true>();
-  if (e != cudaSuccess) return e;
-  e = prepare_tc_kernel<false>();
-  if (e != cudaSuccess) return e;
+  const int64_t slot = p.partial_slot > kPartialSlotFloats ? p.partial_slot : kPartialSlotFloats;
   tc::Args a{};
   a.offsets = p.offsets;
   a.active = p.active;
@@ -172,16 +200,14 @@ cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
   gu.out_ld = p.I;
   gu.rows = p.I;
   gu.K = p.H;
-  e = launch_pdl(tc::expert_tc_kernel<true>, dim3(p.num_ctas), dim3(tc::Geo<true>::kThreads), tc::Geo<true>::kSmem,
-                 s, tg, tu, txg, gu);
+  cudaError_t e = launch_tc_pass<true>(p.passes.gate_up, slot, tg, tu, p.xg, p.H, p.P, gu, p.num_ctas, s);
   if (e != cudaSuccess) return e;
   tc::Args dn = a;
   dn.out = p.Y;
   dn.out_ld = p.H;
   dn.rows = p.H;
   dn.K = p.I;
-  return launch_pdl(tc::expert_tc_kernel<false>, dim3(p.num_ctas), dim3(tc::Geo<false>::kThreads),
-                    tc::Geo<false>::kSmem, s, td, td, th, dn);
+  return launch_tc_pass<false>(p.passes.down, slot, td, td, p.h, p.I, p.P, dn, p.num_ctas, s);
 }
 
 // ---- INT8 on CTA pairs
@@ -342,6 +368,18 @@ cudaError_t launch_gather_f16(const uint16_t* x, int T, int H, int P, const int3
   const int64_t x_bytes = static_cast<int64_t>(T) * H * 2;
   return launch_rows_to_f16(x, H, P, xg16, xg_scale, num_sms, stream, sorted_token,
                             x_bytes <= kPrefetchMaxBytes ? x_bytes : int64_t{0});
+}
+
+PassTokens pass_tokens(int64_t P, int E) {
+  const int auto_pass = pass_by_mean(P, E);
+  const int gu = valid_pass(g_pass_gate_up.load(std::memory_order_relaxed));
+  const int dn = valid_pass(g_pass_down.load(std::memory_order_relaxed));
+  return PassTokens{gu ? gu : auto_pass, dn ? dn : auto_pass};
+}
+
+void set_pass_tokens(int gate_up, int down) {
+  g_pass_gate_up.store(valid_pass(gate_up), std::memory_order_relaxed);
+  g_pass_down.store(valid_pass(down), std::memory_order_relaxed);
 }
 
 cudaError_t launch_expert_ffn(const ExpertFfnPlan& plan, cudaStream_t stream) {

@@ -28,27 +28,33 @@ namespace tc {
 
 constexpr int kEpiThreads = 128;    // warps 2..5
 constexpr int kTable = 256;
-constexpr int kIssueGroup = 1;  // stages issued per producer wake-up: each as soon as its slot drains
-constexpr int kPartialFloats = 16384;  // one CTA slot: 128 rows x 128 accumulator columns
+constexpr int kPartialFloats = 16384;  // one INT8 pair-kernel CTA slot: 128 rows x 128 accumulator columns
+constexpr int kMaxRanks = 4;           // CTAs sharing one weight block (BF16, 128- and 256-token passes)
 
-template <bool kGateUp>
+// kN: tokens per pass (64, 128 or 256; the launch picks it from the batch's tokens per expert). An
+// expert with more tokens than a pass streams its weights once per pass, so larger passes read the
+// weights fewer times when experts see many tokens (prefill-sized batches); smaller passes leave room
+// for more stages at decode sizes.
+template <bool kGateUp, int kN = 64>
 struct Geo {
   static constexpr int kThreads = 192;
-  static constexpr int kNMax = 64;                          // tokens per pass
+  static constexpr int kNMax = kN;                          // tokens per pass
   static constexpr int kKStage = 64;                        // reduction elements per stage
   static constexpr int kWBytes = kGateUp ? 32768 : 16384;   // weight bytes per stage
-  static constexpr int kBBytes = kNMax * 128;               // token tile: 64 rows x 64 elements x 2 B
+  static constexpr int kBBytes = kNMax * 128;               // token tile: kN rows x 64 elements x 2 B
+  static constexpr int kBoxRows = kN >= 128 ? 32 : 16;      // token rows per TMA box
   static constexpr int kStage = kWBytes + kBBytes;
-  static constexpr int kStages = kGateUp ? 5 : 9;                // down: as many as fit (7: -0.4%, 9: +0.3%)
-  static constexpr int kAccCols = kGateUp ? 2 * kNMax : kNMax;  // one accumulator buffer
-  static constexpr int kTmemCols = 2 * kAccCols;                 // double buffered
-  static constexpr int kBarBytes = (2 * kStages + 5) * 8;
   static constexpr int kTableBytes = (4 * kTable + 32) * 4;
+  // as many stages as fit (down at 64-token passes: 9; measured on GB300 7: -0.4%, 9: +0.3%)
+  static constexpr int kStages = (232448 - kTableBytes - 256) / kStage;
+  static constexpr int kAccCols = kGateUp ? 2 * kNMax : kNMax;  // one accumulator buffer
+  static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;  // double buffered where TMEM allows
+  static constexpr int kTmemCols = kAccBufs * kAccCols;
+  static constexpr int kBarBytes = (2 * kStages + 5) * 8;
   static constexpr int kSmem = kStages * kStage + kBarBytes + kTableBytes;
+  static constexpr int64_t kPartialSlot = 128LL * kAccCols;     // fp32 per stream-K partial slot
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
-  static_assert(kTmemCols == 128 || kTmemCols == 256, "TMEM allocations are powers of two");
-  static_assert(128 * kAccCols <= kPartialFloats, "partial slot size");
-  static_assert(kIssueGroup <= kStages, "an issue group must fit in the ring");
+  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
   static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
 
@@ -58,7 +64,8 @@ struct Args {
   const int32_t* num_active;  // [1]
   void* out;                  // h bf16 [P, I] (gate+up) or Y f32 [P, H] (down)
   int64_t out_ld;
-  float* partials;            // [kMaxCtas][2][kPartialFloats]
+  float* partials;            // [kMaxCtas][2][partial_stride]
+  int64_t partial_stride;     // fp32 per partial slot (BF16: at least Geo<kGateUp, kN>::kPartialSlot)
   int32_t* counters;          // zero on entry, left zero on exit
   int32_t* status;
   int rows;                   // I (gate+up) or H (down)
@@ -129,11 +136,20 @@ __device__ __forceinline__ int load_schedule(const Args& args, int* t_e, int* t_
   return A;
 }
 
-template <bool kGateUp>
-__global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
+// A rank's share of a round of mr tokens split over g ranks: a multiple of 16.
+__device__ __forceinline__ int rank_share(int mr, int g) { return ((mr + g - 1) / g + 15) / 16 * 16; }
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+template <bool kGateUp, int kN>
+__global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const Args args) {
-  using G = Geo<kGateUp>;
+  using G = Geo<kGateUp, kN>;
   constexpr int kThreads = G::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStage);
@@ -180,12 +196,32 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == 0) {  // prefix sum of the 256 pass counts: 8 per lane, then a warp scan
+  if (warp == 0) {
+    // Ranks per weight block: at 128- and 256-token passes (prefill-sized batches), an expert with
+    // more tokens than one pass has them split evenly over g CTAs (ranks) that run the same reduction
+    // stages of the same weight blocks side by side, so the weights come from HBM once and from L2
+    // for the other ranks, instead of once per pass.
+    int mx = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int a = lane * 8 + i;
+      if (a < A) mx = t_ntok[a] > mx ? t_ntok[a] : mx;
+    }
+    mx = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<uint32_t>(mx)));
+    int g = 1;
+    if (G::kNMax >= 128) {
+      g = (mx + G::kNMax - 1) / G::kNMax;
+      g = g < 1 ? 1 : (g > kMaxRanks ? kMaxRanks : g);
+      g = g < static_cast<int>(gridDim.x) ? g : static_cast<int>(gridDim.x);
+    }
+    const int span = g * G::kNMax;  // tokens of an expert per round
+    // rounds per active expert and their prefix sum: 8 per lane, then a warp scan
     int v[8];
     int sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      v[i] = t_pp[1 + lane * 8 + i];
+      const int a = lane * 8 + i;
+      v[i] = a < A ? (t_ntok[a] + span - 1) / span : 0;
       sum += v[i];
     }
     int incl = sum;
@@ -201,9 +237,9 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       t_pp[1 + lane * 8 + i] = run;
     }
     if (lane == 0) t_pp[0] = 0;
-    // One token-tile shape for the whole launch: the largest pass's token count, rounded up to 16.
-    // Every stage loads that many token rows and every MMA takes that many columns; columns past a
-    // pass's own tokens meet the following rows (or TMA's zero fill) and are never read. Measured
+    // One token-tile shape for the whole launch: the largest rank's share, rounded up to the token
+    // box. Every stage loads that many token rows and every MMA takes that many columns; columns past
+    // a rank's own tokens meet the following rows (or TMA's zero fill) and are never read. Measured
     // on GB300, a shape per pass made stages of different passes cost different times, which the
     // equal-stage stream-K split turned into CTAs finishing apart (4-5% at 16 tokens per expert).
     int m = 16;
@@ -211,24 +247,72 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
     for (int i = 0; i < 8; ++i) {
       const int a = lane * 8 + i;
       if (a < A) {
-        const int n = t_ntok[a] < G::kNMax ? t_ntok[a] : G::kNMax;
+        const int n = rank_share(t_ntok[a] < span ? t_ntok[a] : span, g);
         m = n > m ? n : m;
       }
     }
-    m = __reduce_max_sync(0xffffffffu, m);
-    if (lane == 0) s_misc[12] = ((m + 15) >> 4) * 16;
+    m = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<uint32_t>(m)));
+    if (lane == 0) {
+      s_misc[12] = (m + G::kBoxRows - 1) / G::kBoxRows * G::kBoxRows;
+      s_misc[13] = g;
+    }
   }
   __syncthreads();
   const uint32_t tmem_base = *tmem_slot;
   const int n_tile = s_misc[12];  // token rows per stage and MMA columns, 16..kNMax
+  const int ranks = s_misc[13];   // CTAs per weight block
+  const int span = ranks * G::kNMax;
 
+  // Work split over columns of `ranks` CTAs (blockIdx = column * ranks + rank): the CTAs of a column
+  // take the same stages of the same units, each with its rank's share of the tokens. A unit is one
+  // 128-row block of one expert round (KI reduction stages).
+  //  * 64-token passes (decode-sized batches): stream-K over all units, each column a contiguous
+  //    range of stages; a unit split between columns is finished by the last one to arrive.
+  //  * 128- and 256-token passes with at least two units per column: whole units in waves
+  //    (wave w gives column c unit w * NC + c), so the columns work on neighbouring blocks of one
+  //    or two experts at a time and those experts' token rows stay in L2 while the weights stream
+  //    past; the last NC to 2 NC units are split stream-K as above. Contiguous ranges over every
+  //    expert kept all token rows live at once and re-read them from DRAM (4x the down weights at
+  //    512 tokens per expert, measured on GB300).
   const int RB = (args.rows + 127) / 128;
   const int KI = (args.K + G::kKStage - 1) / G::kKStage;
-  const int64_t W = static_cast<int64_t>(t_pp[A]) * RB * KI;
-  const int64_t NC = W < static_cast<int64_t>(gridDim.x) ? W : static_cast<int64_t>(gridDim.x);
+  const int64_t U = static_cast<int64_t>(t_pp[A]) * RB;
+  const int64_t ncols = static_cast<int64_t>(gridDim.x) / ranks;
+  const int64_t col = blockIdx.x / ranks;
+  const int rank = static_cast<int>(blockIdx.x % ranks);
   const int64_t cta = blockIdx.x;
-  const int64_t it_beg = cta < NC ? cta * W / NC : 0;
-  const int64_t it_end = cta < NC ? (cta + 1) * W / NC : 0;
+  const bool waves = G::kNMax >= 128 && U >= 2 * ncols;
+  const int64_t NC = waves ? ncols : (U * KI < ncols ? U * KI : ncols);
+  const int64_t nW = (waves && col < NC) ? U / NC - 1 : 0;          // whole-unit waves of this column
+  const int64_t D = waves ? (U / NC - 1) * NC : 0;                  // units done in waves
+  const int64_t Wt = (U - D) * KI;                                  // stages split stream-K
+  const int64_t sb = col < NC ? col * Wt / NC : 0;                  // this column's stream-K range
+  const int64_t se = col < NC ? (col + 1) * Wt / NC : 0;
+  const int64_t n_sk = sb < se ? (se - 1) / KI - sb / KI + 1 : 0;
+  const int64_t n_pieces = nW + n_sk;
+  const int64_t n_stages = nW * KI + (se - sb);
+
+  // Piece p of this column: unit u and its stages [kb, ke).
+  struct Piece {
+    int64_t u;
+    int kb, ke;
+  };
+  auto piece_of = [&](int64_t p) -> Piece {
+    Piece r;
+    if (p < nW) {
+      r.u = p * NC + col;
+      r.kb = 0;
+      r.ke = KI;
+    } else {
+      const int64_t uf = sb / KI;
+      const int64_t ut = uf + (p - nW);
+      r.u = D + ut;
+      r.kb = p == nW ? static_cast<int>(sb - uf * KI) : 0;
+      const int64_t left = se - ut * KI;
+      r.ke = left < KI ? static_cast<int>(left) : KI;
+    }
+    return r;
+  };
 
   auto decode = [&](int64_t u) -> Unit {
     const int q = static_cast<int>(u / RB);
@@ -239,24 +323,26 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       const int mid = (lo + hi + 1) >> 1;
       if (t_pp[mid] <= q) lo = mid; else hi = mid - 1;
     }
-    const int np = q - t_pp[lo];
+    const int round = q - t_pp[lo];
     r.e = t_e[lo];
-    r.tok0 = t_tok0[lo] + np * G::kNMax;
-    const int left = t_ntok[lo] - np * G::kNMax;
-    r.ntok = left < G::kNMax ? left : G::kNMax;
+    const int left = t_ntok[lo] - round * span;
+    const int mr = left < span ? left : span;  // the round's tokens
+    const int share = rank_share(mr, ranks);
+    const int off = rank * share;
+    r.tok0 = t_tok0[lo] + round * span + off;
+    const int n = mr - off;
+    r.ntok = n < 0 ? 0 : (n < share ? n : share);
     return r;
   };
 
   if (warp == 0) {
     // =========================== TMA producer ===========================
-    const uint64_t policy = l2_policy_evict_first();
+    // ranks sharing a weight block read it from L2 after the first: keep it there meanwhile
+    const uint64_t policy = ranks > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    int64_t u = it_beg / KI;
-    int kk0 = static_cast<int>(it_beg - u * KI);
-    Unit un = it_beg < it_end ? decode(u) : Unit{};
     const int bbytes = n_tile * 128;
     auto issue_a = [&](int stg, const Unit& w, int kk) {
       uint8_t* st = smem + stg * G::kStage;
@@ -268,81 +354,76 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       }
     };
     auto issue_b = [&](int stg, const Unit& w, int kk) {
-      uint8_t* sb = smem + stg * G::kStage + G::kWBytes;
-      for (int j = 0; j < n_tile; j += 16) tma_load_2d(sb + j * 128, &tmB, &full[stg], kk * G::kKStage, w.tok0 + j);
+      uint8_t* sb_ = smem + stg * G::kStage + G::kWBytes;
+      for (int j = 0; j < n_tile; j += G::kBoxRows)
+        tma_load_2d(sb_ + j * 128, &tmB, &full[stg], kk * G::kKStage, w.tok0 + j);
+    };
+    // cursor over this column's stages: piece, its stage range and unit
+    struct Cursor {
+      int64_t p;
+      Piece pc;
+      int kk;
+      Unit un;
+    };
+    auto start = [&](Cursor& c) {
+      c.p = 0;
+      if (n_pieces > 0) {
+        c.pc = piece_of(0);
+        c.kk = c.pc.kb;
+        c.un = decode(c.pc.u);
+      }
+    };
+    auto advance = [&](Cursor& c) {
+      if (++c.kk == c.pc.ke && ++c.p < n_pieces) {
+        c.pc = piece_of(c.p);
+        c.kk = c.pc.kb;
+        c.un = decode(c.pc.u);
+      }
     };
     // weights first (they do not depend on the preceding kernel), token tiles after the wait
-    const int64_t npre = (it_end - it_beg) < G::kStages ? (it_end - it_beg) : G::kStages;
+    const int64_t npre = n_stages < G::kStages ? n_stages : G::kStages;
+    Cursor cur;
+    start(cur);
     {
-      int64_t pu = u;
-      int pk = kk0;
-      Unit pun = un;
+      Cursor pre = cur;
       for (int64_t q = 0; q < npre; ++q) {
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[q], G::kWBytes + bbytes);
-          issue_a(static_cast<int>(q), pun, pk);
+          issue_a(static_cast<int>(q), pre.un, pre.kk);
         }
-        if (++pk == KI && q + 1 < npre) {
-          pk = 0;
-          pun = decode(++pu);
-        }
+        if (q + 1 < npre) advance(pre);
       }
     }
     pdl_wait_predecessor();
     pdl_allow_successor();
     for (int64_t q = 0; q < npre; ++q) {
-      if (lane == 0) issue_b(static_cast<int>(q), un, kk0);
+      if (lane == 0) issue_b(static_cast<int>(q), cur.un, cur.kk);
       ++issued;
       if (++stage == G::kStages) {
         stage = 0;
         phase ^= 1;
       }
-      if (++kk0 == KI) {
-        kk0 = 0;
-        ++u;
-        if (it_beg + q + 1 < it_end) un = decode(u);
-      }
+      if (issued < n_stages) advance(cur);
     }
-    for (int64_t it = it_beg + npre; it < it_end && ok;) {
-      int64_t n = KI - kk0;
-      if (n > it_end - it) n = it_end - it;
-      if (n > kIssueGroup) n = kIssueGroup;
+    for (int64_t i = npre; i < n_stages; ++i) {
       bool drained = true;
-      if (lane == 0) {
-        int s = stage;
-        uint32_t ph = phase;
-        for (int64_t q = 0; q < n && drained; ++q) {
-          drained = mbar_wait(&empty[s], ph ^ 1);
-          if (++s == G::kStages) {
-            s = 0;
-            ph ^= 1;
-          }
-        }
-      }
+      if (lane == 0) drained = mbar_wait(&empty[stage], phase ^ 1);
       drained = __shfl_sync(0xffffffffu, drained, 0);
       if (!drained) {
         ok = false;
         break;
       }
-      for (int64_t q = 0; q < n; ++q) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], G::kWBytes + bbytes);
-          issue_a(stage, un, kk0 + static_cast<int>(q));
-          issue_b(stage, un, kk0 + static_cast<int>(q));
-        }
-        ++issued;
-        if (++stage == G::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[stage], G::kWBytes + bbytes);
+        issue_a(stage, cur.un, cur.kk);
+        issue_b(stage, cur.un, cur.kk);
       }
-      it += n;
-      kk0 += static_cast<int>(n);
-      if (kk0 == KI && it < it_end) {
-        kk0 = 0;
-        ++u;
-        un = decode(u);
+      ++issued;
+      if (++stage == G::kStages) {
+        stage = 0;
+        phase ^= 1;
       }
+      if (i + 1 < n_stages) advance(cur);
     }
     if (lane == 0) {  // never leave copies in flight
       const int64_t n = issued < G::kStages ? issued : G::kStages;
@@ -368,47 +449,43 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
       bool ok = true;
       int stage = 0;
       uint32_t phase = 0;
-      int64_t piece = 0;
-      int kk = static_cast<int>(it_beg % KI);
       const uint32_t smem_base = smem_addr(smem);
       const uint32_t idesc = umma_idesc_bf16_m128(n_tile);
-      for (int64_t it = it_beg; it < it_end; ++it) {
-        const bool first = (it == it_beg) || (kk == 0);
-        const bool last = (kk == KI - 1) || (it == it_end - 1);
-        const int b = static_cast<int>(piece & 1);
-        if (first && ok) {
-          if (!mbar_wait(&acc_empty[b], static_cast<uint32_t>(((piece >> 1) & 1) ^ 1))) {
+      for (int64_t piece = 0; piece < n_pieces; ++piece) {
+        const Piece pc = piece_of(piece);
+        const int b = G::kAccBufs == 2 ? static_cast<int>(piece & 1) : 0;
+        for (int kk = pc.kb; kk < pc.ke; ++kk) {
+          const bool first = kk == pc.kb;
+          if (first && ok) {
+            if (!mbar_wait(&acc_empty[b], static_cast<uint32_t>(((piece / G::kAccBufs) & 1) ^ 1))) {
+              ok = false;
+              atomicExch(args.status, kStatusWaitEmptyTimeout);
+            }
+            tc_fence_after_sync();
+          }
+          if (ok && !mbar_wait(&full[stage], phase)) {
             ok = false;
-            atomicExch(args.status, kStatusWaitEmptyTimeout);
+            atomicExch(args.status, kStatusWaitFullTimeout);
           }
-          tc_fence_after_sync();
-        }
-        if (ok && !mbar_wait(&full[stage], phase)) {
-          ok = false;
-          atomicExch(args.status, kStatusWaitFullTimeout);
-        }
-        if (ok) {
-          tc_fence_after_sync();
-          const uint32_t st = smem_base + stage * G::kStage;
-          const uint32_t d = tmem_base + b * G::kAccCols;
+          if (ok) {
+            tc_fence_after_sync();
+            const uint32_t st = smem_base + stage * G::kStage;
+            const uint32_t d = tmem_base + b * G::kAccCols;
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint64_t db = umma_desc_sw128(st + G::kWBytes + 32 * s);
-            const bool acc = !(first && s == 0);
-            umma_bf16(d, umma_desc_sw128(st + 32 * s), db, idesc, acc);
-            if (kGateUp) umma_bf16(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, idesc, acc);
+            for (int s = 0; s < 4; ++s) {
+              const uint64_t db = umma_desc_sw128(st + G::kWBytes + 32 * s);
+              const bool acc = !(first && s == 0);
+              umma_bf16(d, umma_desc_sw128(st + 32 * s), db, idesc, acc);
+              if (kGateUp) umma_bf16(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, idesc, acc);
+            }
+          }
+          umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == G::kStages) {
+            stage = 0;
+            phase ^= 1;
           }
         }
-        umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
-        if (last) {
-          umma_commit(&acc_full[b]);
-          ++piece;
-        }
-        if (++stage == G::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (++kk == KI) kk = 0;
+        umma_commit(&acc_full[b]);
       }
       // every issued MMA has finished before TMEM is released
       umma_commit(mma_done);
@@ -423,24 +500,18 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;         // weight row within the 128-row block
     bool ok = true;
-    int64_t piece = 0;
-    const int64_t first_unit = it_beg / KI;
-    int64_t u = first_unit;
-    for (int64_t it = it_beg; it < it_end;) {
-      // one piece: stages [it, pe) of unit u
-      const int64_t ub = u * KI;
-      const int64_t ue = ub + KI;
-      const int64_t pe = ue < it_end ? ue : it_end;
-      const Unit un = decode(u);
-      const int b = static_cast<int>(piece & 1);
-      if (ok && !mbar_wait(&acc_full[b], static_cast<uint32_t>((piece >> 1) & 1))) {
+    for (int64_t piece = 0; piece < n_pieces; ++piece) {
+      const Piece pc = piece_of(piece);
+      const Unit un = decode(pc.u);
+      const int b = G::kAccBufs == 2 ? static_cast<int>(piece & 1) : 0;
+      if (ok && !mbar_wait(&acc_full[b], static_cast<uint32_t>((piece / G::kAccBufs) & 1))) {
         ok = false;
         atomicExch(args.status, kStatusWaitFullTimeout);
       }
       tc_fence_after_sync();
       const int npad = ((un.ntok + 15) >> 4) * 16;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * G::kAccCols;
-      const bool whole = (ub >= it_beg) && (ue <= it_end);
+      const bool whole = pc.kb == 0 && pc.ke == KI;
 
       auto emit = [&](int n0, const float (&g)[16], const float (&v)[16]) {
         // g: gate (or down) accumulators of tokens n0..n0+15, v: up accumulators
@@ -491,12 +562,14 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
       } else {
-        // unit split across CTAs: publish this piece's fp32 accumulators, last arriver reduces
-        auto cta_of = [&](int64_t i) -> int64_t { return ((i + 1) * NC - 1) / W; };
-        const int64_t c_first = cta_of(ub);
-        const int64_t c_last = cta_of(ue - 1);
-        const int slot = (u == first_unit) ? 0 : 1;
-        float* mine = args.partials + (cta * 2 + slot) * static_cast<int64_t>(kPartialFloats) + etid;
+        // unit split across columns: publish this piece's fp32 accumulators, last arriver reduces.
+        // Stage indices here count the stream-K part only (units D.. of the launch).
+        const int64_t ut = pc.u - D;
+        auto col_of = [&](int64_t i) -> int64_t { return ((i + 1) * NC - 1) / Wt; };
+        const int64_t c_first = col_of(ut * KI);  // columns whose ranges hold this unit's stages
+        const int64_t c_last = col_of(ut * KI + KI - 1);
+        const int slot = piece == nW ? 0 : 1;    // a column's first stream-K piece, or its last
+        float* mine = args.partials + (cta * 2 + slot) * args.partial_stride + etid;
         for (int n0 = 0; n0 < npad; n0 += 16) {
           float g[16], v[16];
           load_acc(n0, g, v);
@@ -512,9 +585,10 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
         __threadfence();
         named_bar_sync(1, kEpiThreads);
         if (etid == 0) {
-          const int old = atomicAdd(&args.counters[c_first], 1);
+          int32_t* counter = &args.counters[c_first * ranks + rank];
+          const int old = atomicAdd(counter, 1);
           const int last = (old == static_cast<int>(c_last - c_first));
-          if (last) args.counters[c_first] = 0;
+          if (last) *counter = 0;
           s_misc[8] = last;
         }
         named_bar_sync(1, kEpiThreads);
@@ -525,9 +599,9 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) g[j] = v[j] = 0.0f;
             for (int64_t c = c_first; c <= c_last; ++c) {
-              const int64_t c_first_unit = (c * W / NC) / KI;
-              const int cslot = (u == c_first_unit) ? 0 : 1;
-              const float* src = args.partials + (c * 2 + cslot) * static_cast<int64_t>(kPartialFloats) + etid;
+              const int64_t c_first_unit = (c * Wt / NC) / KI;
+              const int cslot = (ut == c_first_unit) ? 0 : 1;
+              const float* src = args.partials + ((c * ranks + rank) * 2 + cslot) * args.partial_stride + etid;
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 g[j] += __ldcg(src + (n0 + j) * kEpiThreads);
@@ -539,9 +613,6 @@ __global__ void __launch_bounds__(Geo<kGateUp>::kThreads, 1)
         }
         named_bar_sync(1, kEpiThreads);  // s_misc[8] is reused by the next piece
       }
-      ++piece;
-      it = pe;
-      ++u;
     }
   }
 

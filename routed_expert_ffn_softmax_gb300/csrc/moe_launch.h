@@ -44,10 +44,23 @@ cudaError_t launch_combine(const float* Y, const int32_t* inv_pos, const float* 
 cudaError_t launch_gather_f16(const uint16_t* x, int T, int H, int P, const int32_t* sorted_token, uint16_t* xg16,
                               float* xg_scale, int num_sms, cudaStream_t stream);
 
-// fp32 slots per CTA the expert kernels' stream-K partials need (the larger of the two kernel
-// families), and the CTA capacity the workspace provides.
+// fp32 slots per CTA the expert kernels' stream-K partials need at 64-token passes (the larger of
+// the two kernel families), and the CTA capacity the workspace provides.
 constexpr int kPartialSlotFloats = 16384;
 constexpr int kPartialCtas = 256;
+
+// BF16 expert kernels: tokens per pass (64, 128 or 256) of gate+up and of down, and the fp32 per
+// stream-K partial slot a pass size needs (128 rows x the accumulator columns: gate and up, or down).
+struct PassTokens {
+  int gate_up, down;
+};
+// The passes a BF16 launch of P assignments over E experts takes: by the mean tokens per expert,
+// unless set_pass_tokens forced a size. The workspace layout and the launch both call it.
+PassTokens pass_tokens(int64_t P, int E);
+void set_pass_tokens(int gate_up, int down);  // 0 = by batch shape
+inline int64_t partial_slot_floats(int pass_tokens, bool gate_up) {
+  return 128LL * (gate_up ? 2 : 1) * pass_tokens;
+}
 
 // Grouped expert FFN (gate+up then down) over an expert-sorted token block.
 struct ExpertFfnPlan {
@@ -76,7 +89,10 @@ struct ExpertFfnPlan {
   bool xg16_ready;    // INT8: xg16 / xg_scale were written by the gather (xg is then not read)
   float* h_scale;     // [P]
   float* Y;           // [P, H]
-  float* partials;    // stream-K partial slots
+  float* partials;    // stream-K partial slots, [kPartialCtas][2][partial_slot]
+  int64_t partial_slot;  // fp32 per slot (at least kPartialSlotFloats)
+  PassTokens passes;     // BF16: tokens per pass; a size whose partials need more than partial_slot
+                         // falls back to 64
   int32_t* counters;  // zeroed, kMaxCtas entries
   int32_t* status;
   int num_ctas;
