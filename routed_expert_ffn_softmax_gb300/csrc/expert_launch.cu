@@ -131,43 +131,90 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, int K, int P, uint16_t* dst,
                     src_prefetch_bytes);
 }
 
-template <bool kGateUp, int kN>
-cudaError_t prepare_tc_kernel() {
+// Per device: the shared-memory attribute set, and (CTA pairs) the clusters that can be resident
+// at once (a persistent grid must not be larger, or the late CTAs would run after the others).
+template <bool kGateUp, int kN, bool kPair>
+cudaError_t prepare_tc_kernel(int* resident) {
+  using G = tc::Geo<kGateUp, kN, kPair>;
   constexpr int kMaxDev = 64;
-  static std::atomic<bool> done[kMaxDev];
+  static std::atomic<int> cache[kMaxDev];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp, kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::Geo<kGateUp, kN>::kSmem);
-  if (e == cudaSuccess && dev < kMaxDev) done[dev].store(true, std::memory_order_release);
-  return e;
+  if (dev < kMaxDev) {
+    const int c = cache[dev].load(std::memory_order_acquire);
+    if (c > 0) {
+      *resident = c;
+      return cudaSuccess;
+    }
+  }
+  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp, kN, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           G::kSmem);
+  if (e != cudaSuccess) return e;
+  int n = kPartialCtas;
+  if (kPair) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kPartialCtas);
+    cfg.blockDim = dim3(G::kThreads);
+    cfg.dynamicSmemBytes = G::kSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, tc::expert_tc_kernel<kGateUp, kN, kPair>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorNotSupported;
+  }
+  if (dev < kMaxDev) cache[dev].store(n, std::memory_order_release);
+  *resident = n;
+  return cudaSuccess;
 }
 
-template <bool kGateUp, int kN>
+template <bool kGateUp, int kN, bool kPair>
 cudaError_t launch_tc_kernel(const CUtensorMap& a0, const CUtensorMap& a1, const void* tokens, int K, int P,
                              const tc::Args& args, int num_ctas, cudaStream_t s) {
-  using G = tc::Geo<kGateUp, kN>;
+  using G = tc::Geo<kGateUp, kN, kPair>;
   CUtensorMap tb;
   if (!encode_tokens(&tb, tokens, K, P, false, G::kBoxRows)) return cudaErrorInvalidValue;
-  cudaError_t e = prepare_tc_kernel<kGateUp, kN>();
+  int resident = 0;
+  cudaError_t e = prepare_tc_kernel<kGateUp, kN, kPair>(&resident);
   if (e != cudaSuccess) return e;
-  return launch_pdl(tc::expert_tc_kernel<kGateUp, kN>, dim3(num_ctas), dim3(G::kThreads), G::kSmem, s, a0, a1, tb,
-                    args);
+  if (!kPair)
+    return launch_pdl(tc::expert_tc_kernel<kGateUp, kN, kPair>, dim3(num_ctas), dim3(G::kThreads), G::kSmem, s, a0,
+                      a1, tb, args);
+  int pairs = num_ctas / 2 < resident ? num_ctas / 2 : resident;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(G::kThreads);
+  cfg.dynamicSmemBytes = G::kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, tc::expert_tc_kernel<kGateUp, kN, kPair>, a0, a1, tb, args);
 }
 
-// Launch the kernel of `pass` tokens per pass (64, 128 or 256), or of 64 where its partial slots
-// would not fit in `slot` fp32.
+// Launch the kernel of `pass` tokens per pass (64 on single CTAs; 128 or 256 on CTA pairs), or of
+// 64 where its partial slots would not fit in `slot` fp32.
 template <bool kGateUp>
 cudaError_t launch_tc_pass(int pass, int64_t slot, const CUtensorMap& a0, const CUtensorMap& a1, const void* tokens,
                            int K, int P, tc::Args args, int num_ctas, cudaStream_t s) {
   if (partial_slot_floats(pass, kGateUp) > slot) pass = 64;
   args.partial_stride = partial_slot_floats(pass, kGateUp);
-  if (pass == 256) return launch_tc_kernel<kGateUp, 256>(a0, a1, tokens, K, P, args, num_ctas, s);
-  if (pass == 128) return launch_tc_kernel<kGateUp, 128>(a0, a1, tokens, K, P, args, num_ctas, s);
+  if (pass == 256) return launch_tc_kernel<kGateUp, 256, true>(a0, a1, tokens, K, P, args, num_ctas, s);
+  if (pass == 128) return launch_tc_kernel<kGateUp, 128, true>(a0, a1, tokens, K, P, args, num_ctas, s);
   args.partial_stride = kPartialSlotFloats;
-  return launch_tc_kernel<kGateUp, 64>(a0, a1, tokens, K, P, args, num_ctas, s);
+  return launch_tc_kernel<kGateUp, 64, false>(a0, a1, tokens, K, P, args, num_ctas, s);
 }
 
 std::atomic<int> g_pass_gate_up{0}, g_pass_down{0};

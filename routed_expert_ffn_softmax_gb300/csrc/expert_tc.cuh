@@ -29,20 +29,33 @@ namespace tc {
 constexpr int kEpiThreads = 128;    // warps 2..5
 constexpr int kTable = 256;
 constexpr int kPartialFloats = 16384;  // one INT8 pair-kernel CTA slot: 128 rows x 128 accumulator columns
-constexpr int kMaxRanks = 4;           // CTAs sharing one weight block (BF16, 128- and 256-token passes)
+constexpr int kMaxRanks = 8;           // passes sharing one weight block (BF16, 128- and 256-token passes)
 
 // kN: tokens per pass (64, 128 or 256; the launch picks it from the batch's tokens per expert). An
 // expert with more tokens than a pass streams its weights once per pass, so larger passes read the
 // weights fewer times when experts see many tokens (prefill-sized batches); smaller passes leave room
 // for more stages at decode sizes.
-template <bool kGateUp, int kN = 64>
+//
+// kPair: the pass runs on a CTA pair (a cluster of two) with tcgen05.mma cta_group::2, M = 256: each
+// CTA holds 128 weight rows of a 256-row block and half of the pass's token rows, and the even CTA
+// issues MMAs that read both CTAs' tiles and write each CTA's 128 rows into its own TMEM. Per CTA a
+// stage then carries half the token bytes for the same tensor work, which is what bounds these
+// kernels at prefill sizes (bytes in flight per SM against L2 latency, measured on GB300).
+template <bool kGateUp, int kN = 64, bool kPair = false>
 struct Geo {
   static constexpr int kThreads = 192;
+  static constexpr int kCtas = kPair ? 2 : 1;               // CTAs per pass
+  static constexpr int kUnitRows = 128 * kCtas;             // weight rows per unit
   static constexpr int kNMax = kN;                          // tokens per pass
   static constexpr int kKStage = 64;                        // reduction elements per stage
-  static constexpr int kWBytes = kGateUp ? 32768 : 16384;   // weight bytes per stage
-  static constexpr int kBBytes = kNMax * 128;               // token tile: kN rows x 64 elements x 2 B
-  static constexpr int kBoxRows = kN >= 128 ? 32 : 16;      // token rows per TMA box
+  static constexpr int kWBytes = kGateUp ? 32768 : 16384;   // this CTA's weight bytes per stage
+  static constexpr int kBRows = kN / kCtas;                 // this CTA's token rows per stage, at most
+  static constexpr int kBBytes = kBRows * 128;              // token tile: kBRows rows x 64 elements x 2 B
+  // Token rows per TMA box. A pair loads its whole token slot as one box every stage (rows past the
+  // pass's own are never read): measured on GB300, TMA moves 2 KB boxes from L2 at a quarter of the
+  // rate of 16 KB ones, and the token tile is the larger part of a stage at these sizes.
+  static constexpr int kBoxRows = kPair ? kBRows : (kN >= 128 ? 32 : 16);
+  static constexpr int kTileRound = kPair ? 32 : kBoxRows;  // the launch's token tile is a multiple
   static constexpr int kStage = kWBytes + kBBytes;
   static constexpr int kTableBytes = (4 * kTable + 32) * 4;
   // as many stages as fit (down at 64-token passes: 9; measured on GB300 7: -0.4%, 9: +0.3%)
@@ -54,6 +67,7 @@ struct Geo {
   static constexpr int kSmem = kStages * kStage + kBarBytes + kTableBytes;
   static constexpr int64_t kPartialSlot = 128LL * kAccCols;     // fp32 per stream-K partial slot
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
+  static_assert(kNMax % 32 == 0, "the gate+up epilogue reads 32 accumulator columns at a time");
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
   static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
@@ -136,6 +150,46 @@ __device__ __forceinline__ int load_schedule(const Args& args, int* t_e, int* t_
   return A;
 }
 
+// SiLU(g) * u = g * u / (1 + e^-g), with e^-g = 2^(-g log2 e) and the reciprocal from the hardware's
+// approximate instructions (PTX ex2.approx.ftz, rcp.approx.ftz: relative errors near 2^-22 and 2^-23,
+// far below the bf16 rounding of h that follows). g -> -inf gives -0, g -> +inf gives g * u. The
+// exact division and exponential cost the single epilogue warp per TMEM lane quarter a quarter of
+// the gate+up kernel's time at prefill sizes (measured on GB300), while its MMAs wait for the
+// accumulator.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return g * r * u;
+}
+
+// 32 consecutive fp32 TMEM columns at each of two addresses of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
+  uint32_t r[32], q[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]),
+        "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]), "=r"(q[16]),
+        "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]), "=r"(q[24]),
+        "=r"(q[25]), "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
+      : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(q[i]);
+  }
+}
+
 // A rank's share of a round of mr tokens split over g ranks: a multiple of 16.
 __device__ __forceinline__ int rank_share(int mr, int g) { return ((mr + g - 1) / g + 15) / 16 * 16; }
 
@@ -145,11 +199,53 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
   return p;
 }
 
-template <bool kGateUp, int kN>
-__global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
+// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B, fp32 D, M = 256 (a CTA pair),
+// N = n (a multiple of 16, each CTA holding n / 2 rows of B).
+__device__ __forceinline__ uint32_t umma_idesc_bf16_m256(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (16u << 24);
+}
+
+// Pair MMA issued by the even CTA: D (+)= A * B^T, A and B from the same shared-memory offsets in
+// both CTAs (each CTA's 128 rows of A, and its half of B's rows), each CTA's D rows in its TMEM.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
+// Shared::cluster address of the mbarrier at this offset in the pair's even CTA.
+__device__ __forceinline__ uint32_t leader_barrier(uint64_t* bar) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(bar)), "r"(0));
+  return remote;
+}
+
+// Tiled loads into this CTA's shared memory whose completion is counted on the even CTA's
+// mbarrier (`bar`, a shared::cluster address): both CTAs' tiles of a stage complete one barrier.
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+template <bool kGateUp, int kN, bool kPair>
+__global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const Args args) {
-  using G = Geo<kGateUp, kN>;
+  using G = Geo<kGateUp, kN, kPair>;
   constexpr int kThreads = G::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStage);
@@ -174,8 +270,8 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
       mbar_init(&empty[s], 1);  // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);   // MMA commit
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_full[b], 1);              // MMA commit
+      mbar_init(&acc_empty[b], 4 * G::kCtas);  // one arrival per epilogue warp (of both CTAs of a pair)
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -185,7 +281,10 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
     if (kGateUp) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, G::kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_alloc_pair(tmem_slot, G::kTmemCols);
+    else tmem_alloc(tmem_slot, G::kTmemCols);
+  }
 
   // ---- schedule tables. They are read before waiting for the preceding kernel: every kernel of
   // this library waits for its predecessor before it lets its successor start, so all work two
@@ -212,7 +311,8 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
     if (G::kNMax >= 128) {
       g = (mx + G::kNMax - 1) / G::kNMax;
       g = g < 1 ? 1 : (g > kMaxRanks ? kMaxRanks : g);
-      g = g < static_cast<int>(gridDim.x) ? g : static_cast<int>(gridDim.x);
+      const int units = static_cast<int>(gridDim.x) / G::kCtas;
+      g = g < units ? g : units;
     }
     const int span = g * G::kNMax;  // tokens of an expert per round
     // rounds per active expert and their prefix sum: 8 per lane, then a warp scan
@@ -253,19 +353,22 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
     }
     m = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<uint32_t>(m)));
     if (lane == 0) {
-      s_misc[12] = (m + G::kBoxRows - 1) / G::kBoxRows * G::kBoxRows;
+      s_misc[12] = (m + G::kTileRound - 1) / G::kTileRound * G::kTileRound;
       s_misc[13] = g;
     }
   }
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // both CTAs' barriers are initialised before any cross-CTA use
   const uint32_t tmem_base = *tmem_slot;
-  const int n_tile = s_misc[12];  // token rows per stage and MMA columns, 16..kNMax
+  const int n_tile = s_misc[12];  // MMA columns (token rows of the pass's tile), 16..kNMax
+  const int b_rows = n_tile / G::kCtas;  // token rows this CTA loads per stage
   const int ranks = s_misc[13];   // CTAs per weight block
   const int span = ranks * G::kNMax;
 
-  // Work split over columns of `ranks` CTAs (blockIdx = column * ranks + rank): the CTAs of a column
-  // take the same stages of the same units, each with its rank's share of the tokens. A unit is one
-  // 128-row block of one expert round (KI reduction stages).
+  // Work split over columns of `ranks` passes (blockIdx = (column * ranks + rank) * kCtas + half, half
+  // the CTA's place in its pair): the passes of a column take the same stages of the same units, each
+  // with its rank's share of the tokens. A unit is one kUnitRows-row block of one expert round (KI
+  // reduction stages).
   //  * 64-token passes (decode-sized batches): stream-K over all units, each column a contiguous
   //    range of stages; a unit split between columns is finished by the last one to arrive.
   //  * 128- and 256-token passes with at least two units per column: whole units in waves
@@ -274,13 +377,16 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
   //    past; the last NC to 2 NC units are split stream-K as above. Contiguous ranges over every
   //    expert kept all token rows live at once and re-read them from DRAM (4x the down weights at
   //    512 tokens per expert, measured on GB300).
-  const int RB = (args.rows + 127) / 128;
+  const int RB = (args.rows + G::kUnitRows - 1) / G::kUnitRows;
   const int KI = (args.K + G::kKStage - 1) / G::kKStage;
   const int64_t U = static_cast<int64_t>(t_pp[A]) * RB;
-  const int64_t ncols = static_cast<int64_t>(gridDim.x) / ranks;
-  const int64_t col = blockIdx.x / ranks;
-  const int rank = static_cast<int>(blockIdx.x % ranks);
+  const int64_t pass_id = blockIdx.x / G::kCtas;
+  const int half = kPair ? static_cast<int>(cluster_cta_rank()) : 0;
+  const int64_t ncols = static_cast<int64_t>(gridDim.x / G::kCtas) / ranks;
+  const int64_t col = pass_id / ranks;
+  const int rank = static_cast<int>(pass_id % ranks);
   const int64_t cta = blockIdx.x;
+  const bool leader = half == 0;  // issues the MMAs of a pair (every CTA when not paired)
   const bool waves = G::kNMax >= 128 && U >= 2 * ncols;
   const int64_t NC = waves ? ncols : (U * KI < ncols ? U * KI : ncols);
   const int64_t nW = (waves && col < NC) ? U / NC - 1 : 0;          // whole-unit waves of this column
@@ -343,20 +449,30 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    const int bbytes = n_tile * 128;
+    const int bbytes = kPair ? G::kBBytes : b_rows * 128;
+    // both CTAs' bytes of a stage complete the even CTA's barrier (kCtas x this CTA's share)
+    const uint32_t stage_tx = G::kCtas * (G::kWBytes + bbytes);
     auto issue_a = [&](int stg, const Unit& w, int kk) {
       uint8_t* st = smem + stg * G::kStage;
-      if (kGateUp) {
-        tma_load_3d(st, &tmA0, &full[stg], kk * G::kKStage, w.rb * 128, w.e, policy);
-        tma_load_3d(st + 16384, &tmA1, &full[stg], kk * G::kKStage, w.rb * 128, w.e, policy);
+      const int row = w.rb * G::kUnitRows + half * 128;
+      if constexpr (kPair) {
+        const uint32_t bar = leader_barrier(&full[stg]);
+        tma_load_3d_pair(st, &tmA0, bar, kk * G::kKStage, row, w.e, policy);
+        if (kGateUp) tma_load_3d_pair(st + 16384, &tmA1, bar, kk * G::kKStage, row, w.e, policy);
       } else {
-        tma_load_3d(st, &tmA0, &full[stg], kk * G::kKStage, w.rb * 128, w.e, policy);
+        tma_load_3d(st, &tmA0, &full[stg], kk * G::kKStage, row, w.e, policy);
+        if (kGateUp) tma_load_3d(st + 16384, &tmA1, &full[stg], kk * G::kKStage, row, w.e, policy);
       }
     };
     auto issue_b = [&](int stg, const Unit& w, int kk) {
       uint8_t* sb_ = smem + stg * G::kStage + G::kWBytes;
-      for (int j = 0; j < n_tile; j += G::kBoxRows)
-        tma_load_2d(sb_ + j * 128, &tmB, &full[stg], kk * G::kKStage, w.tok0 + j);
+      const int r0 = w.tok0 + half * b_rows;
+      if constexpr (kPair) {
+        tma_load_2d_pair(sb_, &tmB, leader_barrier(&full[stg]), kk * G::kKStage, r0);
+      } else {
+        for (int j = 0; j < b_rows; j += G::kBoxRows)
+          tma_load_2d(sb_ + j * 128, &tmB, &full[stg], kk * G::kKStage, r0 + j);
+      }
     };
     // cursor over this column's stages: piece, its stage range and unit
     struct Cursor {
@@ -388,7 +504,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
       Cursor pre = cur;
       for (int64_t q = 0; q < npre; ++q) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[q], G::kWBytes + bbytes);
+          if (leader) mbar_arrive_expect_tx(&full[q], stage_tx);
           issue_a(static_cast<int>(q), pre.un, pre.kk);
         }
         if (q + 1 < npre) advance(pre);
@@ -414,7 +530,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
         break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full[stage], G::kWBytes + bbytes);
+        if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
         issue_a(stage, cur.un, cur.kk);
         issue_b(stage, cur.un, cur.kk);
       }
@@ -425,7 +541,9 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
       }
       if (i + 1 < n_stages) advance(cur);
     }
-    if (lane == 0) {  // never leave copies in flight
+    // never leave copies in flight: the even CTA's barriers count both CTAs' copies (the odd CTA's
+    // are covered by the cluster barrier before exit, which the even CTA reaches after this)
+    if (lane == 0 && leader) {
       const int64_t n = issued < G::kStages ? issued : G::kStages;
       int s = stage;
       uint32_t ph = phase;
@@ -439,18 +557,26 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
           break;
         }
       }
-      if (!ok) atomicExch(args.status, kStatusWaitEmptyTimeout);
     }
+    if (lane == 0 && !ok) atomicExch(args.status, kStatusWaitEmptyTimeout);
   } else if (warp == 1) {
     // =========================== MMA issuer ===========================
     pdl_wait_predecessor();
     pdl_allow_successor();
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       bool ok = true;
       int stage = 0;
       uint32_t phase = 0;
       const uint32_t smem_base = smem_addr(smem);
-      const uint32_t idesc = umma_idesc_bf16_m128(n_tile);
+      const uint32_t idesc = kPair ? umma_idesc_bf16_m256(n_tile) : umma_idesc_bf16_m128(n_tile);
+      auto mma = [&](uint32_t d, uint64_t a, uint64_t b_, bool acc) {
+        if constexpr (kPair) umma_bf16_pair(d, a, b_, idesc, acc);
+        else umma_bf16(d, a, b_, idesc, acc);
+      };
+      auto commit = [&](uint64_t* bar) {  // arrives in both CTAs of a pair
+        if constexpr (kPair) umma_commit_pair(bar);
+        else umma_commit(bar);
+      };
       for (int64_t piece = 0; piece < n_pieces; ++piece) {
         const Piece pc = piece_of(piece);
         const int b = G::kAccBufs == 2 ? static_cast<int>(piece & 1) : 0;
@@ -475,20 +601,20 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
             for (int s = 0; s < 4; ++s) {
               const uint64_t db = umma_desc_sw128(st + G::kWBytes + 32 * s);
               const bool acc = !(first && s == 0);
-              umma_bf16(d, umma_desc_sw128(st + 32 * s), db, idesc, acc);
-              if (kGateUp) umma_bf16(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, idesc, acc);
+              mma(d, umma_desc_sw128(st + 32 * s), db, acc);
+              if (kGateUp) mma(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, acc);
             }
           }
-          umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          commit(&empty[stage]);  // frees the stage (of both CTAs) once these MMAs have read it
           if (++stage == G::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
-        umma_commit(&acc_full[b]);
+        commit(&acc_full[b]);
       }
       // every issued MMA has finished before TMEM is released
-      umma_commit(mma_done);
+      commit(mma_done);
       if (!mbar_wait(mma_done, 0)) atomicExch(args.status, kStatusDrainTimeout);
     }
     __syncwarp();
@@ -500,6 +626,11 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;         // weight row within the 128-row block
     bool ok = true;
+    // the accumulator buffer is free again: tell the CTA that issues the MMAs
+    auto release_acc = [&](uint64_t* bar) {
+      if (kPair && !leader) mbar_arrive_cta(bar, 0);
+      else mbar_arrive(bar);
+    };
     for (int64_t piece = 0; piece < n_pieces; ++piece) {
       const Piece pc = piece_of(piece);
       const Unit un = decode(pc.u);
@@ -516,20 +647,18 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
       auto emit = [&](int n0, const float (&g)[16], const float (&v)[16]) {
         // g: gate (or down) accumulators of tokens n0..n0+15, v: up accumulators
         if constexpr (kGateUp) {
-          const int i = un.rb * 128 + r;
+          const int i = un.rb * G::kUnitRows + half * 128 + r;
           if (i < args.rows) {
             __nv_bfloat16* h = static_cast<__nv_bfloat16*>(args.out);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int n = n0 + j;
-              if (n < un.ntok) {
-                const float silu = g[j] / (1.0f + expf(-g[j]));
-                h[static_cast<int64_t>(un.tok0 + n) * args.out_ld + i] = __float2bfloat16_rn(silu * v[j]);
-              }
+              if (n < un.ntok)
+                h[static_cast<int64_t>(un.tok0 + n) * args.out_ld + i] = __float2bfloat16_rn(silu_mul(g[j], v[j]));
             }
           }
         } else {
-          const int row = un.rb * 128 + r;
+          const int row = un.rb * G::kUnitRows + half * 128 + r;
           if (row < args.rows) {
             float* y = static_cast<float*>(args.out);
 #pragma unroll
@@ -552,7 +681,23 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
         if (kGateUp) tmem_ld16(tb + G::kNMax + n0, v);
       };
 
-      if (whole) {
+      if (whole && kGateUp) {
+        // 32 tokens per TMEM round trip (columns past npad, up to kNMax, are read and not stored)
+        for (int n0 = 0; n0 < npad; n0 += 32) {
+          float g[32], v[32];
+          if (ok) {
+            tmem_ld32x2(tb + n0, tb + G::kNMax + n0, g, v);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] = v[j] = 0.0f;
+          }
+          emit(n0, reinterpret_cast<const float(&)[16]>(g[0]), reinterpret_cast<const float(&)[16]>(v[0]));
+          emit(n0 + 16, reinterpret_cast<const float(&)[16]>(g[16]), reinterpret_cast<const float(&)[16]>(v[16]));
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) release_acc(&acc_empty[b]);
+      } else if (whole) {
         for (int n0 = 0; n0 < npad; n0 += 16) {
           float g[16], v[16];
           load_acc(n0, g, v);
@@ -560,7 +705,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        if (lane == 0) release_acc(&acc_empty[b]);
       } else {
         // unit split across columns: publish this piece's fp32 accumulators, last arriver reduces.
         // Stage indices here count the stream-K part only (units D.. of the launch).
@@ -581,11 +726,11 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);  // TMEM buffer free again
+        if (lane == 0) release_acc(&acc_empty[b]);  // TMEM buffer free again
         __threadfence();
         named_bar_sync(1, kEpiThreads);
         if (etid == 0) {
-          int32_t* counter = &args.counters[c_first * ranks + rank];
+          int32_t* counter = &args.counters[(c_first * ranks + rank) * G::kCtas + half];
           const int old = atomicAdd(counter, 1);
           const int last = (old == static_cast<int>(c_last - c_first));
           if (last) *counter = 0;
@@ -601,7 +746,8 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
             for (int64_t c = c_first; c <= c_last; ++c) {
               const int64_t c_first_unit = (c * Wt / NC) / KI;
               const int cslot = (ut == c_first_unit) ? 0 : 1;
-              const float* src = args.partials + ((c * ranks + rank) * 2 + cslot) * args.partial_stride + etid;
+              const int64_t src_cta = (c * ranks + rank) * G::kCtas + half;
+              const float* src = args.partials + (src_cta * 2 + cslot) * args.partial_stride + etid;
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 g[j] += __ldcg(src + (n0 + j) * kEpiThreads);
@@ -616,11 +762,16 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN>::kThreads, 1)
     }
   }
 
-  // ---- teardown: every role has finished; warp 1 releases TMEM
+  // ---- teardown: every role has finished (of both CTAs of a pair: the even CTA's issuer has seen its
+  // last MMAs complete and no copy or arrival targets either CTA any more); warp 1 releases TMEM
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, G::kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, G::kTmemCols);
+    else tmem_dealloc(tmem_base, G::kTmemCols);
+  }
 }
 
 }  // namespace tc
