@@ -26,7 +26,7 @@
 namespace moe {
 namespace tc {
 
-constexpr int kEpiThreads = 128;    // warps 2..5
+constexpr int kRows = 128;          // weight rows of one CTA's accumulators (TMEM lanes)
 constexpr int kTable = 256;
 constexpr int kPartialFloats = 16384;  // one INT8 pair-kernel CTA slot: 128 rows x 128 accumulator columns
 constexpr int kMaxRanks = 8;           // passes sharing one weight block (BF16, 128- and 256-token passes)
@@ -43,7 +43,12 @@ constexpr int kMaxRanks = 8;           // passes sharing one weight block (BF16,
 // kernels at prefill sizes (bytes in flight per SM against L2 latency, measured on GB300).
 template <bool kGateUp, int kN = 64, bool kPair = false>
 struct Geo {
-  static constexpr int kThreads = 192;
+  // Epilogue warps: on pairs two per TMEM lane quarter, taking alternate groups of accumulator
+  // columns, so a unit's accumulators drain in half the time (gate+up holds one accumulator buffer
+  // at 256-token passes, and its MMAs wait for the drain); at 64-token passes one per quarter
+  // (measured on GB300, eight cost decode batches 2-3%).
+  static constexpr int kEpiWarps = kPair ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kCtas = kPair ? 2 : 1;               // CTAs per pass
   static constexpr int kUnitRows = 128 * kCtas;             // weight rows per unit
   static constexpr int kNMax = kN;                          // tokens per pass
@@ -271,7 +276,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);              // MMA commit
-      mbar_init(&acc_empty[b], 4 * G::kCtas);  // one arrival per epilogue warp (of both CTAs of a pair)
+      mbar_init(&acc_empty[b], G::kEpiWarps * G::kCtas);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -619,12 +624,15 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
     }
     __syncwarp();
   } else {
-    // =========================== epilogue (warps 2..5) ===========================
+    // =========================== epilogue (warps 2..9) ===========================
     pdl_wait_predecessor();
     pdl_allow_successor();
-    const int etid = tid - 64;                 // 0..127
+    const int ew = warp - 2;                   // epilogue warp 0..7
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
-    const int r = quarter * 32 + lane;         // weight row within the 128-row block
+    const int ch = ew >> 2;                    // which of the warps of its quarter
+    constexpr int kPerQuarter = G::kEpiWarps / 4;
+    const int r = quarter * 32 + lane;         // weight row within the CTA's 128 rows
+    constexpr int kEpiThreads = G::kEpiWarps * 32;
     bool ok = true;
     // the accumulator buffer is free again: tell the CTA that issues the MMAs
     auto release_acc = [&](uint64_t* bar) {
@@ -681,27 +689,21 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
         if (kGateUp) tmem_ld16(tb + G::kNMax + n0, v);
       };
 
-      if (whole && kGateUp) {
-        // 32 tokens per TMEM round trip (columns past npad, up to kNMax, are read and not stored)
-        for (int n0 = 0; n0 < npad; n0 += 32) {
+      if (whole) {
+        // 32 tokens per TMEM round trip, the two warps of a quarter alternating (columns past npad,
+        // up to kNMax, are read and not stored)
+        for (int n0 = 32 * ch; n0 < npad; n0 += 32 * kPerQuarter) {
           float g[32], v[32];
-          if (ok) {
-            tmem_ld32x2(tb + n0, tb + G::kNMax + n0, g, v);
-          } else {
+          if (!ok) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) g[j] = v[j] = 0.0f;
+          } else if constexpr (kGateUp) {
+            tmem_ld32x2(tb + n0, tb + G::kNMax + n0, g, v);
+          } else {
+            tmem_ld32(tb + n0, g);
           }
           emit(n0, reinterpret_cast<const float(&)[16]>(g[0]), reinterpret_cast<const float(&)[16]>(v[0]));
           emit(n0 + 16, reinterpret_cast<const float(&)[16]>(g[16]), reinterpret_cast<const float(&)[16]>(v[16]));
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) release_acc(&acc_empty[b]);
-      } else if (whole) {
-        for (int n0 = 0; n0 < npad; n0 += 16) {
-          float g[16], v[16];
-          load_acc(n0, g, v);
-          emit(n0, g, v);
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -714,14 +716,14 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
         const int64_t c_first = col_of(ut * KI);  // columns whose ranges hold this unit's stages
         const int64_t c_last = col_of(ut * KI + KI - 1);
         const int slot = piece == nW ? 0 : 1;    // a column's first stream-K piece, or its last
-        float* mine = args.partials + (cta * 2 + slot) * args.partial_stride + etid;
-        for (int n0 = 0; n0 < npad; n0 += 16) {
+        float* mine = args.partials + (cta * 2 + slot) * args.partial_stride + r;
+        for (int n0 = 16 * ch; n0 < npad; n0 += 16 * kPerQuarter) {
           float g[16], v[16];
           load_acc(n0, g, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            mine[(n0 + j) * kEpiThreads] = g[j];
-            if (kGateUp) mine[(G::kNMax + n0 + j) * kEpiThreads] = v[j];
+            mine[(n0 + j) * kRows] = g[j];
+            if (kGateUp) mine[(G::kNMax + n0 + j) * kRows] = v[j];
           }
         }
         tc_fence_before_sync();
@@ -729,7 +731,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
         if (lane == 0) release_acc(&acc_empty[b]);  // TMEM buffer free again
         __threadfence();
         named_bar_sync(1, kEpiThreads);
-        if (etid == 0) {
+        if (ew == 0 && lane == 0) {
           int32_t* counter = &args.counters[(c_first * ranks + rank) * G::kCtas + half];
           const int old = atomicAdd(counter, 1);
           const int last = (old == static_cast<int>(c_last - c_first));
@@ -739,7 +741,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
         named_bar_sync(1, kEpiThreads);
         if (s_misc[8] != 0) {
           __threadfence();
-          for (int n0 = 0; n0 < npad; n0 += 16) {
+          for (int n0 = 16 * ch; n0 < npad; n0 += 16 * kPerQuarter) {
             float g[16], v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) g[j] = v[j] = 0.0f;
@@ -747,11 +749,11 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
               const int64_t c_first_unit = (c * Wt / NC) / KI;
               const int cslot = (ut == c_first_unit) ? 0 : 1;
               const int64_t src_cta = (c * ranks + rank) * G::kCtas + half;
-              const float* src = args.partials + (src_cta * 2 + cslot) * args.partial_stride + etid;
+              const float* src = args.partials + (src_cta * 2 + cslot) * args.partial_stride + r;
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                g[j] += __ldcg(src + (n0 + j) * kEpiThreads);
-                if (kGateUp) v[j] += __ldcg(src + (G::kNMax + n0 + j) * kEpiThreads);
+                g[j] += __ldcg(src + (n0 + j) * kRows);
+                if (kGateUp) v[j] += __ldcg(src + (G::kNMax + n0 + j) * kRows);
               }
             }
             emit(n0, g, v);
