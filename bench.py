@@ -126,6 +126,7 @@ def tensor_peak():
 # the BF16 family alone, whose captures an INT8-only change leaves valid), the attention kernel
 EXPERT_SOURCES = ("expert_tc.cuh", "expert_pair.cuh", "moe_device.cuh", "expert_launch.cu")
 BF16_SOURCES = ("expert_tc.cuh", "moe_device.cuh", "expert_launch.cu")
+DECODE_SOURCES = ("decode_step.cu", "decode_device.cuh", "route_topk.cuh", "moe_device.cuh")
 ATTN_SOURCES = ("gqa_decode.cu", "moe_device.cuh")
 
 
