@@ -2,22 +2,25 @@
 //
 // HiNa-MoE (arXiv 2610.05123), §4.1 FFN equation with bf16 inputs and fp32 accumulation (§4.2.1):
 // gate+up with SiLU(g) * u -> h (bf16), then down -> Y (fp32), over an expert-sorted token block.
-// The weights stream from HBM once per pass of up to 64 tokens of an expert; one thread issues
-// asynchronous MMAs that read the TMA-filled shared-memory tiles directly.
+// The weights stream from HBM once per pass of an expert's tokens (64, 128 or 256 tokens per pass;
+// at 128 and 256 the passes of one expert share each weight block, see Geo and the schedule); one
+// thread issues asynchronous MMAs that read the TMA-filled shared-memory tiles directly.
 //
-// Per CTA (one per SM, persistent, stream-K over (expert pass, 128-row block) x 64-element
-// reduction stages; 6 warps):
+// Per CTA (persistent; decode sizes: one CTA per SM, prefill sizes: CTA pairs; units of
+// (expert round, 128- or 256-row block) x 64-element reduction stages):
 //   warp 0      TMA producer: per stage the weight tile(s) (gate and up: 2 x 128 rows x 128 B;
 //               down: 128 rows x 128 B) and the stage's token tile (the launch's largest pass
-//               rounded up to 16 rows, at most 64, 16 at a time);
-//   warp 1      owns the TMEM allocation; its lane 0 issues tcgen05.mma (M = 128, N = that tile's
-//               rows, K = 16 per instruction) and commits each stage back to the producer and
-//               each finished unit to the epilogue;
-//   warps 2-5   epilogue: TMEM -> registers (thread = weight row), SiLU(g)*u -> h (gate+up) or
-//               Y (down), or the fp32 partial of a unit that another CTA finishes.
-// Accumulators are double buffered in TMEM per unit, so the epilogue of one unit overlaps the MMAs
-// of the next. Gate and up of the same 128 rows go to adjacent column ranges of one buffer, so
-// every epilogue thread holds g and u of the same intermediate index.
+//               share, rounded up; a pair's CTAs each load half of it);
+//   warp 1      owns the TMEM allocation; its lane 0 (the even CTA's, on pairs) issues tcgen05.mma
+//               (M = 128, or 256 over a pair; N = the token tile; K = 16 per instruction) and
+//               commits each stage back to the producer(s) and each finished unit to the epilogue;
+//   warps 2..   epilogue (4 warps, 8 on pairs): TMEM -> registers (thread = weight row), SiLU(g)*u
+//               -> h (gate+up) or Y (down), or the fp32 partial of a unit that another column
+//               finishes.
+// Accumulators are double buffered in TMEM where two fit (not gate+up at 256-token passes), so the
+// epilogue of one unit overlaps the MMAs of the next. Gate and up of the same 128 rows go to
+// adjacent column ranges of one buffer, so every epilogue thread holds g and u of the same
+// intermediate index.
 // Args, Unit and the schedule table size are shared with the INT8 pair kernels (expert_pair.cuh).
 #pragma once
 
