@@ -177,8 +177,9 @@ template <bool kGateUp, int kN, bool kPair>
 cudaError_t launch_tc_kernel(const CUtensorMap& a0, const CUtensorMap& a1, const void* tokens, int K, int P,
                              const tc::Args& args, int num_ctas, cudaStream_t s) {
   using G = tc::Geo<kGateUp, kN, kPair>;
-  CUtensorMap tb;
-  if (!encode_tokens(&tb, tokens, K, P, false, G::kBoxRows)) return cudaErrorInvalidValue;
+  tc::TokenMaps tb;
+  for (int m = 0; m < 4; ++m)
+    if (!encode_tokens(&tb.m[m], tokens, K, P, false, 128 >> m)) return cudaErrorInvalidValue;
   int resident = 0;
   cudaError_t e = prepare_tc_kernel<kGateUp, kN, kPair>(&resident);
   if (e != cudaSuccess) return e;

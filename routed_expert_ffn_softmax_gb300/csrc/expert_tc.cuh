@@ -59,11 +59,14 @@ struct Geo {
   static constexpr int kWBytes = kGateUp ? 32768 : 16384;   // this CTA's weight bytes per stage
   static constexpr int kBRows = kN / kCtas;                 // this CTA's token rows per stage, at most
   static constexpr int kBBytes = kBRows * 128;              // token tile: kBRows rows x 64 elements x 2 B
-  // Token rows per TMA box. A pair loads its whole token slot as one box every stage (rows past the
-  // pass's own are never read): measured on GB300, TMA moves 2 KB boxes from L2 at a quarter of the
-  // rate of 16 KB ones, and the token tile is the larger part of a stage at these sizes.
-  static constexpr int kBoxRows = kPair ? kBRows : (kN >= 128 ? 32 : 16);
-  static constexpr int kTileRound = kPair ? 32 : kBoxRows;  // the launch's token tile is a multiple
+  // The launch's token tile is a multiple of 16 rows per CTA. Measured on GB300, TMA moves 2 KB
+  // boxes from L2 at a quarter of the rate of 16 KB ones, and fewer boxes per stage beat fewer
+  // bytes: a pair loads its whole token slot (kBRows rows, rows past its share never read) as one
+  // box every stage (5-7% faster at prefill sizes than the exact rows in two or three boxes); a
+  // single CTA loads exactly its rows as at most three boxes of 64, 32 or 16 rows (TokenMaps;
+  // against 16-row boxes +3% at 64 tokens per expert, the same elsewhere).
+  static constexpr int kTileRound = 16 * kCtas;
+  static constexpr int kSlotMap = kBRows == 128 ? 0 : (kBRows == 64 ? 1 : 2);  // TokenMaps index of a slot
   static constexpr int kStage = kWBytes + kBBytes;
   static constexpr int kTableBytes = (4 * kTable + 32) * 4;
   // as many stages as fit (down at 64-token passes: 9; measured on GB300 7: -0.4%, 9: +0.3%)
@@ -76,8 +79,16 @@ struct Geo {
   static constexpr int64_t kPartialSlot = 128LL * kAccCols;     // fp32 per stream-K partial slot
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
   static_assert(kNMax % 32 == 0, "the gate+up epilogue reads 32 accumulator columns at a time");
+  static_assert(kPair ? (kBRows == 128 || kBRows == 64) : kBRows <= 128 + 64 + 32 + 16,
+                "a pair's token slot is one box; a single CTA's rows at most four");
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
   static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
+};
+
+// Tensor maps of the token block with boxes of 128 >> m rows (m = 0..3: 128, 64, 32, 16), 64
+// elements each.
+struct TokenMaps {
+  CUtensorMap m[4];
 };
 
 struct Args {
@@ -252,7 +263,7 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
 template <bool kGateUp, int kN, bool kPair>
 __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                     const __grid_constant__ CUtensorMap tmB, const Args args) {
+                     const __grid_constant__ TokenMaps tmB, const Args args) {
   using G = Geo<kGateUp, kN, kPair>;
   constexpr int kThreads = G::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -287,7 +298,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA0);
     if (kGateUp) tma_prefetch_desc(&tmA1);
-    tma_prefetch_desc(&tmB);
+    for (int m = 0; m < 4; ++m) tma_prefetch_desc(&tmB.m[m]);
   }
   if (warp == 1) {
     if constexpr (kPair) tmem_alloc_pair(tmem_slot, G::kTmemCols);
@@ -476,10 +487,16 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
       uint8_t* sb_ = smem + stg * G::kStage + G::kWBytes;
       const int r0 = w.tok0 + half * b_rows;
       if constexpr (kPair) {
-        tma_load_2d_pair(sb_, &tmB, leader_barrier(&full[stg]), kk * G::kKStage, r0);
+        tma_load_2d_pair(sb_, &tmB.m[G::kSlotMap], leader_barrier(&full[stg]), kk * G::kKStage, r0);
       } else {
-        for (int j = 0; j < b_rows; j += G::kBoxRows)
-          tma_load_2d(sb_ + j * 128, &tmB, &full[stg], kk * G::kKStage, r0 + j);
+        int j = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {  // b_rows (a multiple of 16, at most kBRows) as a sum of box heights
+          if (b_rows - j >= (128 >> m)) {
+            tma_load_2d(sb_ + j * 128, &tmB.m[m], &full[stg], kk * G::kKStage, r0 + j);
+            j += 128 >> m;
+          }
+        }
       }
     };
     // cursor over this column's stages: piece, its stage range and unit
