@@ -146,11 +146,11 @@ moe_status_t moe_gather(const uint16_t* x, int T, int H, int top_k, const int32_
  *   workspace       >= moe_workspace_size(T, H, I, E, top_k, wtype) bytes (device)
  * Only the weights of active experts are read. BF16 weights stream once per pass of an
  * expert's tokens: 64-token passes when the mean tokens per expert P / E is at most 40,
- * 128 up to 96, 256 above (moe_set_expert_pass_tokens can force a size). At 128- and
- * 256-token passes an expert with more tokens than one pass has them split evenly over up
- * to 4 CTAs that run the same weight blocks side by side, so its weights come from HBM
- * once and from L2 for the others (up to 4 x 256 tokens per expert; more take further
- * rounds). INT8 weights stream once per 64 tokens.
+ * 128 up to 96, 192 or 256 above (moe_set_expert_pass_tokens can force a size). At 128- to
+ * 256-token passes (on CTA pairs) an expert with more tokens than one pass has them split
+ * evenly over up to 8 passes that run the same weight blocks side by side, so its weights
+ * come from HBM once and from L2 for the others (up to 8 passes' worth of tokens per expert;
+ * more take further rounds). INT8 weights stream once per 16 or 32 tokens.
  * The result is deterministic for a given device and pass size.
  */
 moe_status_t moe_expert_ffn(const uint16_t* xg, const int32_t* expert_offsets,
@@ -237,7 +237,7 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
 moe_status_t moe_set_decode_step_policy(int policy);
 
 /*
- * Tokens per pass of the BF16 expert kernels, gate+up and down separately: 64, 128 or 256,
+ * Tokens per pass of the BF16 expert kernels, gate+up and down separately: 64, 128, 192 or 256,
  * or 0 for the rule of moe_expert_ffn (the default). A tuning and test control; the paper
  * has no counterpart. Process-wide, affects only later calls. moe_workspace_size sizes the
  * stream-K partial slots for the sizes in force when it is called; a call whose workspace

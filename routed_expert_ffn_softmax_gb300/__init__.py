@@ -178,7 +178,7 @@ def moe_set_decode_step_policy(policy: int) -> None:
 
 
 def moe_set_expert_pass_tokens(gate_up: int = 0, down: int = 0) -> None:
-    """Tokens per pass of the BF16 expert kernels (64, 128 or 256; 0 = by batch shape, the default).
+    """Tokens per pass of the BF16 expert kernels (64, 128, 192 or 256; 0 = by batch shape, the default).
     Size workspaces after setting it (see include/moe.h)."""
     f = load().moe_set_expert_pass_tokens
     f.argtypes = [ctypes.c_int, ctypes.c_int]

@@ -440,7 +440,7 @@ moe_status_t moe_set_decode_step_policy(int policy) {
 }
 
 moe_status_t moe_set_expert_pass_tokens(int gate_up, int down) {
-  auto ok = [](int n) { return n == 0 || n == 64 || n == 128 || n == 256; };
+  auto ok = [](int n) { return n == 0 || n == 64 || n == 128 || n == 192 || n == 256; };
   if (!ok(gate_up) || !ok(down)) return MOE_ERR_INVALID_ARG;
   moe::set_pass_tokens(gate_up, down);
   return MOE_OK;

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -179,7 +180,8 @@ cudaError_t launch_tc_kernel(const CUtensorMap& a0, const CUtensorMap& a1, const
   using G = tc::Geo<kGateUp, kN, kPair>;
   tc::TokenMaps tb;
   for (int m = 0; m < 4; ++m)
-    if (!encode_tokens(&tb.m[m], tokens, K, P, false, 128 >> m)) return cudaErrorInvalidValue;
+    if (!encode_tokens(&tb.m[m], tokens, K, P, false, (kPair && m == 0) ? G::kBRows : 128 >> m))
+      return cudaErrorInvalidValue;
   int resident = 0;
   cudaError_t e = prepare_tc_kernel<kGateUp, kN, kPair>(&resident);
   if (e != cudaSuccess) return e;
@@ -205,7 +207,7 @@ cudaError_t launch_tc_kernel(const CUtensorMap& a0, const CUtensorMap& a1, const
   return cudaLaunchKernelEx(&cfg, tc::expert_tc_kernel<kGateUp, kN, kPair>, a0, a1, tb, args);
 }
 
-// Launch the kernel of `pass` tokens per pass (64 on single CTAs; 128 or 256 on CTA pairs), or of
+// Launch the kernel of `pass` tokens per pass (64 on single CTAs; 128, 192 or 256 on CTA pairs), or of
 // 64 where its partial slots would not fit in `slot` fp32.
 template <bool kGateUp>
 cudaError_t launch_tc_pass(int pass, int64_t slot, const CUtensorMap& a0, const CUtensorMap& a1, const void* tokens,
@@ -213,17 +215,27 @@ cudaError_t launch_tc_pass(int pass, int64_t slot, const CUtensorMap& a0, const 
   if (partial_slot_floats(pass, kGateUp) > slot) pass = 64;
   args.partial_stride = partial_slot_floats(pass, kGateUp);
   if (pass == 256) return launch_tc_kernel<kGateUp, 256, true>(a0, a1, tokens, K, P, args, num_ctas, s);
+  if (pass == 192) return launch_tc_kernel<kGateUp, 192, true>(a0, a1, tokens, K, P, args, num_ctas, s);
   if (pass == 128) return launch_tc_kernel<kGateUp, 128, true>(a0, a1, tokens, K, P, args, num_ctas, s);
   args.partial_stride = kPartialSlotFloats;
   return launch_tc_kernel<kGateUp, 64, false>(a0, a1, tokens, K, P, args, num_ctas, s);
 }
 
 std::atomic<int> g_pass_gate_up{0}, g_pass_down{0};
+// Above 96 tokens per expert on average: 192-token passes when the largest expert (estimated as
+// mean + 2 sqrt(mean)) needs no more ranks at 192 than at 256 (its token slots then load as one
+// box with nothing past the ranks' shares; measured on GB300 +1-4% at 256 and 512 tokens per
+// expert), else 256 (one rank more cost 8% at 1024 tokens per expert).
 int pass_by_mean(int64_t P, int E) {
   const int64_t mean = (P + E - 1) / (E > 0 ? E : 1);
-  return mean <= 40 ? 64 : (mean <= 96 ? 128 : 256);
+  if (mean <= 40) return 64;
+  if (mean <= 96) return 128;
+  const double est = static_cast<double>(mean) + 2.0 * std::sqrt(static_cast<double>(mean));
+  const int64_t g256 = static_cast<int64_t>(std::ceil(est / 256.0));
+  const int64_t g192 = static_cast<int64_t>(std::ceil(est / 192.0));
+  return g192 == g256 ? 192 : 256;
 }
-int valid_pass(int n) { return n == 64 || n == 128 || n == 256 ? n : 0; }
+int valid_pass(int n) { return n == 64 || n == 128 || n == 192 || n == 256 ? n : 0; }
 
 // BF16: weight boxes of 128 rows by 128 bytes, token boxes of 16 rows (64-token passes) or 32.
 cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {

@@ -2,8 +2,8 @@
 //
 // HiNa-MoE (arXiv 2610.05123), §4.1 FFN equation with bf16 inputs and fp32 accumulation (§4.2.1):
 // gate+up with SiLU(g) * u -> h (bf16), then down -> Y (fp32), over an expert-sorted token block.
-// The weights stream from HBM once per pass of an expert's tokens (64, 128 or 256 tokens per pass;
-// at 128 and 256 the passes of one expert share each weight block, see Geo and the schedule); one
+// The weights stream from HBM once per pass of an expert's tokens (64, 128, 192 or 256 tokens per
+// pass; above 64 the passes of one expert share each weight block, see Geo and the schedule); one
 // thread issues asynchronous MMAs that read the TMA-filled shared-memory tiles directly.
 //
 // Per CTA (persistent; decode sizes: one CTA per SM, prefill sizes: CTA pairs; units of
@@ -34,7 +34,7 @@ constexpr int kTable = 256;
 constexpr int kPartialFloats = 16384;  // one INT8 pair-kernel CTA slot: 128 rows x 128 accumulator columns
 constexpr int kMaxRanks = 8;           // passes sharing one weight block (BF16, 128- and 256-token passes)
 
-// kN: tokens per pass (64, 128 or 256; the launch picks it from the batch's tokens per expert). An
+// kN: tokens per pass (64, 128, 192 or 256; the launch picks it from the batch's tokens per expert). An
 // expert with more tokens than a pass streams its weights once per pass, so larger passes read the
 // weights fewer times when experts see many tokens (prefill-sized batches); smaller passes leave room
 // for more stages at decode sizes.
@@ -66,7 +66,7 @@ struct Geo {
   // single CTA loads exactly its rows as at most three boxes of 64, 32 or 16 rows (TokenMaps;
   // against 16-row boxes +3% at 64 tokens per expert, the same elsewhere).
   static constexpr int kTileRound = 16 * kCtas;
-  static constexpr int kSlotMap = kBRows == 128 ? 0 : (kBRows == 64 ? 1 : 2);  // TokenMaps index of a slot
+
   static constexpr int kStage = kWBytes + kBBytes;
   static constexpr int kTableBytes = (4 * kTable + 32) * 4;
   // as many stages as fit (down at 64-token passes: 9; measured on GB300 7: -0.4%, 9: +0.3%)
@@ -74,19 +74,20 @@ struct Geo {
   static constexpr int kAccCols = kGateUp ? 2 * kNMax : kNMax;  // one accumulator buffer
   static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;  // double buffered where TMEM allows
   static constexpr int kTmemCols = kAccBufs * kAccCols;
+  static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : (kTmemCols <= 256 ? 256 : 512);  // a power of two
   static constexpr int kBarBytes = (2 * kStages + 5) * 8;
   static constexpr int kSmem = kStages * kStage + kBarBytes + kTableBytes;
   static constexpr int64_t kPartialSlot = 128LL * kAccCols;     // fp32 per stream-K partial slot
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
   static_assert(kNMax % 32 == 0, "the gate+up epilogue reads 32 accumulator columns at a time");
-  static_assert(kPair ? (kBRows == 128 || kBRows == 64) : kBRows <= 128 + 64 + 32 + 16,
-                "a pair's token slot is one box; a single CTA's rows at most four");
-  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
+  static_assert(kPair ? kBRows <= 256 : kBRows <= 64 + 32 + 16 + 8,
+                "a pair's token slot is one box; a single CTA's rows at most three");
+  static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
 
-// Tensor maps of the token block with boxes of 128 >> m rows (m = 0..3: 128, 64, 32, 16), 64
-// elements each.
+// Tensor maps of the token block, 64 elements wide: for a single CTA boxes of 128 >> m rows
+// (m = 1..3: 64, 32, 16); for a pair m[0] has the height of its token slot.
 struct TokenMaps {
   CUtensorMap m[4];
 };
@@ -301,8 +302,8 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
     for (int m = 0; m < 4; ++m) tma_prefetch_desc(&tmB.m[m]);
   }
   if (warp == 1) {
-    if constexpr (kPair) tmem_alloc_pair(tmem_slot, G::kTmemCols);
-    else tmem_alloc(tmem_slot, G::kTmemCols);
+    if constexpr (kPair) tmem_alloc_pair(tmem_slot, G::kTmemAlloc);
+    else tmem_alloc(tmem_slot, G::kTmemAlloc);
   }
 
   // ---- schedule tables. They are read before waiting for the preceding kernel: every kernel of
@@ -487,11 +488,11 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
       uint8_t* sb_ = smem + stg * G::kStage + G::kWBytes;
       const int r0 = w.tok0 + half * b_rows;
       if constexpr (kPair) {
-        tma_load_2d_pair(sb_, &tmB.m[G::kSlotMap], leader_barrier(&full[stg]), kk * G::kKStage, r0);
+        tma_load_2d_pair(sb_, &tmB.m[0], leader_barrier(&full[stg]), kk * G::kKStage, r0);
       } else {
         int j = 0;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {  // b_rows (a multiple of 16, at most kBRows) as a sum of box heights
+        for (int m = 1; m < 4; ++m) {  // b_rows (a multiple of 16, at most 64) as a sum of box heights
           if (b_rows - j >= (128 >> m)) {
             tma_load_2d(sb_ + j * 128, &tmB.m[m], &full[stg], kk * G::kKStage, r0 + j);
             j += 128 >> m;
@@ -791,8 +792,8 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
   if constexpr (kPair) cluster_sync_all();
   tc_fence_after_sync();
   if (warp == 1) {
-    if constexpr (kPair) tmem_dealloc_pair(tmem_base, G::kTmemCols);
-    else tmem_dealloc(tmem_base, G::kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, G::kTmemAlloc);
+    else tmem_dealloc(tmem_base, G::kTmemAlloc);
   }
 }
 

@@ -49,7 +49,7 @@ cudaError_t launch_gather_f16(const uint16_t* x, int T, int H, int P, const int3
 constexpr int kPartialSlotFloats = 16384;
 constexpr int kPartialCtas = 256;
 
-// BF16 expert kernels: tokens per pass (64, 128 or 256) of gate+up and of down, and the fp32 per
+// BF16 expert kernels: tokens per pass (64, 128, 192 or 256) of gate+up and of down, and the fp32 per
 // stream-K partial slot a pass size needs (128 rows x the accumulator columns: gate and up, or down).
 struct PassTokens {
   int gate_up, down;

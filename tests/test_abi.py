@@ -235,18 +235,19 @@ def test_decode_step_policy_and_launch_count(lib):
 
 def test_pass_tokens_size_the_workspace(lib):
     """BF16 workspaces hold stream-K partial slots for the pass size the batch shape picks (mean tokens per
-    expert <= 40: 64, <= 96: 128, else 256) or the one forced; INT8 ones stay at 64-token slots."""
+    expert <= 40: 64, <= 96: 128, else 192 or 256 by the estimated largest expert) or the one forced;
+    INT8 ones stay at 64-token slots."""
     ws = lib.moe_workspace_size
     f = lib.moe_set_expert_pass_tokens
     f.argtypes = [ctypes.c_int, ctypes.c_int]
     f.restype = ctypes.c_int
     slot64 = 4 * 256 * 2 * 16384                # 256 CTAs x 2 slots x (128 rows x 128 columns) fp32
     mix = lambda T, wt=BF16: ws(T, 4096, 14336, 8, 2, wt)   # mean tokens per expert = T / 4
-    auto = {T: mix(T) for T in (64, 256, 1024)}
+    auto = {T: mix(T) for T in (64, 256, 1024, 4096)}
     int8 = mix(1024, INT8)
     try:
         assert f(64, 64) == OK
-        base = {T: mix(T) for T in (64, 256, 1024)}
+        base = {T: mix(T) for T in (64, 256, 1024, 4096)}
         assert mix(1024, INT8) == int8
         assert f(256, 64) == OK                  # gate+up at 256: slots of 128 x 512 columns
         assert mix(64) == base[64] + 3 * slot64
@@ -254,12 +255,15 @@ def test_pass_tokens_size_the_workspace(lib):
         assert mix(64) == base[64] + slot64
         assert f(128, 0) == OK                   # gate+up at 128: 128 x 256; down by shape (64)
         assert mix(64) == base[64] + slot64
+        assert f(192, 192) == OK                 # gate+up at 192: 128 x 384 columns
+        assert mix(64) == base[64] + 2 * slot64
         assert f(96, 0) == INVALID and f(0, 32) == INVALID
     finally:
         assert f(0, 0) == OK
     assert auto[64] == base[64]                  # 16 per expert: 64-token passes
     assert auto[256] == base[256] + slot64       # 64 per expert: 128
-    assert auto[1024] == base[1024] + 3 * slot64  # 256 per expert: 256
+    assert auto[1024] == base[1024] + 2 * slot64  # 256 per expert: 192 (the largest expert needs 2 ranks either way)
+    assert auto[4096] == base[4096] + 3 * slot64  # 1024 per expert: 256 (at 192 it would need a sixth rank)
     assert mix(1024) == auto[1024]
 
 

@@ -67,7 +67,8 @@ def test_prefill_matches_oracle(T, H, I, E, k, skew):
     assert_moe_close(to_np_f32(out), oracle.bf16_bits_to_f32(ref["out"]), "bf16", f"T={T} H={H} I={I} E={E}")
 
 
-@pytest.mark.parametrize("passes", [(64, 64), (128, 128), (256, 256), (128, 256), (256, 64), (64, 128)])
+@pytest.mark.parametrize("passes", [(64, 64), (128, 128), (192, 192), (256, 256), (128, 256), (256, 64), (64, 128),
+                                    (192, 64)])
 def test_every_pass_size_matches_oracle(passes):
     """Each gate+up / down pass size on one skewed batch (experts 0 and 1 hot): ranks, rounds, and ranks
     left without tokens all occur for some pass size."""
