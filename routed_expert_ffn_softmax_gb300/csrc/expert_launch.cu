@@ -134,9 +134,9 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, int K, int P, uint16_t* dst,
 
 // Per device: the shared-memory attribute set, and (CTA pairs) the clusters that can be resident
 // at once (a persistent grid must not be larger, or the late CTAs would run after the others).
-template <bool kGateUp, int kN, bool kPair>
+template <int kKind, int kN, bool kPair>
 cudaError_t prepare_tc_kernel(int* resident) {
-  using G = tc::Geo<kGateUp, kN, kPair>;
+  using G = tc::Geo<kKind, kN, kPair>;
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev];
   int dev = 0;
@@ -149,7 +149,7 @@ cudaError_t prepare_tc_kernel(int* resident) {
       return cudaSuccess;
     }
   }
-  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kGateUp, kN, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(tc::expert_tc_kernel<kKind, kN, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            G::kSmem);
   if (e != cudaSuccess) return e;
   int n = kPartialCtas;
@@ -165,7 +165,7 @@ cudaError_t prepare_tc_kernel(int* resident) {
     cfg.dynamicSmemBytes = G::kSmem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaOccupancyMaxActiveClusters(&n, tc::expert_tc_kernel<kGateUp, kN, kPair>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, tc::expert_tc_kernel<kKind, kN, kPair>, &cfg);
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorNotSupported;
   }
@@ -174,19 +174,19 @@ cudaError_t prepare_tc_kernel(int* resident) {
   return cudaSuccess;
 }
 
-template <bool kGateUp, int kN, bool kPair>
+template <int kKind, int kN, bool kPair>
 cudaError_t launch_tc_kernel(const CUtensorMap& a0, const CUtensorMap& a1, const void* tokens, int K, int P,
                              const tc::Args& args, int num_ctas, cudaStream_t s) {
-  using G = tc::Geo<kGateUp, kN, kPair>;
+  using G = tc::Geo<kKind, kN, kPair>;
   tc::TokenMaps tb;
   for (int m = 0; m < 4; ++m)
     if (!encode_tokens(&tb.m[m], tokens, K, P, false, (kPair && m == 0) ? G::kBRows : 128 >> m))
       return cudaErrorInvalidValue;
   int resident = 0;
-  cudaError_t e = prepare_tc_kernel<kGateUp, kN, kPair>(&resident);
+  cudaError_t e = prepare_tc_kernel<kKind, kN, kPair>(&resident);
   if (e != cudaSuccess) return e;
   if (!kPair)
-    return launch_pdl(tc::expert_tc_kernel<kGateUp, kN, kPair>, dim3(num_ctas), dim3(G::kThreads), G::kSmem, s, a0,
+    return launch_pdl(tc::expert_tc_kernel<kKind, kN, kPair>, dim3(num_ctas), dim3(G::kThreads), G::kSmem, s, a0,
                       a1, tb, args);
   int pairs = num_ctas / 2 < resident ? num_ctas / 2 : resident;
   if (pairs < 1) pairs = 1;
@@ -204,7 +204,7 @@ cudaError_t launch_tc_kernel(const CUtensorMap& a0, const CUtensorMap& a1, const
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, tc::expert_tc_kernel<kGateUp, kN, kPair>, a0, a1, tb, args);
+  return cudaLaunchKernelEx(&cfg, tc::expert_tc_kernel<kKind, kN, kPair>, a0, a1, tb, args);
 }
 
 // Launch the kernel of `pass` tokens per pass (64 on single CTAs; 128, 192 or 256 on CTA pairs), or of
@@ -214,11 +214,13 @@ cudaError_t launch_tc_pass(int pass, int64_t slot, const CUtensorMap& a0, const 
                            int K, int P, tc::Args args, int num_ctas, cudaStream_t s) {
   if (partial_slot_floats(pass, kGateUp) > slot) pass = 64;
   args.partial_stride = partial_slot_floats(pass, kGateUp);
-  if (pass == 256) return launch_tc_kernel<kGateUp, 256, true>(a0, a1, tokens, K, P, args, num_ctas, s);
-  if (pass == 192) return launch_tc_kernel<kGateUp, 192, true>(a0, a1, tokens, K, P, args, num_ctas, s);
-  if (pass == 128) return launch_tc_kernel<kGateUp, 128, true>(a0, a1, tokens, K, P, args, num_ctas, s);
+  // on pairs down takes two 128-row tiles per stage (tc::kDown2), like gate and up
+  constexpr int kPairKind = kGateUp ? tc::kGateUp : tc::kDown2;
+  if (pass == 256) return launch_tc_kernel<kPairKind, 256, true>(a0, a1, tokens, K, P, args, num_ctas, s);
+  if (pass == 192) return launch_tc_kernel<kPairKind, 192, true>(a0, a1, tokens, K, P, args, num_ctas, s);
+  if (pass == 128) return launch_tc_kernel<kPairKind, 128, true>(a0, a1, tokens, K, P, args, num_ctas, s);
   args.partial_stride = kPartialSlotFloats;
-  return launch_tc_kernel<kGateUp, 64, false>(a0, a1, tokens, K, P, args, num_ctas, s);
+  return launch_tc_kernel<kGateUp ? tc::kGateUp : tc::kDown, 64, false>(a0, a1, tokens, K, P, args, num_ctas, s);
 }
 
 std::atomic<int> g_pass_gate_up{0}, g_pass_down{0};

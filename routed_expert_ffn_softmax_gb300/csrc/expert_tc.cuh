@@ -44,8 +44,16 @@ constexpr int kMaxRanks = 8;           // passes sharing one weight block (BF16,
 // issues MMAs that read both CTAs' tiles and write each CTA's 128 rows into its own TMEM. Per CTA a
 // stage then carries half the token bytes for the same tensor work, which is what bounds these
 // kernels at prefill sizes (bytes in flight per SM against L2 latency, measured on GB300).
-template <bool kGateUp, int kN = 64, bool kPair = false>
+// kKind: kDown (one 128-row weight tile per stage), kGateUp (gate and up tiles of the same rows),
+// kDown2 (two 128-row tiles of down per stage, on pairs: a unit is 256 rows per CTA, so a stage
+// carries as many weight bytes per token byte as gate+up; down on single tiles ran its tensor pipe
+// at 59% at prefill sizes, bounded by the token tile's L2 stream).
+constexpr int kDown = 0, kGateUp = 1, kDown2 = 2;
+
+template <int kKind, int kN = 64, bool kPair = false>
 struct Geo {
+  static constexpr bool kGU = kKind == kGateUp;
+  static constexpr bool kTwoA = kKind != kDown;             // two weight tiles (accumulators) per stage
   // Epilogue warps: on pairs two per TMEM lane quarter, taking alternate groups of accumulator
   // columns, so a unit's accumulators drain in half the time (gate+up holds one accumulator buffer
   // at 256-token passes, and its MMAs wait for the drain); at 64-token passes one per quarter
@@ -53,10 +61,11 @@ struct Geo {
   static constexpr int kEpiWarps = kPair ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kCtas = kPair ? 2 : 1;               // CTAs per pass
-  static constexpr int kUnitRows = 128 * kCtas;             // weight rows per unit
+  static constexpr int kUnitRows = 128 * kCtas * (kKind == kDown2 ? 2 : 1);  // weight rows per unit
+  static constexpr int kSecondRows = 128 * kCtas;           // kDown2: row offset of a stage's second tile
   static constexpr int kNMax = kN;                          // tokens per pass
   static constexpr int kKStage = 64;                        // reduction elements per stage
-  static constexpr int kWBytes = kGateUp ? 32768 : 16384;   // this CTA's weight bytes per stage
+  static constexpr int kWBytes = kTwoA ? 32768 : 16384;     // this CTA's weight bytes per stage
   static constexpr int kBRows = kN / kCtas;                 // this CTA's token rows per stage, at most
   static constexpr int kBBytes = kBRows * 128;              // token tile: kBRows rows x 64 elements x 2 B
   // The launch's token tile is a multiple of 16 rows per CTA. Measured on GB300, TMA moves 2 KB
@@ -71,7 +80,7 @@ struct Geo {
   static constexpr int kTableBytes = (4 * kTable + 32) * 4;
   // as many stages as fit (down at 64-token passes: 9; measured on GB300 7: -0.4%, 9: +0.3%)
   static constexpr int kStages = (232448 - kTableBytes - 256) / kStage;
-  static constexpr int kAccCols = kGateUp ? 2 * kNMax : kNMax;  // one accumulator buffer
+  static constexpr int kAccCols = kTwoA ? 2 * kNMax : kNMax;  // one accumulator buffer
   static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;  // double buffered where TMEM allows
   static constexpr int kTmemCols = kAccBufs * kAccCols;
   static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : (kTmemCols <= 256 ? 256 : 512);  // a power of two
@@ -99,7 +108,7 @@ struct Args {
   void* out;                  // h bf16 [P, I] (gate+up) or Y f32 [P, H] (down)
   int64_t out_ld;
   float* partials;            // [kMaxCtas][2][partial_stride]
-  int64_t partial_stride;     // fp32 per partial slot (BF16: at least Geo<kGateUp, kN>::kPartialSlot)
+  int64_t partial_stride;     // fp32 per partial slot (BF16: at least Geo<kKind, kN, kPair>::kPartialSlot)
   int32_t* counters;          // zero on entry, left zero on exit
   int32_t* status;
   int rows;                   // I (gate+up) or H (down)
@@ -261,11 +270,11 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-template <bool kGateUp, int kN, bool kPair>
-__global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
+template <int kKind, int kN, bool kPair>
+__global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ TokenMaps tmB, const Args args) {
-  using G = Geo<kGateUp, kN, kPair>;
+  using G = Geo<kKind, kN, kPair>;
   constexpr int kThreads = G::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kStages * G::kStage);
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA0);
-    if (kGateUp) tma_prefetch_desc(&tmA1);
+    if (G::kGU) tma_prefetch_desc(&tmA1);
     for (int m = 0; m < 4; ++m) tma_prefetch_desc(&tmB.m[m]);
   }
   if (warp == 1) {
@@ -475,13 +484,16 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
     auto issue_a = [&](int stg, const Unit& w, int kk) {
       uint8_t* st = smem + stg * G::kStage;
       const int row = w.rb * G::kUnitRows + half * 128;
+      // the second tile: up of the same rows, or (kDown2) the down rows kSecondRows further on
+      const CUtensorMap* a1 = G::kGU ? &tmA1 : &tmA0;
+      const int row1 = G::kGU ? row : row + G::kSecondRows;
       if constexpr (kPair) {
         const uint32_t bar = leader_barrier(&full[stg]);
         tma_load_3d_pair(st, &tmA0, bar, kk * G::kKStage, row, w.e, policy);
-        if (kGateUp) tma_load_3d_pair(st + 16384, &tmA1, bar, kk * G::kKStage, row, w.e, policy);
+        if (G::kTwoA) tma_load_3d_pair(st + 16384, a1, bar, kk * G::kKStage, row1, w.e, policy);
       } else {
         tma_load_3d(st, &tmA0, &full[stg], kk * G::kKStage, row, w.e, policy);
-        if (kGateUp) tma_load_3d(st + 16384, &tmA1, &full[stg], kk * G::kKStage, row, w.e, policy);
+        if (G::kTwoA) tma_load_3d(st + 16384, a1, &full[stg], kk * G::kKStage, row1, w.e, policy);
       }
     };
     auto issue_b = [&](int stg, const Unit& w, int kk) {
@@ -628,7 +640,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
               const uint64_t db = umma_desc_sw128(st + G::kWBytes + 32 * s);
               const bool acc = !(first && s == 0);
               mma(d, umma_desc_sw128(st + 32 * s), db, acc);
-              if (kGateUp) mma(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, acc);
+              if (G::kTwoA) mma(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, acc);
             }
           }
           commit(&empty[stage]);  // frees the stage (of both CTAs) once these MMAs have read it
@@ -674,8 +686,8 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
       const bool whole = pc.kb == 0 && pc.ke == KI;
 
       auto emit = [&](int n0, const float (&g)[16], const float (&v)[16]) {
-        // g: gate (or down) accumulators of tokens n0..n0+15, v: up accumulators
-        if constexpr (kGateUp) {
+        // g: gate (or down) accumulators of tokens n0..n0+15, v: up (or the second down tile's)
+        if constexpr (G::kGU) {
           const int i = un.rb * G::kUnitRows + half * 128 + r;
           if (i < args.rows) {
             __nv_bfloat16* h = static_cast<__nv_bfloat16*>(args.out);
@@ -687,13 +699,23 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
             }
           }
         } else {
+          float* y = static_cast<float*>(args.out);
           const int row = un.rb * G::kUnitRows + half * 128 + r;
           if (row < args.rows) {
-            float* y = static_cast<float*>(args.out);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int n = n0 + j;
               if (n < un.ntok) y[static_cast<int64_t>(un.tok0 + n) * args.out_ld + row] = g[j];
+            }
+          }
+          if constexpr (kKind == kDown2) {
+            const int row2 = row + G::kSecondRows;
+            if (row2 < args.rows) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int n = n0 + j;
+                if (n < un.ntok) y[static_cast<int64_t>(un.tok0 + n) * args.out_ld + row2] = v[j];
+              }
             }
           }
         }
@@ -707,7 +729,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
           return;
         }
         tmem_ld16(tb + n0, g);
-        if (kGateUp) tmem_ld16(tb + G::kNMax + n0, v);
+        if (G::kTwoA) tmem_ld16(tb + G::kNMax + n0, v);
       };
 
       if (whole) {
@@ -718,7 +740,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
           if (!ok) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) g[j] = v[j] = 0.0f;
-          } else if constexpr (kGateUp) {
+          } else if constexpr (G::kTwoA) {
             tmem_ld32x2(tb + n0, tb + G::kNMax + n0, g, v);
           } else {
             tmem_ld32(tb + n0, g);
@@ -744,7 +766,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             mine[(n0 + j) * kRows] = g[j];
-            if (kGateUp) mine[(G::kNMax + n0 + j) * kRows] = v[j];
+            if (G::kTwoA) mine[(G::kNMax + n0 + j) * kRows] = v[j];
           }
         }
         tc_fence_before_sync();
@@ -774,7 +796,7 @@ __global__ void __launch_bounds__(Geo<kGateUp, kN, kPair>::kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 g[j] += __ldcg(src + (n0 + j) * kRows);
-                if (kGateUp) v[j] += __ldcg(src + (G::kNMax + n0 + j) * kRows);
+                if (G::kTwoA) v[j] += __ldcg(src + (G::kNMax + n0 + j) * kRows);
               }
             }
             emit(n0, g, v);

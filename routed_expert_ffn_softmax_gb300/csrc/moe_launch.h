@@ -50,7 +50,7 @@ constexpr int kPartialSlotFloats = 16384;
 constexpr int kPartialCtas = 256;
 
 // BF16 expert kernels: tokens per pass (64, 128, 192 or 256) of gate+up and of down, and the fp32 per
-// stream-K partial slot a pass size needs (128 rows x the accumulator columns: gate and up, or down).
+// stream-K partial slot a pass size needs (128 rows x the accumulator columns).
 struct PassTokens {
   int gate_up, down;
 };
@@ -58,8 +58,10 @@ struct PassTokens {
 // unless set_pass_tokens forced a size. The workspace layout and the launch both call it.
 PassTokens pass_tokens(int64_t P, int E);
 void set_pass_tokens(int gate_up, int down);  // 0 = by batch shape
+// Passes above 64 tokens run on CTA pairs, where down also holds two accumulator regions (two
+// 128-row tiles per stage).
 inline int64_t partial_slot_floats(int pass_tokens, bool gate_up) {
-  return 128LL * (gate_up ? 2 : 1) * pass_tokens;
+  return 128LL * ((gate_up || pass_tokens > 64) ? 2 : 1) * pass_tokens;
 }
 
 // Grouped expert FFN (gate+up then down) over an expert-sorted token block.

@@ -251,8 +251,8 @@ def test_pass_tokens_size_the_workspace(lib):
         assert mix(1024, INT8) == int8
         assert f(256, 64) == OK                  # gate+up at 256: slots of 128 x 512 columns
         assert mix(64) == base[64] + 3 * slot64
-        assert f(64, 256) == OK                  # down at 256: 128 x 256 columns
-        assert mix(64) == base[64] + slot64
+        assert f(64, 256) == OK                  # down at 256 on pairs: two tiles, 128 x 512 columns
+        assert mix(64) == base[64] + 3 * slot64
         assert f(128, 0) == OK                   # gate+up at 128: 128 x 256; down by shape (64)
         assert mix(64) == base[64] + slot64
         assert f(192, 192) == OK                 # gate+up at 192: 128 x 384 columns
