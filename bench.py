@@ -285,7 +285,8 @@ def expert_ffn(moe, cfg, L, xg, r, Y, ws, stream):
 
 # ------------------------------------------------------------------ workload
 # The (config, T) points of the sweep: every expert shape and token count of the five workloads.
-SWEEP_CONFIGS = ("mixtral8x7b", "mixtral8x22b", "mixtral8x22b_skew", "dsv3", "qwen3_int8", "mixtral8x7b_prefill")
+SWEEP_CONFIGS = ("mixtral8x7b", "mixtral8x22b", "mixtral8x22b_skew", "dsv3", "qwen3_int8", "mixtral8x7b_prefill",
+                 "dsv3_prefill")
 L2_BYTES = 129e6
 
 

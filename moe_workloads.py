@@ -83,6 +83,8 @@ CONFIGS: Dict[str, MoEConfig] = {
         # tokens, HiNa-MoE §8.2 "Prefill Phase", Table 4): 64 to 1024 tokens per expert, where the
         # expert FFN is a real contraction and is timed in TFLOP/s.
         MoEConfig("mixtral8x7b_prefill", 4096, 14336, 8, 2, "bf16", (256, 1024, 2048, 4096)),
+        # The DeepSeek-V3 expert shape at prefill sizes: 128 and 256 tokens per expert over 256 experts.
+        MoEConfig("dsv3_prefill", 7168, 2048, 256, 8, "bf16", (4096, 8192)),
         MoEConfig("qwen3_int8", 4096, 1536, 128, 8, "int8", (1, 8, 64, 256)),
         MoEConfig("qwen3_int8_residual", 4096, 1536, 128, 8, "int8_residual", (1, 8, 64, 256)),
     )
