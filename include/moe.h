@@ -258,6 +258,17 @@ moe_status_t moe_set_expert_pass_tokens(int gate_up, int down);
 moe_status_t moe_test_expire_grid_barrier(int enable, uint64_t wait_ns);
 
 /*
+ * Failure-detection test hook; the paper has no counterpart. wait_ns (100 ns .. 2 s, or 0 for the
+ * normal 2 s) limits the pipeline waits of the BF16 expert kernels that run on single CTAs (passes of
+ * 64 tokens): a wait for a tile or an accumulator that runs out records a nonzero status in the
+ * workspace status word, the CTA's MMA issuer stops, its producer drains the copies it issued (those
+ * waits keep the full limit, so no copy outlives its CTA), and the kernel returns (outputs undefined;
+ * the GPU and the context stay usable). Zero the workspace before its next use. Process-wide; affects
+ * only later calls. Returns MOE_ERR_INVALID_ARG for other values.
+ */
+moe_status_t moe_test_expert_wait_limit(uint64_t wait_ns);
+
+/*
  * Kernels one moe_ffn_forward call launches for these sizes under the current policy
  * (1 for the one-launch decode step), or -1 when the sizes are invalid. Host only.
  */

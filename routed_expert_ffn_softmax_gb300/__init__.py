@@ -27,7 +27,7 @@ __all__ = [
     "moe_expert_ffn", "moe_combine", "moe_ffn_forward", "alloc_workspace", "workspace_status",
     "moe_expert_ffn_noalloc", "moe_expert_ffn_noalloc_status", "moe_gqa_workspace_size", "moe_gqa_decode", "alloc_gqa_workspace",
     "moe_expert_ffn_residual", "moe_ffn_forward_residual", "moe_set_decode_step_policy", "moe_ffn_forward_launches",
-    "moe_test_expire_grid_barrier", "moe_set_expert_pass_tokens",
+    "moe_test_expire_grid_barrier", "moe_set_expert_pass_tokens", "moe_test_expert_wait_limit",
 ]
 
 MOE_W_BF16 = 0
@@ -184,6 +184,15 @@ def moe_set_expert_pass_tokens(gate_up: int = 0, down: int = 0) -> None:
     f.argtypes = [ctypes.c_int, ctypes.c_int]
     f.restype = ctypes.c_int
     _check("moe_set_expert_pass_tokens", f(int(gate_up), int(down)))
+
+
+def moe_test_expert_wait_limit(wait_ns: int = 0) -> None:
+    """Failure-detection test hook: limit of the BF16 single-CTA expert kernels' pipeline waits (ns; 0 =
+    the normal 2 s). A short limit makes the waits run out: nonzero workspace status (see include/moe.h)."""
+    f = load().moe_test_expert_wait_limit
+    f.argtypes = [ctypes.c_uint64]
+    f.restype = ctypes.c_int
+    _check("moe_test_expert_wait_limit", f(int(wait_ns)))
 
 
 def moe_test_expire_grid_barrier(enable: bool, wait_ns: int = 2_000_000_000) -> None:

@@ -133,6 +133,8 @@ std::atomic<int> g_decode_policy{0};
 // moe_test_expire_grid_barrier: extra arrivals the decode step's grid barrier waits for, and its wait limit.
 std::atomic<int> g_grid_extra{0};
 std::atomic<unsigned long long> g_grid_wait_ns{2000000000ull};
+// moe_test_expert_wait_limit: limit of the BF16 single-CTA expert kernels' pipeline waits (0 = normal).
+std::atomic<unsigned long long> g_expert_wait_ns{0};
 
 // Whether moe_ffn_forward runs the fused one-launch decode step for these sizes.
 bool use_decode_step(int T, int H, int I, int E, int top_k, moe_wtype_t wtype, bool residual) {
@@ -194,6 +196,7 @@ moe_status_t run_expert_ffn(const uint16_t* xg, const int32_t* offsets, const in
   plan.partials = reinterpret_cast<float*>(ws + L.partials);
   plan.partial_slot = L.partial_slot;
   plan.passes = L.passes;
+  plan.wait_ns = g_expert_wait_ns.load(std::memory_order_relaxed);
   plan.counters = reinterpret_cast<int32_t*>(ws + L.ctrl + kCountersOffset);
   plan.status = reinterpret_cast<int32_t*>(ws + L.ctrl);
   plan.num_ctas = sms < kMaxCtas ? sms : kMaxCtas;
@@ -443,6 +446,12 @@ moe_status_t moe_set_expert_pass_tokens(int gate_up, int down) {
   auto ok = [](int n) { return n == 0 || n == 64 || n == 128 || n == 192 || n == 256; };
   if (!ok(gate_up) || !ok(down)) return MOE_ERR_INVALID_ARG;
   moe::set_pass_tokens(gate_up, down);
+  return MOE_OK;
+}
+
+moe_status_t moe_test_expert_wait_limit(uint64_t wait_ns) {
+  if (wait_ns != 0 && (wait_ns < 100ull || wait_ns > 2000000000ull)) return MOE_ERR_INVALID_ARG;
+  g_expert_wait_ns.store(wait_ns, std::memory_order_relaxed);
   return MOE_OK;
 }
 

@@ -154,6 +154,7 @@ extern "C" moe_status_t moe_expert_ffn_noalloc(const uint16_t* xg, const int32_t
   plan.partials = reinterpret_cast<float*>(scratch + kPartialsOffset);
   plan.partial_slot = moe::kPartialSlotFloats;
   plan.passes = moe::PassTokens{64, 64};
+  plan.wait_ns = 0;
   plan.counters = reinterpret_cast<int32_t*>(scratch + kCountersOffset);
   plan.status = reinterpret_cast<int32_t*>(scratch);
   plan.num_ctas = sms < kCtas ? sms : kCtas;

@@ -249,6 +249,7 @@ cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int64_t slot = p.partial_slot > kPartialSlotFloats ? p.partial_slot : kPartialSlotFloats;
   tc::Args a{};
+  a.wait_ns = p.wait_ns;
   a.offsets = p.offsets;
   a.active = p.active;
   a.num_active = p.num_active;

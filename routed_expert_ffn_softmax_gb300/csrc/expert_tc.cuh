@@ -126,6 +126,10 @@ struct Args {
   const float* s0r;
   const float* s1r;
   int kq;
+  // Limit of the pipeline waits in ns (0 = kWaitLimitNs). A failure-detection test shortens it so
+  // that the waits run out; only single-CTA kernels take it (a pair's copies complete on the even
+  // CTA's barriers, so a pair could not drain its own copies after a short wait gave up).
+  uint64_t wait_ns;
 };
 
 struct Unit {
@@ -216,6 +220,31 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)
   for (int i = 0; i < 32; ++i) {
     a[i] = __uint_as_float(r[i]);
     b[i] = __uint_as_float(q[i]);
+  }
+}
+
+// try_wait that suspends the thread for at most about hint_ns before returning false.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after limit_ns. The normal limit takes
+// mbar_wait's loop; a shorter one (a failure-detection test) bounds each try and checks the clock
+// after every try, since a plain try_wait may suspend for microseconds by itself.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns >= kWaitLimitNs) return mbar_wait(bar, parity);
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 64)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -416,6 +445,8 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
   const int rank = static_cast<int>(pass_id % ranks);
   const int64_t cta = blockIdx.x;
   const bool leader = half == 0;  // issues the MMAs of a pair (every CTA when not paired)
+  // pipeline waits (the drains of copies and MMAs keep kWaitLimitNs)
+  const uint64_t wait_limit = (!kPair && args.wait_ns != 0) ? args.wait_ns : kWaitLimitNs;
   const bool waves = G::kNMax >= 128 && U >= 2 * ncols;
   const int64_t NC = waves ? ncols : (U * KI < ncols ? U * KI : ncols);
   const int64_t nW = (waves && col < NC) ? U / NC - 1 : 0;          // whole-unit waves of this column
@@ -561,7 +592,7 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
     }
     for (int64_t i = npre; i < n_stages; ++i) {
       bool drained = true;
-      if (lane == 0) drained = mbar_wait(&empty[stage], phase ^ 1);
+      if (lane == 0) drained = mbar_wait_for(&empty[stage], phase ^ 1, wait_limit);
       drained = __shfl_sync(0xffffffffu, drained, 0);
       if (!drained) {
         ok = false;
@@ -615,33 +646,36 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
         if constexpr (kPair) umma_commit_pair(bar);
         else umma_commit(bar);
       };
-      for (int64_t piece = 0; piece < n_pieces; ++piece) {
+      // A wait that gives up stops the issuer for good: a stage it has not seen full is never handed
+      // back, so the producer cannot re-arm a stage whose copies are still in flight (its own wait for
+      // that stage then runs out, and it drains the copies it issued).
+      for (int64_t piece = 0; piece < n_pieces && ok; ++piece) {
         const Piece pc = piece_of(piece);
         const int b = G::kAccBufs == 2 ? static_cast<int>(piece & 1) : 0;
         for (int kk = pc.kb; kk < pc.ke; ++kk) {
           const bool first = kk == pc.kb;
-          if (first && ok) {
-            if (!mbar_wait(&acc_empty[b], static_cast<uint32_t>(((piece / G::kAccBufs) & 1) ^ 1))) {
+          if (first) {
+            if (!mbar_wait_for(&acc_empty[b], static_cast<uint32_t>(((piece / G::kAccBufs) & 1) ^ 1), wait_limit)) {
               ok = false;
               atomicExch(args.status, kStatusWaitEmptyTimeout);
+              break;
             }
             tc_fence_after_sync();
           }
-          if (ok && !mbar_wait(&full[stage], phase)) {
+          if (!mbar_wait_for(&full[stage], phase, wait_limit)) {
             ok = false;
             atomicExch(args.status, kStatusWaitFullTimeout);
+            break;
           }
-          if (ok) {
-            tc_fence_after_sync();
-            const uint32_t st = smem_base + stage * G::kStage;
-            const uint32_t d = tmem_base + b * G::kAccCols;
+          tc_fence_after_sync();
+          const uint32_t st = smem_base + stage * G::kStage;
+          const uint32_t d = tmem_base + b * G::kAccCols;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              const uint64_t db = umma_desc_sw128(st + G::kWBytes + 32 * s);
-              const bool acc = !(first && s == 0);
-              mma(d, umma_desc_sw128(st + 32 * s), db, acc);
-              if (G::kTwoA) mma(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, acc);
-            }
+          for (int s = 0; s < 4; ++s) {
+            const uint64_t db = umma_desc_sw128(st + G::kWBytes + 32 * s);
+            const bool acc = !(first && s == 0);
+            mma(d, umma_desc_sw128(st + 32 * s), db, acc);
+            if (G::kTwoA) mma(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, acc);
           }
           commit(&empty[stage]);  // frees the stage (of both CTAs) once these MMAs have read it
           if (++stage == G::kStages) {
@@ -649,7 +683,7 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
             phase ^= 1;
           }
         }
-        commit(&acc_full[b]);
+        if (ok) commit(&acc_full[b]);
       }
       // every issued MMA has finished before TMEM is released
       commit(mma_done);
@@ -676,7 +710,7 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
       const Piece pc = piece_of(piece);
       const Unit un = decode(pc.u);
       const int b = G::kAccBufs == 2 ? static_cast<int>(piece & 1) : 0;
-      if (ok && !mbar_wait(&acc_full[b], static_cast<uint32_t>((piece / G::kAccBufs) & 1))) {
+      if (ok && !mbar_wait_for(&acc_full[b], static_cast<uint32_t>((piece / G::kAccBufs) & 1), wait_limit)) {
         ok = false;
         atomicExch(args.status, kStatusWaitFullTimeout);
       }

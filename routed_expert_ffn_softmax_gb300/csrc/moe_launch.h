@@ -95,6 +95,7 @@ struct ExpertFfnPlan {
   int64_t partial_slot;  // fp32 per slot (at least kPartialSlotFloats)
   PassTokens passes;     // BF16: tokens per pass; a size whose partials need more than partial_slot
                          // falls back to 64
+  uint64_t wait_ns;      // BF16 single-CTA kernels: limit of their pipeline waits (0 = the normal 2 s)
   int32_t* counters;  // zeroed, kMaxCtas entries
   int32_t* status;
   int num_ctas;

@@ -50,7 +50,7 @@ def test_header_declares_the_boundary():
         "moe_expert_ffn", "moe_expert_ffn_noalloc", "moe_expert_ffn_noalloc_status", "moe_combine", "moe_ffn_forward",
         "moe_gqa_workspace_size", "moe_gqa_decode", "moe_expert_ffn_residual", "moe_ffn_forward_residual",
         "moe_set_decode_step_policy", "moe_ffn_forward_launches", "moe_test_expire_grid_barrier",
-        "moe_set_expert_pass_tokens"])
+        "moe_set_expert_pass_tokens", "moe_test_expert_wait_limit"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -265,6 +265,18 @@ def test_pass_tokens_size_the_workspace(lib):
     assert auto[1024] == base[1024] + 2 * slot64  # 256 per expert: 192 (the largest expert needs 2 ranks either way)
     assert auto[4096] == base[4096] + 3 * slot64  # 1024 per expert: 256 (at 192 it would need a sixth rank)
     assert mix(1024) == auto[1024]
+
+
+def test_expert_wait_limit_hook_arguments(lib):
+    f = lib.moe_test_expert_wait_limit
+    f.argtypes = [ctypes.c_uint64]
+    f.restype = ctypes.c_int
+    try:
+        assert f(50) == INVALID                # below 100 ns
+        assert f(3 * 10**9) == INVALID         # above the normal 2 s limit
+        assert f(1000) == OK
+    finally:
+        assert f(0) == OK
 
 
 def test_grid_barrier_test_hook_arguments(lib):
