@@ -102,11 +102,25 @@ struct Shared {
   float red[2][kComputeWarps][kMaxNEAll];
 };
 
-template <bool kInt8>
-constexpr int smem_bytes() {
-  return Geo<kInt8>::kStages * Geo<kInt8>::kSlot + static_cast<int>(sizeof(Shared));
+// INT8 at one token (kNE = 1): the token's records stay in shared memory for the whole step (written
+// once by the compute warps, H / 128 records of kRec bytes after Shared), so a gate+up slot carries
+// only weights and scales and its copies need not wait for the records; the ring has four slots to
+// make room. Measured on GB300, the first gate+up slot landed ~9 us after routing when its token
+// slice had to be written to global memory and copied back.
+template <bool kInt8, int kNE>
+struct GeoN : Geo<kInt8> {
+  static constexpr bool kRecSmem = kInt8 && kNE == 1;
+  static constexpr int kStages = kRecSmem ? 4 : Geo<kInt8>::kStages;
+};
+
+constexpr int kSharedBytes = (static_cast<int>(sizeof(Shared)) + 15) / 16 * 16;
+template <bool kInt8, int kNE>
+constexpr int smem_bytes(int H) {
+  return GeoN<kInt8, kNE>::kStages * Geo<kInt8>::kSlot + kSharedBytes + (GeoN<kInt8, kNE>::kRecSmem ? (H / 128) * kRec : 0);
 }
-static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "dynamic shared memory per CTA");
+static_assert(smem_bytes<false, 8>(0) <= 232448 && smem_bytes<true, 4>(0) <= 232448 &&
+                  smem_bytes<true, 1>(16384) <= 232448,
+              "dynamic shared memory per CTA");
 
 // Stream-K by cost: a tile of a pass with n tokens costs max(kCostMem, kCostBase + kCostTok * n), its
 // HBM time or its compute warps' time, whichever is longer (the compute grows with the tokens: on GB300
@@ -231,9 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSG,
                        const __grid_constant__ CUtensorMap tmSU, const __grid_constant__ CUtensorMap tmSD,
                        const DecodeArgs a) {
-  using G = Geo<kInt8>;
+  using G = GeoN<kInt8, kNE>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Shared& S = *reinterpret_cast<Shared*>(smem + G::kStages * G::kSlot);
+  uint8_t* const rec_smem = smem + G::kStages * G::kSlot + kSharedBytes;  // kRecSmem: the token's records
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -462,7 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mx = warp_max_abs(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
         const int kx = fixed_exponent(mx);
         const int X0 = fixed_value(f0, kx), X1 = fixed_value(f1, kx), X2 = fixed_value(f2, kx), X3 = fixed_value(f3, kx);
-        uint8_t* rec = reinterpret_cast<uint8_t*>(a.x16) + (static_cast<int64_t>(t) * ng + g) * kRec;
+        uint8_t* rec = G::kRecSmem ? rec_smem + g * kRec  // one token (T = 1)
+                                   : reinterpret_cast<uint8_t*>(a.x16) + (static_cast<int64_t>(t) * ng + g) * kRec;
         // plane p, elements 4 lane .. 4 lane + 3: bytes of (X >> 8 p)
 #pragma unroll
         for (int p = 0; p < 3; ++p) {
@@ -472,8 +488,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) *reinterpret_cast<float*>(rec + kRecScale) = ldexpf(1.0f, kx);
       }
-      fence_proxy_async_global();  // the producer's bulk copies of these records come after the barrier
-      named_bar_sync(1, kThreads);
+      if constexpr (G::kRecSmem) {
+        named_bar_sync(3, kComputeThreads);  // the compute warps read the records from shared memory
+      } else {
+        fence_proxy_async_global();  // the producer's bulk copies of these records come after the barrier
+        named_bar_sync(1, kThreads);
+      }
     }
   }
 
@@ -525,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto weights_gu = [&](int sl, const GuCursor& c) {
         uint8_t* st = slots + sl * G::kSlot;
-        mbar_arrive_expect_tx(&S.full[sl], G::kWBytes + G::kScaleBytes + c.un.n * G::kSliceGU);
+        mbar_arrive_expect_tx(&S.full[sl], G::kWBytes + G::kScaleBytes + (G::kRecSmem ? 0 : c.un.n * G::kSliceGU));
         tma_load_3d(st, &tmG, &S.full[sl], c.kk * G::kKt, c.un.rb * 128, c.un.e, pol);
         tma_load_3d(st + 16384, &tmU, &S.full[sl], c.kk * G::kKt, c.un.rb * 128, c.un.e, pol);
         if (kInt8) {
@@ -534,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto tokens_gu = [&](int sl, const GuCursor& c) {
+        if constexpr (G::kRecSmem) return;  // the records are in shared memory already
         uint8_t* st = slots + sl * G::kSlot;
 #pragma unroll
         for (int t = 0; t < kNE; ++t)
@@ -560,9 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (kInt8) named_bar_sync(1, kThreads);
+      if (kInt8 && !G::kRecSmem) named_bar_sync(1, kThreads);
       if (lane == 0) {
-      if (kInt8) {  // the records are written: the first ring's token slices
+      if (kInt8 && !G::kRecSmem) {  // the records are written: the first ring's token slices
         GuCursor c = first;
         rows_of(c.un);
         for (int64_t j = 0; j < npre; ++j) {
@@ -838,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < kNE; ++t) {
             if (t < un.n) {
-              const uint32_t rec = st + G::kTokOff + t * G::kSliceGU;
+              const uint32_t rec = G::kRecSmem ? smem_addr(rec_smem) + kk * kRec : st + G::kTokOff + t * G::kSliceGU;
               const float xsc = lds_f32(rec + kRecScale);  // the record's 2^e
               acc[t][0] = fmaf(record_dot(rec, ca, cb, gq), sg * xsc, acc[t][0]);
               acc[t][1] = fmaf(record_dot(rec, ca, cb, uq), su * xsc, acc[t][1]);
@@ -1033,12 +1054,11 @@ cudaError_t prepare(int* max_ctas) {
       return cudaSuccess;
     }
   }
-  e = cudaFuncSetAttribute(decode_step_kernel<kInt8, kNE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem_bytes<kInt8>());
+  e = cudaFuncSetAttribute(decode_step_kernel<kInt8, kNE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
   if (e != cudaSuccess) return e;
   int per_sm = 0, sms = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_step_kernel<kInt8, kNE>, kThreads,
-                                                    smem_bytes<kInt8>());
+                                                    smem_bytes<kInt8, kNE>(16384));
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
@@ -1091,7 +1111,7 @@ cudaError_t launch(const DecodePlan& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<kInt8>();
+  cfg.dynamicSmemBytes = smem_bytes<kInt8, kNE>(p.H);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_ok.load(std::memory_order_relaxed) ? 2 : 1;
@@ -1111,6 +1131,7 @@ bool decode_step_supported(int T, int H, int I, int E, int k, bool int8) {
   if (T < 1 || T > kDecodeMaxT || static_cast<int64_t>(T) * k > kDecodeMaxP || E > 256) return false;
   if (H % 128 || I % 128) return false;
   if (int8 && (H % 512 || I % 512)) return false;  // scale boxes of 4 groups; two groups per down slot
+  if (int8 && T == 1 && H > 16384) return false;     // the token's records in shared memory
   return true;
 }
 
