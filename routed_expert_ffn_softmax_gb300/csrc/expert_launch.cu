@@ -220,7 +220,7 @@ cudaError_t launch_tc_pass(int pass, int64_t slot, const CUtensorMap& a0, const 
   if (pass == 192) return launch_tc_kernel<kPairKind, 192, true>(a0, a1, tokens, K, P, args, num_ctas, s);
   if (pass == 128) return launch_tc_kernel<kPairKind, 128, true>(a0, a1, tokens, K, P, args, num_ctas, s);
   args.partial_stride = kPartialSlotFloats;
-  return launch_tc_kernel<kGateUp ? tc::kGateUp : tc::kDown, 64, false>(a0, a1, tokens, K, P, args, num_ctas, s);
+  return launch_tc_kernel<kGateUp ? tc::kGateUp : tc::kDownK2, 64, false>(a0, a1, tokens, K, P, args, num_ctas, s);
 }
 
 std::atomic<int> g_pass_gate_up{0}, g_pass_down{0};

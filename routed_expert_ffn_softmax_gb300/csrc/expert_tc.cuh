@@ -48,12 +48,16 @@ constexpr int kMaxRanks = 8;           // passes sharing one weight block (BF16,
 // kDown2 (two 128-row tiles of down per stage, on pairs: a unit is 256 rows per CTA, so a stage
 // carries as many weight bytes per token byte as gate+up; down on single tiles ran its tensor pipe
 // at 59% at prefill sizes, bounded by the token tile's L2 stream).
-constexpr int kDown = 0, kGateUp = 1, kDown2 = 2;
+// kDownK2: down on a single CTA with two consecutive 64-element reduction slices per stage (32 KB of
+// weights and two token tiles), one accumulator: on GB300, TMA copies from HBM in 16 KB stages topped
+// out near 6.5 TB/s, and down at one token per expert ran at 70% of the copy rate against gate+up's 83%.
+constexpr int kDown = 0, kGateUp = 1, kDown2 = 2, kDownK2 = 3;
 
 template <int kKind, int kN = 64, bool kPair = false>
 struct Geo {
   static constexpr bool kGU = kKind == kGateUp;
-  static constexpr bool kTwoA = kKind != kDown;             // two weight tiles (accumulators) per stage
+  static constexpr bool kTwoA = kKind == kGateUp || kKind == kDown2;  // two weight tiles, two accumulators
+  static constexpr bool kTwoK = kKind == kDownK2;           // two reduction slices per stage, one accumulator
   // Epilogue warps: on pairs two per TMEM lane quarter, taking alternate groups of accumulator
   // columns, so a unit's accumulators drain in half the time (gate+up holds one accumulator buffer
   // at 256-token passes, and its MMAs wait for the drain); at 64-token passes one per quarter
@@ -64,10 +68,11 @@ struct Geo {
   static constexpr int kUnitRows = 128 * kCtas * (kKind == kDown2 ? 2 : 1);  // weight rows per unit
   static constexpr int kSecondRows = 128 * kCtas;           // kDown2: row offset of a stage's second tile
   static constexpr int kNMax = kN;                          // tokens per pass
-  static constexpr int kKStage = 64;                        // reduction elements per stage
-  static constexpr int kWBytes = kTwoA ? 32768 : 16384;     // this CTA's weight bytes per stage
+  static constexpr int kKStage = kTwoK ? 128 : 64;          // reduction elements per stage
+  static constexpr int kWBytes = (kTwoA || kTwoK) ? 32768 : 16384;  // this CTA's weight bytes per stage
   static constexpr int kBRows = kN / kCtas;                 // this CTA's token rows per stage, at most
-  static constexpr int kBBytes = kBRows * 128;              // token tile: kBRows rows x 64 elements x 2 B
+  static constexpr int kBSlice = kBRows * 128;              // token tile: kBRows rows x 64 elements x 2 B
+  static constexpr int kBBytes = (kTwoK ? 2 : 1) * kBSlice;
   // The launch's token tile is a multiple of 16 rows per CTA. Measured on GB300, TMA moves 2 KB
   // boxes from L2 at a quarter of the rate of 16 KB ones, and fewer boxes per stage beat fewer
   // bytes: a pair loads its whole token slot (kBRows rows, rows past its share never read) as one
@@ -509,7 +514,7 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    const int bbytes = kPair ? G::kBBytes : b_rows * 128;
+    const int bbytes = kPair ? G::kBBytes : (G::kTwoK ? 2 : 1) * b_rows * 128;
     // both CTAs' bytes of a stage complete the even CTA's barrier (kCtas x this CTA's share)
     const uint32_t stage_tx = G::kCtas * (G::kWBytes + bbytes);
     auto issue_a = [&](int stg, const Unit& w, int kk) {
@@ -525,6 +530,7 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
       } else {
         tma_load_3d(st, &tmA0, &full[stg], kk * G::kKStage, row, w.e, policy);
         if (G::kTwoA) tma_load_3d(st + 16384, a1, &full[stg], kk * G::kKStage, row1, w.e, policy);
+        if (G::kTwoK) tma_load_3d(st + 16384, &tmA0, &full[stg], kk * G::kKStage + 64, row, w.e, policy);
       }
     };
     auto issue_b = [&](int stg, const Unit& w, int kk) {
@@ -533,12 +539,15 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
       if constexpr (kPair) {
         tma_load_2d_pair(sb_, &tmB.m[0], leader_barrier(&full[stg]), kk * G::kKStage, r0);
       } else {
-        int j = 0;
 #pragma unroll
-        for (int m = 1; m < 4; ++m) {  // b_rows (a multiple of 16, at most 64) as a sum of box heights
-          if (b_rows - j >= (128 >> m)) {
-            tma_load_2d(sb_ + j * 128, &tmB.m[m], &full[stg], kk * G::kKStage, r0 + j);
-            j += 128 >> m;
+        for (int sl = 0; sl < (G::kTwoK ? 2 : 1); ++sl) {  // each 64-element reduction slice of the stage
+          int j = 0;
+#pragma unroll
+          for (int m = 1; m < 4; ++m) {  // b_rows (a multiple of 16, at most 64) as a sum of box heights
+            if (b_rows - j >= (128 >> m)) {
+              tma_load_2d(sb_ + sl * G::kBSlice + j * 128, &tmB.m[m], &full[stg], kk * G::kKStage + 64 * sl, r0 + j);
+              j += 128 >> m;
+            }
           }
         }
       }
@@ -676,6 +685,11 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
             const bool acc = !(first && s == 0);
             mma(d, umma_desc_sw128(st + 32 * s), db, acc);
             if (G::kTwoA) mma(d + G::kNMax, umma_desc_sw128(st + 16384 + 32 * s), db, acc);
+          }
+          if constexpr (G::kTwoK) {  // the stage's second reduction slice, into the same accumulator
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma(d, umma_desc_sw128(st + 16384 + 32 * s), umma_desc_sw128(st + G::kWBytes + G::kBSlice + 32 * s), true);
           }
           commit(&empty[stage]);  // frees the stage (of both CTAs) once these MMAs have read it
           if (++stage == G::kStages) {
