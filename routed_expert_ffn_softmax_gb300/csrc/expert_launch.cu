@@ -239,7 +239,8 @@ int pass_by_mean(int64_t P, int E) {
 }
 int valid_pass(int n) { return n == 64 || n == 128 || n == 192 || n == 256 ? n : 0; }
 
-// BF16: weight boxes of 128 rows by 128 bytes, token boxes of 16 rows (64-token passes) or 32.
+// BF16: weight boxes of 128 rows by 128 bytes; token boxes of 64/32/16 rows (single CTAs) or one box of a
+// pair CTA's whole token slot (tc::TokenMaps).
 cudaError_t launch_tc(const ExpertFfnPlan& p, cudaStream_t s) {
   CUtensorMap tg, tu, td;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;

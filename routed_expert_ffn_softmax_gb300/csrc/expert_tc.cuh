@@ -17,8 +17,8 @@
 //   warps 2..   epilogue (4 warps, 8 on pairs): TMEM -> registers (thread = weight row), SiLU(g)*u
 //               -> h (gate+up) or Y (down), or the fp32 partial of a unit that another column
 //               finishes.
-// Accumulators are double buffered in TMEM where two fit (not gate+up at 256-token passes), so the
-// epilogue of one unit overlaps the MMAs of the next. Gate and up of the same 128 rows go to
+// Accumulators are double buffered in TMEM where two fit (gate+up and two-tile down hold one at 192-
+// and 256-token passes), so the epilogue of one unit overlaps the MMAs of the next. Gate and up of the same 128 rows go to
 // adjacent column ranges of one buffer, so every epilogue thread holds g and u of the same
 // intermediate index.
 // Args, Unit and the schedule table size are shared with the INT8 pair kernels (expert_pair.cuh).
@@ -42,9 +42,10 @@ constexpr int kMaxRanks = 8;           // passes sharing one weight block (BF16,
 // kPair: the pass runs on a CTA pair (a cluster of two) with tcgen05.mma cta_group::2, M = 256: each
 // CTA holds 128 weight rows of a 256-row block and half of the pass's token rows, and the even CTA
 // issues MMAs that read both CTAs' tiles and write each CTA's 128 rows into its own TMEM. Per CTA a
-// stage then carries half the token bytes for the same tensor work, which is what bounds these
-// kernels at prefill sizes (bytes in flight per SM against L2 latency, measured on GB300).
-// kKind: kDown (one 128-row weight tile per stage), kGateUp (gate and up tiles of the same rows),
+// stage then carries half the token bytes for the same tensor work: at prefill sizes these kernels
+// are bound by the L2 -> shared-memory stream of their stages, not by DRAM (measured on GB300).
+// kKind: kDown (one 128-row weight tile per stage: the plain form, which the launches no longer use),
+// kGateUp (gate and up tiles of the same rows),
 // kDown2 (two 128-row tiles of down per stage, on pairs: a unit is 256 rows per CTA, so a stage
 // carries as many weight bytes per token byte as gate+up; down on single tiles ran its tensor pipe
 // at 59% at prefill sizes, bounded by the token tile's L2 stream).
