@@ -173,7 +173,8 @@ def moe_ffn_forward(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, top_k
 
 
 def moe_set_decode_step_policy(policy: int) -> None:
-    """0: by batch shape (default); 1: never the one-launch decode step; 2: whenever the sizes allow."""
+    """0: by batch shape (default: the one-launch decode step for INT8 at T = 1 only); 1: never; 2: whenever
+    the sizes allow."""
     _check("moe_set_decode_step_policy", load().moe_set_decode_step_policy(policy))
 
 

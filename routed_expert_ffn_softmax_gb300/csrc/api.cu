@@ -136,13 +136,16 @@ std::atomic<unsigned long long> g_grid_wait_ns{2000000000ull};
 // moe_test_expert_wait_limit: limit of the BF16 single-CTA expert kernels' pipeline waits (0 = normal).
 std::atomic<unsigned long long> g_expert_wait_ns{0};
 
-// Whether moe_ffn_forward runs the fused one-launch decode step for these sizes.
+// Whether moe_ffn_forward runs the fused one-launch decode step for these sizes: by batch shape
+// (policy 0) only INT8 weights at one token, where it measured 2855 GB/s against 2778 for the
+// separate launches on GB300 (Qwen3-235B shapes; end to end with host buffers 2836 against ~2400);
+// at 8 INT8 tokens and for BF16 the separate launches were faster.
 bool use_decode_step(int T, int H, int I, int E, int top_k, moe_wtype_t wtype, bool residual) {
   const int policy = g_decode_policy.load(std::memory_order_relaxed);
   if (policy == 1 || residual) return false;
   if (!moe::decode_step_supported(T, H, I, E, top_k, wtype == MOE_W_INT8_G128)) return false;
   if (H / 128 > kMaxRowBlocks) return false;
-  return policy == 2;
+  return policy == 2 || (wtype == MOE_W_INT8_G128 && T == 1);
 }
 
 // Residual-split parts of gate and up (INT8 only); all null when the weights are not split.

@@ -35,6 +35,20 @@ __device__ __forceinline__ void tma_load_3d_plain(void* dst, const CUtensorMap* 
 
 // Order this thread's generic-proxy global writes before later async-proxy (bulk copy) reads, and
 // the acquire of another CTA's release before this thread's later async-proxy reads.
+// mbarrier try_wait that suspends for at most ~64 ns: for a thread that must also poll something else
+// (a plain try_wait may suspend for microseconds before it returns false).
+__device__ __forceinline__ bool mbar_try_wait_short(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(64)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }

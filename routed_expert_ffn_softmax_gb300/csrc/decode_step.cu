@@ -628,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the grid barrier has been passed: every CTA's h is written (acquire, then order the async
       // proxy's later reads after it)
       auto barrier_ready = [&]() -> bool {
-        if (!mbar_try_wait(&S.gbar_arrived, 0)) return false;
+        if (!mbar_try_wait_short(&S.gbar_arrived, 0)) return false;
         return ld_acquire_gpu(a.gbar + 1) != *reinterpret_cast<volatile int*>(&S.gbar_epoch);
       };
       auto release_pending = [&]() {
@@ -644,8 +644,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t t0 = global_timer_ns();
         uint64_t tb = t0;
         for (;;) {
-          if (mbar_try_wait(&S.empty[slot], ph ^ 1u)) return true;
-          if (!passed && npend > 0) {
+          // while h slices wait for the grid barrier, poll both with short tries (the barrier opening is
+          // what the compute warps wait for; measured ~2.3 us from the last arrival to the release)
+          const bool polling = !passed && npend > 0;
+          if (polling ? mbar_try_wait_short(&S.empty[slot], ph ^ 1u) : mbar_try_wait(&S.empty[slot], ph ^ 1u))
+            return true;
+          if (polling) {
             if (barrier_ready()) {
               release_pending();
               tb = global_timer_ns();
@@ -776,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int m = 0; m < kM; ++m) mine[(t * 2 + m) * 128 + r] = vals[t][m];
       }
-      __threadfence();
+      // every thread's partial stores, then one thread's release (fence, atomic) makes them all visible
       named_bar_sync(2, kComputeThreads);
       if (tid == 0) {
         __threadfence();
@@ -1010,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // this unit's Y rows are final: count it toward its row block, and let the row block's last
       // unit write the combine out[t, rows] = bf16(sum_j w[t, j] * Y[inv_pos[t, j], rows]) in slot order
-      __threadfence();
+      // (the barrier, then one thread's fence and atomic, publish every thread's stores)
       named_bar_sync(2, kComputeThreads);
       if (tid == 0) {
         __threadfence();

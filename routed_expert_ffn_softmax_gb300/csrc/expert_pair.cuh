@@ -416,9 +416,10 @@ __device__ __forceinline__ void promote(uint8_t* smem, uint64_t* empty, uint64_t
         if (G::kGU) mine[(N + n) * kEpiThreads] = acc1[n];
       }
     }
-    __threadfence();
+    // every thread's partial stores, then one thread's release (fence, atomic) makes them all visible
     named_bar_sync(1, kEpiThreads);
     if (etid == 0) {
+      __threadfence();
       int32_t* counter = &args.counters[2 * c_first + rank];
       const int old = atomicAdd(counter, 1);
       const int last = (old == static_cast<int>(c_last - c_first));

@@ -830,9 +830,10 @@ __global__ void __launch_bounds__(Geo<kKind, kN, kPair>::kThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) release_acc(&acc_empty[b]);  // TMEM buffer free again
-        __threadfence();
+        // every thread's partial stores, then one thread's release (fence, atomic) makes them all visible
         named_bar_sync(1, kEpiThreads);
         if (ew == 0 && lane == 0) {
+          __threadfence();
           int32_t* counter = &args.counters[(c_first * ranks + rank) * G::kCtas + half];
           const int old = atomicAdd(counter, 1);
           const int last = (old == static_cast<int>(c_last - c_first));
