@@ -28,7 +28,10 @@
 //                mixed-precision FMAs (fma.rn.f32.bf16 / .f16: exact products, fp32 sums) read
 //                the weights straight from the TMA-filled tile and the tokens from the slot;
 //   warp 16      producer: TMA tensor loads of the weight tiles (and INT8 scale boxes), bulk
-//                copies of the tokens' slices (x for gate+up, h for down) into the same slot.
+//                copies of the tokens' slices (x for gate+up, h for down) into the same slot;
+//   warp 17      helper: the hand-offs that wait on global memory (publishing a split unit's
+//                piece, counting finished down units, the grid barrier's arrival), posted to it by
+//                the compute warps through a small ring in shared memory.
 // INT8 weights become exact fp16 values (one logic op, two byte permutes, two fp16x2 subtractions
 // per four weights); the tokens are fp16 copies of the bf16 values, scaled by a power of two (a row
 // scale for x, a scale per 128-element group for h) that the epilogue multiplies back.
@@ -55,7 +58,14 @@ constexpr int kMaxNEAll = 8;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = 32 * kComputeWarps;  // 128 rows x 4 quarters
 constexpr int kProducerWarp = kComputeWarps;
-constexpr int kThreads = kComputeThreads + 32;
+constexpr int kHelperWarp = kComputeWarps + 1;
+constexpr int kThreads = kComputeThreads + 64;
+constexpr int kBar1Threads = kComputeThreads + 32;  // barrier 1: the compute warps and the producer
+// Hand-off ring between the compute warps and the helper warp: the compute warps post a finished
+// unit piece (or a phase end) and go on; the helper does the part that waits on global memory.
+constexpr int kItems = 8;
+enum : int { kItemGuSplit = 0, kItemDnSplit = 1, kItemDnWhole = 2, kItemGuEnd = 3, kItemEnd = 4 };
+constexpr int kMaxOwed = 128;  // row blocks of the output (H <= 16384)
 // INT8 token record of one 128-element group (x for gate+up, h for down): the group's values as 24-bit
 // fixed-point integers X = round(v * 2^-e), e chosen so that the group's largest |v| * 2^-e lies in
 // [2^22, 2^23), split into three int8 digit planes of 128 bytes (X = d2 * 2^16 + d1 * 2^8 + d0, d0 and d1
@@ -81,9 +91,17 @@ struct Geo {
 struct Shared {
   uint64_t full[8];
   uint64_t empty[8];
-  uint64_t gbar_arrived;  // compute -> producer: this CTA has arrived at the grid barrier
+  uint64_t gbar_arrived;  // helper -> producer: this CTA has arrived at the grid barrier
+  uint64_t item_full[kItems];   // compute -> helper: an item is posted
+  uint64_t item_empty[kItems];  // helper -> compute: the item's entry may be reused
+  uint64_t helper_done;         // helper -> compute: every item is handled
+  struct Item {
+    int ub, ue;  // split pieces: the unit's tile range
+    int kind, p0, n, rb;
+  } items[kItems];
+  int owed[kMaxOwed];     // complete row blocks, posted by the helper: the compute warps write their combine
+  int owed_n;
   int gbar_epoch;         // the barrier's release word as read before arriving
-  int flag;               // broadcast word of the epilogues
   uint32_t need;          // INT8: tokens this CTA converts (bit t)
   int A;                  // active experts
   int ids[kDecodeMaxP];   // token t's experts at t * k .. t * k + k - 1 (slot order)
@@ -100,7 +118,8 @@ struct Shared {
   int qc[kDecodeMaxP];    // cost of one tile of pass q (tile_cost of its tokens)
   int pc[kDecodeMaxP + 1];  // prefix sums of qc
   float red[2][kComputeWarps][kMaxNEAll];
-  long long bounds[4];    // this CTA's gate+up and down tile ranges (computed by one thread)
+  int bounds[4];          // this CTA's gate+up and down tile ranges
+  int split_c[2];         // a range's last piece: the unit's CTAs (first, or -1 if not last; last)
 };
 
 // INT8 at one token (kNE = 1): the token's records stay in shared memory for the whole step (written
@@ -155,6 +174,23 @@ __device__ __forceinline__ Unit unit_of(const Shared& S, int q, int rb) {
   u.n = left < kNE ? left : kNE;
   u.rb = rb;
   return u;
+}
+
+// floor(c * C / N) in 32-bit arithmetic, for 0 <= C < 2^31 and 0 <= c <= N < 2^15 (c * C itself
+// may not fit).
+__device__ __forceinline__ int scaled(int c, int C, int N) {
+  const int q = C / N, r = C - q * N;
+  return c * q + (c * r) / N;
+}
+
+// The CTA that holds cost position pos when C is cut into N ranges [scaled(c), scaled(c + 1)): the
+// last c with scaled(c) <= pos (an fp32 estimate, then exact steps).
+__device__ __forceinline__ int cta_at(int pos, int C, int N) {
+  int c = static_cast<int>(static_cast<float>(pos) * static_cast<float>(N) / static_cast<float>(C));
+  c = c < 0 ? 0 : (c > N - 1 ? N - 1 : c);
+  while (c + 1 < N && scaled(c + 1, C, N) <= pos) ++c;
+  while (c > 0 && scaled(c, C, N) > pos) --c;
+  return c;
 }
 
 // Grid barrier that leaves itself reset: the CTA reads the release word, arrives on the counter, and
@@ -264,6 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.empty[s], kComputeWarps);  // one arrival per compute warp
     }
     mbar_init(&S.gbar_arrived, 1);
+    for (int i = 0; i < kItems; ++i) {
+      mbar_init(&S.item_full[i], 1);
+      mbar_init(&S.item_empty[i], 1);
+    }
+    mbar_init(&S.helper_done, 1);
+    S.owed_n = 0;
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -399,16 +441,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int RBg = I / 128, KIg = H / G::kKt;        // gate+up: rows of I, reduction H
   const int RBd = H / 128, KId = I / (2 * G::kKt);  // down: rows of H, reduction I (two slices per slot)
-  const int64_t TPg = static_cast<int64_t>(RBg) * KIg;  // gate+up tiles of one pass
-  const int64_t Wg = static_cast<int64_t>(NU) * TPg;
-  const int64_t Wd = static_cast<int64_t>(NU) * RBd * KId;
-  const int64_t PC = S.pc[NU];
-  const int64_t Cg = PC * TPg, Rd = PC * KId, Cd = Rd * RBd;  // total costs; Rd: one row block of down
+  // Tile indices and cost positions stay below 2^31 (NU <= 256 passes, H <= 16384, I <= 32768, a tile
+  // costs at most 28), so the schedule is 32-bit arithmetic; the one product that does not fit,
+  // c * C / N, is split (scaled). A 64-bit division is a long dependent chain: a dozen of them on one
+  // thread held the producer's first copy back by ~3 us (measured on GB300 at one token).
+  const int TPg = RBg * KIg;  // gate+up tiles of one pass
+  const int Wg = NU * TPg;
+  const int Wd = NU * RBd * KId;
+  const int PC = S.pc[NU];
+  const int Cg = PC * TPg, Rd = PC * KId, Cd = Rd * RBd;  // total costs; Rd: one row block of down
   // CTAs taking part: each range is at least one tile's cost wide, so every one holds a tile
   constexpr int kMaxCost = tile_cost<kInt8>(kNE);
-  const int64_t Ng = Cg / kMaxCost < N ? (Cg / kMaxCost > 0 ? Cg / kMaxCost : 1) : N;
-  const int64_t Nd = Cd / kMaxCost < N ? (Cd / kMaxCost > 0 ? Cd / kMaxCost : 1) : N;
-  auto pass_at = [&](int64_t X) -> int {  // the last pass q with pc[q] <= X
+  const int Ng = Cg / kMaxCost < N ? (Cg / kMaxCost > 0 ? Cg / kMaxCost : 1) : N;
+  const int Nd = Cd / kMaxCost < N ? (Cd / kMaxCost > 0 ? Cd / kMaxCost : 1) : N;
+  auto pass_at = [&](int X) -> int {  // the last pass q with pc[q] <= X
     int lo = 0, hi = NU - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -418,45 +464,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // cost position of a tile, and the first tile at or past a cost position (gate+up: tiles of pass
   // q at q * TPg .., each costing qc[q]; down: row block rb, then pass q, KId tiles each)
-  auto pos_gu = [&](int64_t i) -> int64_t {
-    const int q = static_cast<int>(i / TPg);
+  auto pos_gu = [&](int i) -> int {
+    const int q = i / TPg;
     return S.pc[q] * TPg + (i - q * TPg) * S.qc[q];
   };
-  auto first_gu = [&](int64_t X) -> int64_t {
+  auto first_gu = [&](int X) -> int {
     if (X >= Cg) return Wg;
     const int q = pass_at(X / TPg);
-    const int64_t base = S.pc[q] * TPg;
-    return q * TPg + (X - base + S.qc[q] - 1) / S.qc[q];
+    return q * TPg + (X - S.pc[q] * TPg + S.qc[q] - 1) / S.qc[q];
   };
-  auto pos_dn = [&](int64_t i) -> int64_t {
-    const int64_t u = i / KId;
-    const int64_t rb = u / NU;
-    const int q = static_cast<int>(u - rb * NU);
-    return rb * Rd + static_cast<int64_t>(S.pc[q]) * KId + (i - u * KId) * S.qc[q];
+  auto pos_dn = [&](int i) -> int {
+    const int u = i / KId, rb = u / NU, q = u - rb * NU;
+    return rb * Rd + S.pc[q] * KId + (i - u * KId) * S.qc[q];
   };
-  auto first_dn = [&](int64_t X) -> int64_t {
+  auto first_dn = [&](int X) -> int {
     if (X >= Cd) return Wd;
-    const int64_t rb = X / Rd, rem = X - rb * Rd;
+    const int rb = X / Rd, rem = X - rb * Rd;
     const int q = pass_at(rem / KId);
-    const int64_t base = static_cast<int64_t>(S.pc[q]) * KId;
-    return (rb * NU + q) * KId + (rem - base + S.qc[q] - 1) / S.qc[q];
+    return (rb * NU + q) * KId + (rem - S.pc[q] * KId + S.qc[q] - 1) / S.qc[q];
   };
-  // The CTA's tile ranges, by one thread: a dozen 64-bit divisions and binary searches in all 544
-  // threads held the producer's first copy back by ~4 us (measured on GB300 at one token).
-  if (tid == 0) {
-    S.bounds[0] = cta < Ng ? first_gu(cta * Cg / Ng) : Wg;
-    S.bounds[1] = cta < Ng ? first_gu((cta + 1) * Cg / Ng) : Wg;
-    S.bounds[2] = cta < Nd ? first_dn(cta * Cd / Nd) : Wd;
-    S.bounds[3] = cta < Nd ? first_dn((cta + 1) * Cd / Nd) : Wd;
+  // The CTA's tile ranges, [first(scaled(cta)), first(scaled(cta + 1))) per phase, one bound per thread
+  if (tid < 4) {
+    const bool dn = tid >= 2;
+    const int Nx = dn ? Nd : Ng, Cx = dn ? Cd : Cg, Wx = dn ? Wd : Wg;
+    const int X = scaled(cta + (tid & 1), Cx, Nx);
+    S.bounds[tid] = cta < Nx ? (dn ? first_dn(X) : first_gu(X)) : Wx;
   }
   __syncthreads();
-  const int64_t g_beg = S.bounds[0], g_end = S.bounds[1];
-  const int64_t d_beg = S.bounds[2], d_end = S.bounds[3];
+  const int g_beg = S.bounds[0], g_end = S.bounds[1];
+  const int d_beg = S.bounds[2], d_end = S.bounds[3];
   // gate+up units are pass-major (q * RBg + rb): a CTA's range touches few experts' tokens;
   // down units are row-block-major (rb * NU + q): a row block's combine becomes ready as soon as
   // its last unit is done, spread over the step instead of all at its end.
-  auto gu_unit = [&](int64_t u) { return unit_of<kNE>(S, static_cast<int>(u / RBg), static_cast<int>(u % RBg)); };
-  auto dn_unit = [&](int64_t u) { return unit_of<kNE>(S, static_cast<int>(u % NU), static_cast<int>(u / NU)); };
+  auto gu_unit = [&](int u) { return unit_of<kNE>(S, u / RBg, u % RBg); };
+  auto dn_unit = [&](int u) { return unit_of<kNE>(S, u % NU, u / NU); };
 
   // INT8: records (the digit planes above) of the token rows this CTA's gate+up tiles read, one per
   // 128-element scale group, the same layout as h's. CTAs that share a token write the same bytes;
@@ -465,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       uint32_t need = 0u;
       if (g_beg < g_end) {
-        const int q0 = static_cast<int>((g_beg / KIg) / RBg), q1 = static_cast<int>(((g_end - 1) / KIg) / RBg);
+        const int q0 = (g_beg / KIg) / RBg, q1 = ((g_end - 1) / KIg) / RBg;
         const Unit u0 = unit_of<kNE>(S, q0, 0), u1 = unit_of<kNE>(S, q1, 0);
         for (int p = u0.p0; p < u1.p0 + u1.n; ++p) need |= 1u << S.sorted[p];
       }
@@ -502,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(3, kComputeThreads);  // the compute warps read the records from shared memory
       } else {
         fence_proxy_async_global();  // the producer's bulk copies of these records come after the barrier
-        named_bar_sync(1, kThreads);
+        named_bar_sync(1, kBar1Threads);
       }
     }
   }
@@ -543,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kNE; ++t) xrow[t] = xbase + S.sorted[un.p0 + (t < un.n ? t : 0)] * xrow_bytes;
       };
-      auto step = [&](GuCursor& c, int64_t i) {  // to tile i + 1
+      auto step = [&](GuCursor& c, int i) {  // to tile i + 1
         if (++c.kk == KIg) {
           c.kk = 0;
           if (++c.rb == RBg) {
@@ -571,18 +612,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t < c.un.n)
             bulk_g2s(st + G::kTokOff + t * G::kSliceGU, xrow[t] + c.kk * G::kSliceGU, G::kSliceGU, &S.full[sl]);
       };
-      const int64_t npre = (g_end - g_beg) < G::kStages ? (g_end - g_beg) : G::kStages;
+      const int npre = (g_end - g_beg) < G::kStages ? (g_end - g_beg) : G::kStages;
       if (g_beg < g_end) {
-        const int64_t u0 = g_beg / KIg;
-        cur.kk = static_cast<int>(g_beg - u0 * KIg);
-        cur.q = static_cast<int>(u0 / RBg);
-        cur.rb = static_cast<int>(u0 - static_cast<int64_t>(cur.q) * RBg);
+        const int u0 = g_beg / KIg;
+        cur.kk = g_beg - u0 * KIg;
+        cur.q = u0 / RBg;
+        cur.rb = u0 - cur.q * RBg;
         cur.un = unit_of<kNE>(S, cur.q, cur.rb);
       }
       const GuCursor first = cur;
       if (lane == 0) {
         rows_of(cur.un);
-        for (int64_t j = 0; j < npre; ++j) {  // a fresh ring: no slot to wait for
+        for (int j = 0; j < npre; ++j) {  // a fresh ring: no slot to wait for
           weights_gu(static_cast<int>(j), cur);
           if (!kInt8) tokens_gu(static_cast<int>(j), cur);  // BF16 reads x itself: each slot whole, in order
           const int q0 = cur.q, rb0 = cur.rb;
@@ -591,12 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (kInt8 && !G::kRecSmem) named_bar_sync(1, kThreads);
+      if (kInt8 && !G::kRecSmem) named_bar_sync(1, kBar1Threads);
       if (lane == 0) {
       if (kInt8 && !G::kRecSmem) {  // the records are written: the first ring's token slices
         GuCursor c = first;
         rows_of(c.un);
-        for (int64_t j = 0; j < npre; ++j) {
+        for (int j = 0; j < npre; ++j) {
           tokens_gu(static_cast<int>(j), c);
           const int q0 = c.q, rb0 = c.rb;
           step(c, g_beg + j);
@@ -604,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         rows_of(cur.un);
       }
-      for (int64_t j = 0; j < npre; ++j) advance();
-      for (int64_t i = g_beg + npre; i < g_end && ok; ++i) {
+      for (int j = 0; j < npre; ++j) advance();
+      for (int i = g_beg + npre; i < g_end && ok; ++i) {
         if (!mbar_wait(&S.empty[slot], ph ^ 1u)) {
           ok = false;
           atomicExch(a.status, kStatusWaitEmptyTimeout);
@@ -676,16 +717,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       if (d_beg < d_end && ok) {
-        const int64_t u0 = d_beg / KId;
-        int kk2 = static_cast<int>(d_beg - u0 * KId);
-        int rb = static_cast<int>(u0 / NU), q = static_cast<int>(u0 - static_cast<int64_t>(rb) * NU);
+        const int u0 = d_beg / KId;
+        int kk2 = d_beg - u0 * KId;
+        int rb = u0 / NU, q = u0 - rb * NU;
         Unit un = unit_of<kNE>(S, q, rb);
         auto h_of = [&]() -> const uint8_t* {
           return kInt8 ? static_cast<const uint8_t*>(a.h) + static_cast<int64_t>(un.p0) * (I / 128) * kRec
                        : static_cast<const uint8_t*>(a.h) + static_cast<int64_t>(un.p0) * I * 2;
         };
         const uint8_t* hsrc = h_of();
-        for (int64_t i = d_beg; i < d_end; ++i) {
+        for (int i = d_beg; i < d_end; ++i) {
           if (!wait_slot()) {
             ok = false;
             atomicExch(a.status, kStatusWaitEmptyTimeout);
@@ -746,6 +787,125 @@ __global__ void __launch_bounds__(kThreads, 1)
       }  // lane 0
     }
     __syncwarp();
+  } else if (warp == kHelperWarp) {
+    // ================================ helper ================================
+    // The part of a unit's end that waits on global memory, in the order the compute warps post it:
+    // a range's first piece of a split unit is published (fence, atomic on the unit's counter) and,
+    // in the CTA that arrives last, the pieces are summed in CTA order and h (gate+up) or Y (down)
+    // written; a finished down unit is counted toward its row block, and the row block's last unit
+    // posts the block's combine to the compute warps; the gate+up phase's end is the arrival at the
+    // grid barrier. Each round trip takes microseconds while HBM streams at full rate (measured on
+    // GB300, ~2.7 us per hand-off), time the compute warps now spend on their next tiles.
+    int it = 0;
+    uint32_t iph = 0;
+    int owed_n = 0;
+    // count a finished down unit toward row block rb; the last one posts the row block's combine
+    auto count_dn = [&](int rb) {
+      __syncwarp();  // the lanes' Y stores before lane 0's release
+      if (lane == 0) {
+        __threadfence();
+        const int old = atomicAdd(&a.ccount[rb], 1);
+        if (old == NU - 1) {
+          a.ccount[rb] = 0;
+          __threadfence();  // acquire: every unit's Y of the row block
+          if (owed_n < kMaxOwed) {
+            S.owed[owed_n] = rb;
+            __threadfence_block();
+            *reinterpret_cast<volatile int*>(&S.owed_n) = ++owed_n;
+          }
+        }
+      }
+      __syncwarp();
+    };
+    for (;;) {
+      if (!mbar_wait(&S.item_full[it], iph)) {
+        if (lane == 0) atomicExch(a.status, kStatusWaitFullTimeout);
+        break;
+      }
+      const Shared::Item m = S.items[it];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.item_empty[it]);
+      if (++it == kItems) {
+        it = 0;
+        iph ^= 1u;
+      }
+      if (m.kind == kItemEnd) break;
+      if (m.kind == kItemGuEnd) {
+        if (lane == 0) {
+          S.gbar_epoch = grid_arrive(a.gbar, N + a.grid_extra);
+          mbar_arrive(&S.gbar_arrived);
+        }
+        __syncwarp();
+        continue;
+      }
+      if (m.kind == kItemDnWhole) {
+        count_dn(m.rb);
+        continue;
+      }
+      // a split piece: publish it; the last of the unit's CTAs (the CTA of a tile: the last c with
+      // c * Ct / Nc <= its cost position) sums all pieces in CTA order
+      const bool gu = m.kind == kItemGuSplit;
+      const int KI = gu ? KIg : KId, Nc = gu ? Ng : Nd, Ct = gu ? Cg : Cd;
+      auto cta_of = [&](int i) -> int { return cta_at(gu ? pos_gu(i) : pos_dn(i), Ct, Nc); };
+      const int c_first = cta_of(m.ub), c_last = cta_of(m.ue - 1);
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();
+        const int old = atomicAdd(&a.counters[c_first], 1);
+        last = old == c_last - c_first;
+        if (last) a.counters[c_first] = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+      __threadfence();
+      // (rare: a range's first piece is normally the unit's first to arrive) the pieces summed in CTA
+      // order, one token at a time; lane: rows lane + 32 j
+      for (int t = 0; t < m.n; ++t) {
+        float v[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+        for (int c = c_first; c <= c_last; ++c) {
+          const int cb = scaled(c, Ct, Nc);
+          const int cs = (m.ub / KI == (gu ? first_gu(cb) : first_dn(cb)) / KI) ? 0 : 1;
+          const float* src = a.partials + (static_cast<int64_t>(c) * 2 + cs) * kPartialSlotFloats + t * 256 + lane;
+#pragma unroll
+          for (int mm = 0; mm < 2; ++mm)
+            if (gu || mm == 0)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[mm][j] += __ldcg(src + mm * 128 + 32 * j);
+        }
+        if (!gu) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a.Y[static_cast<int64_t>(m.p0 + t) * H + m.rb * 128 + lane + 32 * j] = v[0][j];
+        } else if constexpr (!kInt8) {
+          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.h);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            h[static_cast<int64_t>(m.p0 + t) * I + m.rb * 128 + lane + 32 * j] = __float2bfloat16_rn(silu_mul(v[0][j], v[1][j]));
+        } else {
+          // h rounded to bf16, then its record (the 128 rows are one scale group of down's reduction)
+          float hv[4], mx = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            hv[j] = __bfloat162float(__float2bfloat16_rn(silu_mul(v[0][j], v[1][j])));
+            mx = fmaxf(mx, fabsf(hv[j]));
+          }
+          mx = warp_max_abs(mx);
+          const int kh = fixed_exponent(mx);
+          uint8_t* rec = static_cast<uint8_t*>(a.h) + (static_cast<int64_t>(m.p0 + t) * (I / 128) + m.rb) * kRec;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int X = fixed_value(hv[j], kh);
+            const int row = lane + 32 * j;
+            rec[row] = static_cast<uint8_t>(X & 0xff);
+            rec[128 + row] = static_cast<uint8_t>((X >> 8) & 0xff);
+            rec[256 + row] = static_cast<uint8_t>((X >> 16) & 0xff);
+          }
+          if (lane == 0) *reinterpret_cast<float*>(rec + kRecScale) = ldexpf(1.0f, kh);
+        }
+      }
+      if (!gu) count_dn(m.rb);
+      __syncwarp();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.helper_done);
   } else {
     // ================================ compute ================================
     const int r = tid >> 2;  // weight row of the tile
@@ -772,46 +932,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    // Split-unit hand-off: publish this CTA's partial sums (vals[t][m], m < kM) and let the last of
-    // the unit's CTAs sum all pieces in CTA order. Returns true in the CTA that must finish the unit
-    // (vals then holds the full sums in its quarter-0 threads).
-    // pos / first: the phase's cost position of a tile and first tile at a cost position; Nc, Ct: the
-    // CTAs taking part and the total cost (the CTA of a tile: the last c with c * Ct / Nc <= pos).
-    auto split_unit = [&](auto& vals, auto kMc, int64_t ub, int64_t ue, int64_t beg, int64_t KI, auto pos,
-                          auto first, int64_t Nc, int64_t Ct) -> bool {
+    // A piece of a unit split between CTAs: this CTA's partial sums (vals[t][m], m < kM, full in
+    // every quarter after the shuffles) into its partial slot, 0 for the phase's first unit, 1 for
+    // the last; the helper publishes them and, in the CTA that arrives last, sums the pieces.
+    auto publish = [&](auto& vals, auto kMc, bool first_unit) {
       constexpr int kM = decltype(kMc)::value;
-      auto cta_of = [&](int64_t i) -> int64_t { return ((pos(i) + 1) * Nc - 1) / Ct; };
-      const int64_t c_first = cta_of(ub), c_last = cta_of(ue - 1);
-      const int sl = (ub / KI == beg / KI) ? 0 : 1;
-      float* mine = a.partials + (static_cast<int64_t>(cta) * 2 + sl) * kPartialSlotFloats;
+      float* mine = a.partials + (static_cast<int64_t>(cta) * 2 + (first_unit ? 0 : 1)) * kPartialSlotFloats;
       if (q == 0) {
 #pragma unroll
         for (int t = 0; t < kNE; ++t)
 #pragma unroll
           for (int m = 0; m < kM; ++m) mine[(t * 2 + m) * 128 + r] = vals[t][m];
       }
+    };
+    // A range's last piece (the unit goes on in a later CTA): the hand-off waited for here, as nothing
+    // of the phase is left to overlap it with. Publish this CTA's partial sums and let the last of the
+    // unit's CTAs sum all pieces in CTA order; true in the CTA that must finish the unit (vals then
+    // holds the full sums in its quarter-0 threads). pos / first: the phase's cost position of a tile
+    // and first tile at a cost position; Nc, Ct: the CTAs taking part and the total cost (the CTA of a
+    // tile: the last c with c * Ct / Nc <= pos).
+    auto split_sync = [&](auto& vals, auto kMc, int ub, int ue, int beg, int KI, auto pos, auto first, int Nc,
+                          int Ct) -> bool {
+      constexpr int kM = decltype(kMc)::value;
+      auto cta_of = [&](int i) -> int { return cta_at(pos(i), Ct, Nc); };
+      const bool first_unit = ub / KI == beg / KI;
+      publish(vals, kMc, first_unit);
       // every thread's partial stores, then one thread's release (fence, atomic) makes them all visible
       named_bar_sync(2, kComputeThreads);
       if (tid == 0) {
+        const int c_first = cta_of(ub), c_last = cta_of(ue - 1);
         __threadfence();
         const int old = atomicAdd(&a.counters[c_first], 1);
-        const int last = old == static_cast<int>(c_last - c_first);
+        const int last = old == c_last - c_first;
         if (last) a.counters[c_first] = 0;
-        S.flag = last;
+        S.split_c[0] = last ? c_first : -1;
+        S.split_c[1] = c_last;
       }
       named_bar_sync(2, kComputeThreads);
-      const bool last = S.flag != 0;
-      named_bar_sync(2, kComputeThreads);  // S.flag is reused by the next hand-off
-      if (!last) return false;
+      const int c_first = S.split_c[0], c_last = S.split_c[1];
+      if (c_first < 0) return false;
       __threadfence();
       if (q == 0) {
 #pragma unroll
         for (int t = 0; t < kNE; ++t)
 #pragma unroll
           for (int m = 0; m < kM; ++m) vals[t][m] = 0.0f;
-        for (int64_t c = c_first; c <= c_last; ++c) {
-          const int cs = (ub / KI == first(c * Ct / Nc) / KI) ? 0 : 1;
-          const float* src = a.partials + (c * 2 + cs) * kPartialSlotFloats;
+        for (int c = c_first; c <= c_last; ++c) {
+          const int cs = (ub / KI == first(scaled(c, Ct, Nc)) / KI) ? 0 : 1;
+          const float* src = a.partials + (static_cast<int64_t>(c) * 2 + cs) * kPartialSlotFloats;
 #pragma unroll
           for (int t = 0; t < kNE; ++t)
 #pragma unroll
@@ -820,12 +988,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
+    // Post an item to the helper once every compute thread's stores (partial sums, h, Y) are done
+    // (the barrier, then one thread's release on the item's mbarrier), and go on. An entry is written
+    // again only after the helper has read it.
+    int it = 0;
+    uint32_t iph = 0;
+    auto post = [&](int kind, int ub, int ue, const Unit& un) {
+      named_bar_sync(2, kComputeThreads);
+      if (tid == 0) {
+        if (!mbar_wait(&S.item_empty[it], iph ^ 1u)) atomicExch(a.status, kStatusWaitEmptyTimeout);
+        Shared::Item& m = S.items[it];
+        m.ub = ub;
+        m.ue = ue;
+        m.kind = kind;
+        m.p0 = un.p0;
+        m.n = un.n;
+        m.rb = un.rb;
+        mbar_arrive(&S.item_full[it]);
+      }
+      if (++it == kItems) {
+        it = 0;
+        iph ^= 1u;
+      }
+    };
+    // The combines of the row blocks the helper found complete, out[t, rows] = bf16(sum_j w[t, j] *
+    // Y[inv_pos[t, j], rows]) in slot order: each thread takes outputs tid, tid + 512, ..., so the
+    // threads need not agree on when they look. A row block's last unit is nearly always a range's
+    // last piece, i.e. found at the phase's end, where the compute warps have nothing else to do.
+    int owed_done = 0;
+    auto drain_owed = [&]() {
+      for (;;) {
+        const int n = *reinterpret_cast<volatile int*>(&S.owed_n);
+        if (owed_done >= n) return;
+        __threadfence();  // the helper acquired every unit's Y of the row block before posting it
+        const int rb = reinterpret_cast<volatile int*>(S.owed)[owed_done++];
+        for (int idx = tid; idx < T * 128; idx += kComputeThreads) {
+          const int t = idx >> 7;
+          const int row = rb * 128 + (idx & 127);
+          float acc2 = 0.0f;
+          for (int j = 0; j < k; ++j) {
+            const float y = __ldcg(a.Y + static_cast<int64_t>(S.inv[t * k + j]) * H + row);
+            acc2 = __fadd_rn(acc2, __fmul_rn(S.w[t * k + j], y));
+          }
+          a.out[static_cast<int64_t>(t) * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc2));
+        }
+      }
+    };
 
     // ---------------------------- gate+up ----------------------------
-    for (int64_t i = g_beg; i < g_end;) {
-      const int64_t u = i / KIg;
-      const int64_t ub = u * KIg, ue = ub + KIg;
-      const int64_t pe = ue < g_end ? ue : g_end;
+    for (int i = g_beg; i < g_end;) {
+      const bool first_unit = i == g_beg;
+      const int u = i / KIg;
+      const int ub = u * KIg, ue = ub + KIg;
+      const int pe = ue < g_end ? ue : g_end;
       const Unit un = gu_unit(u);
       float acc[kNE][2];  // gate, up (INT8: sums of scaled group sums)
 #pragma unroll
@@ -890,9 +1105,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[t][m] += __shfl_xor_sync(0xffffffffu, acc[t][m], 1);
           acc[t][m] += __shfl_xor_sync(0xffffffffu, acc[t][m], 2);
         }
-      bool finish = true;
-      if (!(ub >= g_beg && ue <= g_end)) finish = split_unit(acc, std::integral_constant<int, 2>{}, ub, ue, g_beg, KIg, pos_gu, first_gu, Ng, Cg);
-      if (finish) {
+      if (!(ub >= g_beg && ue <= g_end)) {  // split between CTAs
+        if (ue <= g_end) {  // the range's first piece: the helper publishes (and, if last, finishes) it
+          publish(acc, std::integral_constant<int, 2>{}, first_unit);
+          post(kItemGuSplit, ub, ue, un);
+          continue;
+        }
+        if (!split_sync(acc, std::integral_constant<int, 2>{}, ub, ue, g_beg, KIg, pos_gu, first_gu, Ng, Cg)) continue;
+      }
+      {
         const int i_row = un.rb * 128 + r;
         if constexpr (!kInt8) {
           if (q == 0) {
@@ -908,7 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float hv[kNE];
 #pragma unroll
           for (int t = 0; t < kNE; ++t) {
-            float m = 0.0f;  // only quarter 0 holds the full sums after a split unit's hand-off
+            float m = 0.0f;  // only quarter 0 holds the full sums after split_sync
             if (t < un.n) {
               hv[t] = __bfloat162float(__float2bfloat16_rn(silu_mul(acc[t][0], acc[t][1])));
               if (q == 0) m = fabsf(hv[t]);
@@ -942,18 +1163,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    // ---- grid barrier: every CTA's h is written (this CTA's writes are ordered before the arrival)
-    named_bar_sync(2, kComputeThreads);
-    if (tid == 0) {
-      S.gbar_epoch = grid_arrive(a.gbar, N + a.grid_extra);
-      mbar_arrive(&S.gbar_arrived);
-    }
+    // ---- gate+up done: the helper arrives at the grid barrier after the items before this one (the
+    // split units it finishes write h too)
+    post(kItemGuEnd, 0, 0, Unit{0, 0, 0, 0});
 
     // ---------------------------- down ----------------------------
-    for (int64_t i = d_beg; i < d_end;) {
-      const int64_t u = i / KId;
-      const int64_t ub = u * KId, ue = ub + KId;
-      const int64_t pe = ue < d_end ? ue : d_end;
+    for (int i = d_beg; i < d_end;) {
+      const bool first_unit = i == d_beg;
+      const int u = i / KId;
+      const int ub = u * KId, ue = ub + KId;
+      const int pe = ue < d_end ? ue : d_end;
       const Unit un = dn_unit(u);
       float acc[kNE][1];
 #pragma unroll
@@ -1013,43 +1232,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[t][0] += __shfl_xor_sync(0xffffffffu, acc[t][0], 1);
         acc[t][0] += __shfl_xor_sync(0xffffffffu, acc[t][0], 2);
       }
-      bool finish = true;
-      if (!(ub >= d_beg && ue <= d_end)) finish = split_unit(acc, std::integral_constant<int, 1>{}, ub, ue, d_beg, KId, pos_dn, first_dn, Nd, Cd);
-      if (!finish) continue;
-      const int h_row = un.rb * 128 + r;
-      if (q == 0) {
-#pragma unroll
-        for (int t = 0; t < kNE; ++t)
-          if (t < un.n) a.Y[static_cast<int64_t>(un.p0 + t) * H + h_row] = acc[t][0];
-      }
-      // this unit's Y rows are final: count it toward its row block, and let the row block's last
-      // unit write the combine out[t, rows] = bf16(sum_j w[t, j] * Y[inv_pos[t, j], rows]) in slot order
-      // (the barrier, then one thread's fence and atomic, publish every thread's stores)
-      named_bar_sync(2, kComputeThreads);
-      if (tid == 0) {
-        __threadfence();
-        const int old = atomicAdd(&a.ccount[un.rb], 1);
-        const int last = old == NU - 1;
-        if (last) a.ccount[un.rb] = 0;
-        S.flag = last;
-      }
-      named_bar_sync(2, kComputeThreads);
-      const bool last = S.flag != 0;
-      named_bar_sync(2, kComputeThreads);
-      if (last) {
-        __threadfence();
-        for (int idx = tid; idx < T * 128; idx += kComputeThreads) {
-          const int t = idx >> 7;
-          const int row = un.rb * 128 + (idx & 127);
-          float acc2 = 0.0f;
-          for (int j = 0; j < k; ++j) {
-            const float y = __ldcg(a.Y + static_cast<int64_t>(S.inv[t * k + j]) * H + row);
-            acc2 = __fadd_rn(acc2, __fmul_rn(S.w[t * k + j], y));
-          }
-          a.out[static_cast<int64_t>(t) * H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc2));
+      bool whole = true;
+      if (!(ub >= d_beg && ue <= d_end)) {  // split between CTAs
+        if (ue <= d_end) {  // the range's first piece: the helper publishes (and, if last, finishes) it
+          publish(acc, std::integral_constant<int, 1>{}, first_unit);
+          post(kItemDnSplit, ub, ue, un);
+          whole = false;
+        } else {
+          whole = split_sync(acc, std::integral_constant<int, 1>{}, ub, ue, d_beg, KId, pos_dn, first_dn, Nd, Cd);
         }
       }
+      if (whole) {
+        // the unit's Y rows are final; the helper counts the unit toward its row block
+        const int h_row = un.rb * 128 + r;
+        if (q == 0) {
+#pragma unroll
+          for (int t = 0; t < kNE; ++t)
+            if (t < un.n) a.Y[static_cast<int64_t>(un.p0 + t) * H + h_row] = acc[t][0];
+        }
+        post(kItemDnWhole, ub, ue, un);
+      }
+      drain_owed();
     }
+    post(kItemEnd, 0, 0, Unit{0, 0, 0, 0});
+    if (!mbar_wait(&S.helper_done, 0) && tid == 0) atomicExch(a.status, kStatusWaitFullTimeout);
+    drain_owed();
   }
   __syncthreads();
 }
@@ -1145,7 +1352,8 @@ bool decode_step_supported(int T, int H, int I, int E, int k, bool int8) {
   if (T < 1 || T > kDecodeMaxT || static_cast<int64_t>(T) * k > kDecodeMaxP || E > 256) return false;
   if (H % 128 || I % 128) return false;
   if (int8 && (H % 512 || I % 512)) return false;  // scale boxes of 4 groups; two groups per down slot
-  if (int8 && T == 1 && H > 16384) return false;     // the token's records in shared memory
+  // 32-bit schedule arithmetic and the helper's list of row blocks; INT8 at T = 1: the records in shared memory
+  if (H > 16384 || I > 32768) return false;
   return true;
 }
 
