@@ -18,7 +18,8 @@
 //      stable expert-major order), so no CTA waits for another to learn the routing;
 //   2. gate+up: the (expert pass, 128-row block, 128-byte reduction slice) tiles of all active
 //      experts are cut into equal contiguous ranges per CTA (stream-K); a unit split between CTAs
-//      is finished by its last-arriving CTA in a fixed order;
+//      is finished by its head, the CTA holding its first tiles, which adds the later pieces'
+//      partial sums in CTA order (published with a flag, gathered while it works on its own part);
 //   3. one grid-wide barrier (h complete): while waiting, the producer already streams the CTA's
 //      first down-projection weight tiles, which do not depend on h;
 //   4. down, cut the same way, row-block-major; the CTA that completes the last unit of a 128-row
@@ -64,7 +65,15 @@ constexpr int kBar1Threads = kComputeThreads + 32;  // barrier 1: the compute wa
 // Hand-off ring between the compute warps and the helper warp: the compute warps post a finished
 // unit piece (or a phase end) and go on; the helper does the part that waits on global memory.
 constexpr int kItems = 8;
-enum : int { kItemGuSplit = 0, kItemDnSplit = 1, kItemDnWhole = 2, kItemGuEnd = 3, kItemEnd = 4 };
+enum : int {
+  kItemGuPiece = 0,  // a later piece of a split unit: its partial sums are stored, release them to the head
+  kItemDnPiece = 1,
+  kItemGuHead = 2,   // the head piece begins: fetch the unit's later pieces (sum in CTA order) meanwhile
+  kItemDnHead = 3,
+  kItemDnWhole = 4,  // a down unit's Y rows are final: count it toward its row block
+  kItemGuEnd = 5,    // gate+up done: arrive at the grid barrier
+  kItemEnd = 6,
+};
 constexpr int kMaxOwed = 128;  // row blocks of the output (H <= 16384)
 // INT8 token record of one 128-element group (x for gate+up, h for down): the group's values as 24-bit
 // fixed-point integers X = round(v * 2^-e), e chosen so that the group's largest |v| * 2^-e lies in
@@ -95,6 +104,7 @@ struct Shared {
   uint64_t item_full[kItems];   // compute -> helper: an item is posted
   uint64_t item_empty[kItems];  // helper -> compute: the item's entry may be reused
   uint64_t helper_done;         // helper -> compute: every item is handled
+  uint64_t pre_ready;           // helper -> compute: the head's later pieces are summed in `pre`
   struct Item {
     int ub, ue;  // split pieces: the unit's tile range
     int kind, p0, n, rb;
@@ -119,7 +129,6 @@ struct Shared {
   int pc[kDecodeMaxP + 1];  // prefix sums of qc
   float red[2][kComputeWarps][kMaxNEAll];
   int bounds[4];          // this CTA's gate+up and down tile ranges
-  int split_c[2];         // a range's last piece: the unit's CTAs (first, or -1 if not last; last)
 };
 
 // INT8 at one token (kNE = 1): the token's records stay in shared memory for the whole step (written
@@ -127,18 +136,27 @@ struct Shared {
 // only weights and scales and its copies need not wait for the records; the ring has four slots to
 // make room. Measured on GB300, the first gate+up slot landed ~9 us after routing when its token
 // slice had to be written to global memory and copied back.
+//
+// Every unit split between CTAs is finished by its head, the CTA that holds its first tiles (at the
+// end of that CTA's range); its later pieces (at the start of later CTAs' ranges, or a later CTA's
+// whole range) publish their partial sums with a flag, and the head's helper gathers them into
+// `pre` (kNE x 2 x 128 fp32, after Shared) while the head's compute warps work on their part. BF16
+// passes of eight tokens keep five slots to make room for it.
 template <bool kInt8, int kNE>
 struct GeoN : Geo<kInt8> {
   static constexpr bool kRecSmem = kInt8 && kNE == 1;
-  static constexpr int kStages = kRecSmem ? 4 : Geo<kInt8>::kStages;
+  static constexpr int kStages = kRecSmem ? 4 : (!kInt8 && kNE == 8 ? 5 : Geo<kInt8>::kStages);
+  static constexpr int kPreBytes = kNE * 2 * 128 * 4;
 };
 
 constexpr int kSharedBytes = (static_cast<int>(sizeof(Shared)) + 15) / 16 * 16;
 template <bool kInt8, int kNE>
 constexpr int smem_bytes(int H) {
-  return GeoN<kInt8, kNE>::kStages * Geo<kInt8>::kSlot + kSharedBytes + (GeoN<kInt8, kNE>::kRecSmem ? (H / 128) * kRec : 0);
+  return GeoN<kInt8, kNE>::kStages * Geo<kInt8>::kSlot + kSharedBytes + GeoN<kInt8, kNE>::kPreBytes +
+         (GeoN<kInt8, kNE>::kRecSmem ? (H / 128) * kRec : 0);
 }
-static_assert(smem_bytes<false, 8>(0) <= 232448 && smem_bytes<true, 4>(0) <= 232448 &&
+static_assert(smem_bytes<false, 8>(0) <= 232448 && smem_bytes<false, 4>(0) <= 232448 &&
+                  smem_bytes<false, 1>(0) <= 232448 && smem_bytes<true, 4>(0) <= 232448 &&
                   smem_bytes<true, 1>(16384) <= 232448,
               "dynamic shared memory per CTA");
 
@@ -285,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using G = GeoN<kInt8, kNE>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Shared& S = *reinterpret_cast<Shared*>(smem + G::kStages * G::kSlot);
-  uint8_t* const rec_smem = smem + G::kStages * G::kSlot + kSharedBytes;  // kRecSmem: the token's records
+  float* const pre = reinterpret_cast<float*>(smem + G::kStages * G::kSlot + kSharedBytes);  // the head's later pieces
+  uint8_t* const rec_smem = smem + G::kStages * G::kSlot + kSharedBytes + G::kPreBytes;  // kRecSmem: the token's records
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -305,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.item_empty[i], 1);
     }
     mbar_init(&S.helper_done, 1);
+    mbar_init(&S.pre_ready, 1);
     S.owed_n = 0;
     fence_mbar_init();
   }
@@ -842,67 +862,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         count_dn(m.rb);
         continue;
       }
-      // a split piece: publish it; the last of the unit's CTAs (the CTA of a tile: the last c with
-      // c * Ct / Nc <= its cost position) sums all pieces in CTA order
-      const bool gu = m.kind == kItemGuSplit;
-      const int KI = gu ? KIg : KId, Nc = gu ? Ng : Nd, Ct = gu ? Cg : Cd;
-      auto cta_of = [&](int i) -> int { return cta_at(gu ? pos_gu(i) : pos_dn(i), Ct, Nc); };
-      const int c_first = cta_of(m.ub), c_last = cta_of(m.ue - 1);
-      int last = 0;
-      if (lane == 0) {
+      if (m.kind == kItemGuPiece || m.kind == kItemDnPiece) {
+        // the compute warps' partial sums are stored (ordered before this by the item's barrier):
+        // release them to the unit's head (the flag is this CTA's; a CTA has one such piece per phase).
+        // The phases keep apart flags: a down head starts gathering before the grid barrier opens, while
+        // a gate+up flag may still wait for its own head.
+        if (lane == 0) st_release_gpu((m.kind == kItemGuPiece ? a.counters : a.dn_flags) + cta, 1);
+        __syncwarp();
+        continue;
+      }
+      // a head piece begins: sum the unit's later pieces, CTAs cta + 1 .. c_last in order, into `pre`
+      // (each flag cleared once taken: the flags are zero again when the phase's heads are done)
+      const bool gu = m.kind == kItemGuHead;
+      const int c_last = cta_at(gu ? pos_gu(m.ue - 1) : pos_dn(m.ue - 1), gu ? Cg : Cd, gu ? Ng : Nd);
+      const int nv = m.n * 256;  // floats of a piece (token t, gate/up m at (2 t + m) * 128 + row)
+      int32_t* const flags = gu ? a.counters : a.dn_flags;
+      for (int c = cta + 1; c <= c_last; ++c) {
+        if (lane == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(flags + c) == 0) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              atomicExch(a.status, kStatusWaitFullTimeout);
+              break;
+            }
+          }
+          flags[c] = 0;
+        }
+        __syncwarp();
         __threadfence();
-        const int old = atomicAdd(&a.counters[c_first], 1);
-        last = old == c_last - c_first;
-        if (last) a.counters[c_first] = 0;
-      }
-      if (!__shfl_sync(0xffffffffu, last, 0)) continue;
-      __threadfence();
-      // (rare: a range's first piece is normally the unit's first to arrive) the pieces summed in CTA
-      // order, one token at a time; lane: rows lane + 32 j
-      for (int t = 0; t < m.n; ++t) {
-        float v[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-        for (int c = c_first; c <= c_last; ++c) {
-          const int cb = scaled(c, Ct, Nc);
-          const int cs = (m.ub / KI == (gu ? first_gu(cb) : first_dn(cb)) / KI) ? 0 : 1;
-          const float* src = a.partials + (static_cast<int64_t>(c) * 2 + cs) * kPartialSlotFloats + t * 256 + lane;
+        const float* src = a.partials + static_cast<int64_t>(c) * 2 * kPartialSlotFloats;
+        for (int base = 0; base < nv; base += 256) {  // eight loads in flight per lane
+          float v[8];
 #pragma unroll
-          for (int mm = 0; mm < 2; ++mm)
-            if (gu || mm == 0)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) v[mm][j] += __ldcg(src + mm * 128 + 32 * j);
-        }
-        if (!gu) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) a.Y[static_cast<int64_t>(m.p0 + t) * H + m.rb * 128 + lane + 32 * j] = v[0][j];
-        } else if constexpr (!kInt8) {
-          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.h);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            h[static_cast<int64_t>(m.p0 + t) * I + m.rb * 128 + lane + 32 * j] = __float2bfloat16_rn(silu_mul(v[0][j], v[1][j]));
-        } else {
-          // h rounded to bf16, then its record (the 128 rows are one scale group of down's reduction)
-          float hv[4], mx = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            hv[j] = __bfloat162float(__float2bfloat16_rn(silu_mul(v[0][j], v[1][j])));
-            mx = fmaxf(mx, fabsf(hv[j]));
+          for (int j = 0; j < 8; ++j) {
+            const int idx = base + lane + 32 * j;
+            v[j] = (idx < nv && (gu || !(idx & 128))) ? __ldcg(src + idx) : 0.0f;  // down: one sum per token
           }
-          mx = warp_max_abs(mx);
-          const int kh = fixed_exponent(mx);
-          uint8_t* rec = static_cast<uint8_t*>(a.h) + (static_cast<int64_t>(m.p0 + t) * (I / 128) + m.rb) * kRec;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int X = fixed_value(hv[j], kh);
-            const int row = lane + 32 * j;
-            rec[row] = static_cast<uint8_t>(X & 0xff);
-            rec[128 + row] = static_cast<uint8_t>((X >> 8) & 0xff);
-            rec[256 + row] = static_cast<uint8_t>((X >> 16) & 0xff);
+          for (int j = 0; j < 8; ++j) {
+            const int idx = base + lane + 32 * j;
+            if (idx < nv && (gu || !(idx & 128))) pre[idx] = c == cta + 1 ? v[j] : pre[idx] + v[j];
           }
-          if (lane == 0) *reinterpret_cast<float*>(rec + kRecScale) = ldexpf(1.0f, kh);
         }
       }
-      if (!gu) count_dn(m.rb);
       __syncwarp();
+      if (lane == 0) mbar_arrive(&S.pre_ready);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.helper_done);
@@ -932,12 +936,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    // A piece of a unit split between CTAs: this CTA's partial sums (vals[t][m], m < kM, full in
-    // every quarter after the shuffles) into its partial slot, 0 for the phase's first unit, 1 for
-    // the last; the helper publishes them and, in the CTA that arrives last, sums the pieces.
-    auto publish = [&](auto& vals, auto kMc, bool first_unit) {
+    // A later piece of a unit split between CTAs (the range's first unit, begun in an earlier CTA):
+    // this CTA's partial sums (vals[t][m], m < kM, full in every quarter after the shuffles) into its
+    // partial slot, for the unit's head to gather.
+    auto publish = [&](auto& vals, auto kMc) {
       constexpr int kM = decltype(kMc)::value;
-      float* mine = a.partials + (static_cast<int64_t>(cta) * 2 + (first_unit ? 0 : 1)) * kPartialSlotFloats;
+      float* mine = a.partials + static_cast<int64_t>(cta) * 2 * kPartialSlotFloats;
       if (q == 0) {
 #pragma unroll
         for (int t = 0; t < kNE; ++t)
@@ -945,48 +949,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int m = 0; m < kM; ++m) mine[(t * 2 + m) * 128 + r] = vals[t][m];
       }
     };
-    // A range's last piece (the unit goes on in a later CTA): the hand-off waited for here, as nothing
-    // of the phase is left to overlap it with. Publish this CTA's partial sums and let the last of the
-    // unit's CTAs sum all pieces in CTA order; true in the CTA that must finish the unit (vals then
-    // holds the full sums in its quarter-0 threads). pos / first: the phase's cost position of a tile
-    // and first tile at a cost position; Nc, Ct: the CTAs taking part and the total cost (the CTA of a
-    // tile: the last c with c * Ct / Nc <= pos).
-    auto split_sync = [&](auto& vals, auto kMc, int ub, int ue, int beg, int KI, auto pos, auto first, int Nc,
-                          int Ct) -> bool {
+    // A head piece: add the later pieces' sum the helper gathered (their CTA order after the head's)
+    uint32_t pre_ph = 0;
+    auto add_pre = [&](auto& vals, auto kMc) {
       constexpr int kM = decltype(kMc)::value;
-      auto cta_of = [&](int i) -> int { return cta_at(pos(i), Ct, Nc); };
-      const bool first_unit = ub / KI == beg / KI;
-      publish(vals, kMc, first_unit);
-      // every thread's partial stores, then one thread's release (fence, atomic) makes them all visible
-      named_bar_sync(2, kComputeThreads);
-      if (tid == 0) {
-        const int c_first = cta_of(ub), c_last = cta_of(ue - 1);
-        __threadfence();
-        const int old = atomicAdd(&a.counters[c_first], 1);
-        const int last = old == c_last - c_first;
-        if (last) a.counters[c_first] = 0;
-        S.split_c[0] = last ? c_first : -1;
-        S.split_c[1] = c_last;
-      }
-      named_bar_sync(2, kComputeThreads);
-      const int c_first = S.split_c[0], c_last = S.split_c[1];
-      if (c_first < 0) return false;
-      __threadfence();
+      if (!mbar_wait(&S.pre_ready, pre_ph) && tid == 0) atomicExch(a.status, kStatusWaitFullTimeout);
+      pre_ph ^= 1u;
       if (q == 0) {
 #pragma unroll
         for (int t = 0; t < kNE; ++t)
 #pragma unroll
-          for (int m = 0; m < kM; ++m) vals[t][m] = 0.0f;
-        for (int c = c_first; c <= c_last; ++c) {
-          const int cs = (ub / KI == first(scaled(c, Ct, Nc)) / KI) ? 0 : 1;
-          const float* src = a.partials + (static_cast<int64_t>(c) * 2 + cs) * kPartialSlotFloats;
-#pragma unroll
-          for (int t = 0; t < kNE; ++t)
-#pragma unroll
-            for (int m = 0; m < kM; ++m) vals[t][m] += __ldcg(src + (t * 2 + m) * 128 + r);
-        }
+          for (int m = 0; m < kM; ++m) vals[t][m] += pre[(t * 2 + m) * 128 + r];
       }
-      return true;
     };
     // Post an item to the helper once every compute thread's stores (partial sums, h, Y) are done
     // (the barrier, then one thread's release on the item's mbarrier), and go on. An entry is written
@@ -1037,11 +1011,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------- gate+up ----------------------------
     for (int i = g_beg; i < g_end;) {
-      const bool first_unit = i == g_beg;
       const int u = i / KIg;
       const int ub = u * KIg, ue = ub + KIg;
       const int pe = ue < g_end ? ue : g_end;
       const Unit un = gu_unit(u);
+      const bool head = ub >= g_beg && ue > g_end;  // the unit goes on in later CTAs; this one finishes it
+      if (head) post(kItemGuHead, ub, ue, un);      // the helper gathers the later pieces meanwhile
       float acc[kNE][2];  // gate, up (INT8: sums of scaled group sums)
 #pragma unroll
       for (int t = 0; t < kNE; ++t) acc[t][0] = acc[t][1] = 0.0f;
@@ -1105,14 +1080,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[t][m] += __shfl_xor_sync(0xffffffffu, acc[t][m], 1);
           acc[t][m] += __shfl_xor_sync(0xffffffffu, acc[t][m], 2);
         }
-      if (!(ub >= g_beg && ue <= g_end)) {  // split between CTAs
-        if (ue <= g_end) {  // the range's first piece: the helper publishes (and, if last, finishes) it
-          publish(acc, std::integral_constant<int, 2>{}, first_unit);
-          post(kItemGuSplit, ub, ue, un);
-          continue;
-        }
-        if (!split_sync(acc, std::integral_constant<int, 2>{}, ub, ue, g_beg, KIg, pos_gu, first_gu, Ng, Cg)) continue;
+      if (ub < g_beg) {  // a later piece of a unit begun in an earlier CTA: published for its head
+        publish(acc, std::integral_constant<int, 2>{});
+        post(kItemGuPiece, ub, ue, un);
+        continue;
       }
+      if (head) add_pre(acc, std::integral_constant<int, 2>{});
       {
         const int i_row = un.rb * 128 + r;
         if constexpr (!kInt8) {
@@ -1129,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float hv[kNE];
 #pragma unroll
           for (int t = 0; t < kNE; ++t) {
-            float m = 0.0f;  // only quarter 0 holds the full sums after split_sync
+            float m = 0.0f;  // only quarter 0 holds the full sums after add_pre
             if (t < un.n) {
               hv[t] = __bfloat162float(__float2bfloat16_rn(silu_mul(acc[t][0], acc[t][1])));
               if (q == 0) m = fabsf(hv[t]);
@@ -1169,11 +1142,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------- down ----------------------------
     for (int i = d_beg; i < d_end;) {
-      const bool first_unit = i == d_beg;
       const int u = i / KId;
       const int ub = u * KId, ue = ub + KId;
       const int pe = ue < d_end ? ue : d_end;
       const Unit un = dn_unit(u);
+      const bool head = ub >= d_beg && ue > d_end;
+      if (head) post(kItemDnHead, ub, ue, un);
       float acc[kNE][1];
 #pragma unroll
       for (int t = 0; t < kNE; ++t) acc[t][0] = 0.0f;
@@ -1232,17 +1206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[t][0] += __shfl_xor_sync(0xffffffffu, acc[t][0], 1);
         acc[t][0] += __shfl_xor_sync(0xffffffffu, acc[t][0], 2);
       }
-      bool whole = true;
-      if (!(ub >= d_beg && ue <= d_end)) {  // split between CTAs
-        if (ue <= d_end) {  // the range's first piece: the helper publishes (and, if last, finishes) it
-          publish(acc, std::integral_constant<int, 1>{}, first_unit);
-          post(kItemDnSplit, ub, ue, un);
-          whole = false;
-        } else {
-          whole = split_sync(acc, std::integral_constant<int, 1>{}, ub, ue, d_beg, KId, pos_dn, first_dn, Nd, Cd);
-        }
-      }
-      if (whole) {
+      if (ub < d_beg) {  // a later piece of a unit begun in an earlier CTA: published for its head
+        publish(acc, std::integral_constant<int, 1>{});
+        post(kItemDnPiece, ub, ue, un);
+      } else {
+        if (head) add_pre(acc, std::integral_constant<int, 1>{});
         // the unit's Y rows are final; the helper counts the unit toward its row block
         const int h_row = un.rb * 128 + r;
         if (q == 0) {
