@@ -507,7 +507,9 @@ def bench_ours(args, cfg, T):
     roof_kernel, ffn_achieved, ffn_frac, ffn_avg_ms, ffn_alg = roofline_for(moe, wl, ws, stream,
                                                                              max(min(args.steps, 200), 20), peak)
     workload_name = f"{cfg.name}_T{T}" + ("_hostweights" if host else "")
-    traffic = recorded_traffic(workload_name, expert_sources(cfg.wtype))
+    # the one-launch decode step's capture is keyed by its own sources
+    traffic = recorded_traffic(workload_name, DECODE_SOURCES if kernels_per_step(cfg, T, moe) == 1
+                               else expert_sources(cfg.wtype))
 
     # ---- end to end through the C ABI: host inputs in, host result out, every step (the copies
     # overlap the neighbouring steps' compute, double-buffered)

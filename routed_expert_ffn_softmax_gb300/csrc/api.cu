@@ -141,15 +141,17 @@ std::atomic<unsigned long long> g_grid_wait_ns{2000000000ull};
 std::atomic<unsigned long long> g_expert_wait_ns{0};
 
 // Whether moe_ffn_forward runs the fused one-launch decode step for these sizes: by batch shape
-// (policy 0) only INT8 weights at one token, where it measured 2855 GB/s against 2778 for the
-// separate launches on GB300 (Qwen3-235B shapes; end to end with host buffers 2836 against ~2400);
-// at 8 INT8 tokens and for BF16 the separate launches were faster.
+// (policy 0) INT8 weights while the batch has at most one assignment per four experts (about one
+// token per active expert). Measured on GB300 at Qwen3-235B shapes: 3114 / 4333 / 5072 GB/s at
+// T = 1 / 2 / 4 against 2837 / 4076 / 4919 for the separate launches, level at T = 8, behind at
+// T = 16. BF16 came within 1% of the separate launches up to four tokens (Mixtral, DeepSeek-V3)
+// and behind at eight, so BF16 keeps the separate launches.
 bool use_decode_step(int T, int H, int I, int E, int top_k, moe_wtype_t wtype, bool residual) {
   const int policy = g_decode_policy.load(std::memory_order_relaxed);
   if (policy == 1 || residual) return false;
   if (!moe::decode_step_supported(T, H, I, E, top_k, wtype == MOE_W_INT8_G128)) return false;
   if (H / 128 > kMaxRowBlocks) return false;
-  return policy == 2 || (wtype == MOE_W_INT8_G128 && T == 1);
+  return policy == 2 || (wtype == MOE_W_INT8_G128 && static_cast<int64_t>(T) * top_k * 4 <= E);
 }
 
 // Residual-split parts of gate and up (INT8 only); all null when the weights are not split.

@@ -41,12 +41,14 @@ def test_recorded_traffic_only_while_the_hash_matches(tmp_path, monkeypatch):
 
 
 def test_committed_captures_match_the_current_kernels():
-    """Every committed expert and attention capture was taken on the kernels now in the tree."""
+    """Every committed expert, decode-step and attention capture was taken on the kernels now in the tree."""
     with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
     for name, e in rec.items():
         if name.endswith("_attn"):
             sources = bench.ATTN_SOURCES
+        elif e.get("sources") == "DECODE_SOURCES":  # the one-launch decode step
+            sources = bench.DECODE_SOURCES
         else:
             sources = bench.expert_sources(mw.CONFIGS[name.rsplit("_T", 1)[0]].wtype)
         assert e["kernel_source_hash"] == bench.kernel_source_hash(sources), name
