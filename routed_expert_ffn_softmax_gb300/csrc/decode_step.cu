@@ -142,22 +142,29 @@ struct Shared {
 // whole range) publish their partial sums with a flag, and the head's helper gathers them into
 // `pre` (kNE x 2 x 128 fp32, after Shared) while the head's compute warps work on their part. BF16
 // passes of eight tokens keep five slots to make room for it.
-template <bool kInt8, int kNE>
+//
+// A slot holds the pass's kNE token slices at most. INT8 at one token with the records of a row of
+// up to kDeepMaxH elements (kDeep) keeps five slots: a fifth slot of weights streams in while the CTA
+// waits at the grid barrier.
+constexpr int kDeepMaxH = 8448;
+template <bool kInt8, int kNE, bool kDeep = false>
 struct GeoN : Geo<kInt8> {
   static constexpr bool kRecSmem = kInt8 && kNE == 1;
-  static constexpr int kStages = kRecSmem ? 4 : (!kInt8 && kNE == 8 ? 5 : Geo<kInt8>::kStages);
+  static constexpr int kSlot = (Geo<kInt8>::kTokOff + kNE * Geo<kInt8>::kSliceMax + 1023) / 1024 * 1024;
+  static constexpr int kStages = kRecSmem ? (kDeep ? 5 : 4) : (!kInt8 && kNE == 8 ? 5 : Geo<kInt8>::kStages);
   static constexpr int kPreBytes = kNE * 2 * 128 * 4;
+  static_assert(kSlot % 1024 == 0 && kStages <= 8, "slots keep the 1024-byte alignment; eight mbarriers");
 };
 
 constexpr int kSharedBytes = (static_cast<int>(sizeof(Shared)) + 15) / 16 * 16;
-template <bool kInt8, int kNE>
+template <bool kInt8, int kNE, bool kDeep>
 constexpr int smem_bytes(int H) {
-  return GeoN<kInt8, kNE>::kStages * Geo<kInt8>::kSlot + kSharedBytes + GeoN<kInt8, kNE>::kPreBytes +
-         (GeoN<kInt8, kNE>::kRecSmem ? (H / 128) * kRec : 0);
+  using G = GeoN<kInt8, kNE, kDeep>;
+  return G::kStages * G::kSlot + kSharedBytes + G::kPreBytes + (G::kRecSmem ? (H / 128) * kRec : 0);
 }
-static_assert(smem_bytes<false, 8>(0) <= 232448 && smem_bytes<false, 4>(0) <= 232448 &&
-                  smem_bytes<false, 1>(0) <= 232448 && smem_bytes<true, 4>(0) <= 232448 &&
-                  smem_bytes<true, 1>(16384) <= 232448,
+static_assert(smem_bytes<false, 8, false>(0) <= 232448 && smem_bytes<false, 4, false>(0) <= 232448 &&
+                  smem_bytes<false, 1, false>(0) <= 232448 && smem_bytes<true, 4, false>(0) <= 232448 &&
+                  smem_bytes<true, 1, false>(16384) <= 232448 && smem_bytes<true, 1, true>(kDeepMaxH) <= 232448,
               "dynamic shared memory per CTA");
 
 // Stream-K by cost: a tile of a pass with n tokens costs max(kCostMem, kCostBase + kCostTok * n), its
@@ -294,13 +301,13 @@ __device__ __forceinline__ float record_dot(uint32_t rec, int ca, int cb, const 
   return fmaf(static_cast<float>(s[2]), 65536.0f, fmaf(static_cast<float>(s[1]), 256.0f, static_cast<float>(s[0])));
 }
 
-template <bool kInt8, int kNE>
+template <bool kInt8, int kNE, bool kDeep>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_step_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmU,
                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSG,
                        const __grid_constant__ CUtensorMap tmSU, const __grid_constant__ CUtensorMap tmSD,
                        const DecodeArgs a) {
-  using G = GeoN<kInt8, kNE>;
+  using G = GeoN<kInt8, kNE, kDeep>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Shared& S = *reinterpret_cast<Shared*>(smem + G::kStages * G::kSlot);
   float* const pre = reinterpret_cast<float*>(smem + G::kStages * G::kSlot + kSharedBytes);  // the head's later pieces
@@ -523,18 +530,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 128-element scale group, the same layout as h's. CTAs that share a token write the same bytes;
   // each CTA reads only records it has written itself.
   if (kInt8) {
-    if (tid == 0) {
-      uint32_t need = 0u;
-      if (g_beg < g_end) {
-        const int q0 = (g_beg / KIg) / RBg, q1 = ((g_end - 1) / KIg) / RBg;
-        const Unit u0 = unit_of<kNE>(S, q0, 0), u1 = unit_of<kNE>(S, q1, 0);
-        for (int p = u0.p0; p < u1.p0 + u1.n; ++p) need |= 1u << S.sorted[p];
+    uint32_t need = 0u;
+    if constexpr (G::kRecSmem) {
+      need = g_beg < g_end ? 1u : 0u;  // the one token, if this CTA has gate+up tiles (the producer need not wait)
+    } else {
+      if (tid == 0) {
+        if (g_beg < g_end) {
+          const int q0 = (g_beg / KIg) / RBg, q1 = ((g_end - 1) / KIg) / RBg;
+          const Unit u0 = unit_of<kNE>(S, q0, 0), u1 = unit_of<kNE>(S, q1, 0);
+          for (int p = u0.p0; p < u1.p0 + u1.n; ++p) need |= 1u << S.sorted[p];
+        }
+        S.need = need;
       }
-      S.need = need;
+      __syncthreads();
+      need = S.need;
     }
-    __syncthreads();
     if (warp < kComputeWarps) {
-      const uint32_t need = S.need;
       const int ng = H / 128;
       const int nrec = __popc(need) * ng;
       for (int w = warp; w < nrec; w += kComputeWarps) {  // a warp per (token, group) record
@@ -1229,7 +1240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 }
 
-template <bool kInt8, int kNE>
+template <bool kInt8, int kNE, bool kDeep>
 cudaError_t prepare(int* max_ctas) {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev];
@@ -1243,11 +1254,11 @@ cudaError_t prepare(int* max_ctas) {
       return cudaSuccess;
     }
   }
-  e = cudaFuncSetAttribute(decode_step_kernel<kInt8, kNE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  e = cudaFuncSetAttribute(decode_step_kernel<kInt8, kNE, kDeep>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
   if (e != cudaSuccess) return e;
   int per_sm = 0, sms = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_step_kernel<kInt8, kNE>, kThreads,
-                                                    smem_bytes<kInt8, kNE>(16384));
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_step_kernel<kInt8, kNE, kDeep>, kThreads,
+                                                    smem_bytes<kInt8, kNE, kDeep>(kDeep ? kDeepMaxH : 16384));
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
@@ -1269,7 +1280,7 @@ bool encode_scales(CUtensorMap* map, const float* s, int groups, int rows, int E
                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kInt8, int kNE>
+template <bool kInt8, int kNE, bool kDeep = false>
 cudaError_t launch(const DecodePlan& p, cudaStream_t stream) {
   CUtensorMap tg, tu, td, tsg, tsu, tsd;
   if (!tensor_map_encoder()) return cudaErrorNotSupported;
@@ -1285,7 +1296,7 @@ cudaError_t launch(const DecodePlan& p, cudaStream_t stream) {
                 !encode_scales(&tsd, p.s_down, p.I / 128, p.H, p.E)))
     return cudaErrorInvalidValue;
   int max_ctas = 0;
-  cudaError_t e = prepare<kInt8, kNE>(&max_ctas);
+  cudaError_t e = prepare<kInt8, kNE, kDeep>(&max_ctas);
   if (e != cudaSuccess) return e;
   const int ctas = max_ctas < p.max_ctas ? max_ctas : p.max_ctas;
   // cooperative (all CTAs resident: the grid barrier waits on every CTA) and, where the driver
@@ -1300,16 +1311,16 @@ cudaError_t launch(const DecodePlan& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<kInt8, kNE>(p.H);
+  cfg.dynamicSmemBytes = smem_bytes<kInt8, kNE, kDeep>(p.H);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_ok.load(std::memory_order_relaxed) ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8, kNE>, tg, tu, td, tsg, tsu, tsd, p.args);
+  e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8, kNE, kDeep>, tg, tu, td, tsg, tsu, tsd, p.args);
   if (e != cudaSuccess && cfg.numAttrs == 2) {
     cudaGetLastError();  // clear the launch error, then launch cooperatively alone
     pdl_ok.store(0, std::memory_order_relaxed);
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8, kNE>, tg, tu, td, tsg, tsu, tsd, p.args);
+    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<kInt8, kNE, kDeep>, tg, tu, td, tsg, tsu, tsd, p.args);
   }
   return e;
 }
@@ -1332,7 +1343,12 @@ bool decode_step_supported(int T, int H, int I, int E, int k, bool int8) {
 template <bool kInt8>
 cudaError_t launch_ne(const DecodePlan& plan, cudaStream_t stream) {
   const DecodeArgs& a = plan.args;
-  if (a.T == 1) return dec::launch<kInt8, 1>(plan, stream);
+  if (a.T == 1) {
+    if constexpr (kInt8) {  // five slots where the token's records leave room for them
+      if (a.H <= dec::kDeepMaxH) return dec::launch<true, 1, true>(plan, stream);
+    }
+    return dec::launch<kInt8, 1>(plan, stream);
+  }
   if constexpr (kInt8) {
     return dec::launch<true, 4>(plan, stream);  // INT8: passes of at most 4 (the slots hold 4 tokens' records)
   } else {
