@@ -1,6 +1,6 @@
 // Device-side building blocks of the fused decode step (decode_step.cu): contiguous bulk copies,
-// proxy fences, scoped loads and stores for the grid barrier, and the mixed-precision FMAs that take
-// bf16 or fp16 operands with an fp32 accumulator.
+// proxy fences, scoped loads and stores for the grid barrier and the flags, and the mixed-precision
+// FMA that takes bf16 operands with an fp32 accumulator.
 #pragma once
 
 #include "moe_device.cuh"
@@ -76,20 +76,12 @@ __device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
 }
 
 // ---------------------------------------------------------------- mixed-precision FMAs
-// acc += lo(w) * lo(x) + hi(w) * hi(x) for two packed bf16 (or fp16) pairs, each product exact and
-// added to the fp32 accumulator with one rounding (fma.rn.f32.bf16 / .f16).
+// acc += lo(w) * lo(x) + hi(w) * hi(x) for two packed bf16 pairs, each product exact and added to the
+// fp32 accumulator with one rounding (fma.rn.f32.bf16).
 __device__ __forceinline__ float fma2_bf16(uint32_t w2, uint32_t x2, float acc) {
   asm("{.reg .b16 wl, wh, xl, xh;\n\t"
       "mov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
       "fma.rn.f32.bf16 %0, wl, xl, %0;\n\tfma.rn.f32.bf16 %0, wh, xh, %0;}"
-      : "+f"(acc)
-      : "r"(w2), "r"(x2));
-  return acc;
-}
-__device__ __forceinline__ float fma2_f16(uint32_t w2, uint32_t x2, float acc) {
-  asm("{.reg .b16 wl, wh, xl, xh;\n\t"
-      "mov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.f16 %0, wl, xl, %0;\n\tfma.rn.f32.f16 %0, wh, xh, %0;}"
       : "+f"(acc)
       : "r"(w2), "r"(x2));
   return acc;

@@ -26,16 +26,19 @@
 //      block of the output writes that block's combine (fixed slot order, no atomics on data).
 // Per CTA (one per SM; a cooperative launch, so all CTAs are resident for the barrier):
 //   warps 0..15  compute: thread = (weight row r of the tile, quarter q of its 128-byte slice);
-//                mixed-precision FMAs (fma.rn.f32.bf16 / .f16: exact products, fp32 sums) read
-//                the weights straight from the TMA-filled tile and the tokens from the slot;
+//                BF16: mixed-precision FMAs (fma.rn.f32.bf16: exact products, fp32 sums), INT8:
+//                dp4a against the token records, reading the weights straight from the TMA-filled
+//                tile and the tokens from the slot (INT8 at one token: from shared memory);
 //   warp 16      producer: TMA tensor loads of the weight tiles (and INT8 scale boxes), bulk
 //                copies of the tokens' slices (x for gate+up, h for down) into the same slot;
 //   warp 17      helper: the hand-offs that wait on global memory (publishing a split unit's
-//                piece, counting finished down units, the grid barrier's arrival), posted to it by
-//                the compute warps through a small ring in shared memory.
-// INT8 weights become exact fp16 values (one logic op, two byte permutes, two fp16x2 subtractions
-// per four weights); the tokens are fp16 copies of the bf16 values, scaled by a power of two (a row
-// scale for x, a scale per 128-element group for h) that the epilogue multiplies back.
+//                later piece, gathering a head's later pieces, counting finished down units, the
+//                grid barrier's arrival), posted to it by the compute warps through a small ring
+//                in shared memory.
+// INT8: the int8 weights enter dp4a as they are; the tokens (x, and h between the phases) are held
+// as records of 24-bit fixed point per 128-element group (three int8 digit planes and a power-of-two
+// scale), so each group's dot product is exact in int32, then scaled in fp32 by the weight group's
+// and the record's scales.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -240,19 +243,6 @@ __device__ __forceinline__ float warp_max_abs(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
-}
-
-// k with max * 2^-k in [2^14, 2^15) (fp16 keeps every bf16 value from max down to max * 2^-29 exactly),
-// clamped so that 2^k and 2^-k are normal fp32 numbers; 0 for an all-zero or non-finite group.
-__device__ __forceinline__ int f16_exponent(float m) {
-  int k = 0;
-  if (m > 0.0f && m <= 3.0e38f) {
-    int e = 0;
-    frexpf(m, &e);
-    k = e - 15;
-    k = k < -100 ? -100 : (k > 127 ? 127 : k);
-  }
-  return k;
 }
 
 // e with max * 2^-e in [2^22, 2^23) (the 24-bit fixed point of an INT8 token record), kept where 2^e
@@ -821,12 +811,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kHelperWarp) {
     // ================================ helper ================================
     // The part of a unit's end that waits on global memory, in the order the compute warps post it:
-    // a range's first piece of a split unit is published (fence, atomic on the unit's counter) and,
-    // in the CTA that arrives last, the pieces are summed in CTA order and h (gate+up) or Y (down)
-    // written; a finished down unit is counted toward its row block, and the row block's last unit
-    // posts the block's combine to the compute warps; the gate+up phase's end is the arrival at the
-    // grid barrier. Each round trip takes microseconds while HBM streams at full rate (measured on
-    // GB300, ~2.7 us per hand-off), time the compute warps now spend on their next tiles.
+    // a later piece of a split unit (the range's first unit) is released to its head with a flag; a
+    // head piece's start makes the helper gather the unit's later pieces, in CTA order, into `pre`;
+    // a finished down unit is counted toward its row block, and the row block's last unit posts the
+    // block's combine to the compute warps; the gate+up phase's end is the arrival at the grid
+    // barrier. Each round trip takes microseconds while HBM streams at full rate (measured on GB300,
+    // ~2.7 us per hand-off), time the compute warps now spend on their next tiles.
     int it = 0;
     uint32_t iph = 0;
     int owed_n = 0;
