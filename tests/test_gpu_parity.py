@@ -269,9 +269,10 @@ def oracle_rows(cfg, Lc, x, lg, tokens=None):
 
 
 # Every (config, T) point of the four full-size expert shapes (HiNa-MoE §8.1 Table 3 at 1-16
-# tokens per expert), in config order so that one config's layer serves all its T.
+# tokens per expert), plus INT8 at 2 and 4 tokens, where by batch shape the one-launch decode step
+# runs; in config order so that one config's layer serves all its T.
 FULL = [(name, T) for name in ("mixtral8x7b", "mixtral8x22b", "mixtral8x22b_skew", "dsv3", "qwen3_int8")
-        for T in mw.CONFIGS[name].T]
+        for T in sorted(set(mw.CONFIGS[name].T) | ({2, 4} if name == "qwen3_int8" else set()))]
 
 _LAYERS = {}
 
