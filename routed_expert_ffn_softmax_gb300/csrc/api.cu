@@ -21,9 +21,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Workspace layout, in order (each section 256-byte aligned):
 //   ctrl      status word (byte 0), the fused decode step's grid barrier (bytes 8..15), stream-K
-//             counters at byte 256 (the fused decode step: per-CTA flags of its gate+up phase), the
-//             fused decode step's row-block counters at byte 2048 (H / 128 <= 128 of them) and the
-//             per-CTA flags of its down phase at byte 3072
+//             counters at byte 256, the fused decode step's row-block counters at byte 2048
 //   partials  stream-K partial slots
 //   h         [P, I] bf16 (gate+up output)
 //   INT8 only: h16 [P, I] fp16, xg16 [P, H] fp16, h_scale [P], xg_scale [P] f32
@@ -35,9 +33,7 @@ constexpr size_t kCtrlBytes = 4096;
 constexpr size_t kGridBarrierOffset = 8;
 constexpr size_t kCountersOffset = 256;
 constexpr size_t kRowCountersOffset = 2048;
-constexpr size_t kDownFlagsOffset = 3072;
-constexpr int kMaxRowBlocks = static_cast<int>((kDownFlagsOffset - kRowCountersOffset) / 4);  // H <= 32768
-static_assert(kDownFlagsOffset + 4 * kMaxCtas <= kCtrlBytes, "the down phase's flags fit the control block");
+constexpr int kMaxRowBlocks = static_cast<int>((kCtrlBytes - kRowCountersOffset) / 4);  // H <= 65536
 constexpr int kZeroWords = static_cast<int>((kCountersOffset + 4 * kMaxCtas) / 4);
 
 struct Layout {
@@ -386,9 +382,7 @@ moe_status_t ffn_forward_impl(const uint16_t* x, const float* logits, const void
                : static_cast<void*>(ws + L.h);
     a.Y = Y;
     a.partials = reinterpret_cast<float*>(ws + L.partials);
-    a.counters = I32(L.ctrl + kCountersOffset);
     a.ccount = I32(L.ctrl + kRowCountersOffset);
-    a.dn_flags = I32(L.ctrl + kDownFlagsOffset);
     a.gbar = I32(L.ctrl + kGridBarrierOffset);
     a.status = I32(L.ctrl);
     a.ids = ids;

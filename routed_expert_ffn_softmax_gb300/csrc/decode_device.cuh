@@ -1,5 +1,5 @@
 // Device-side building blocks of the fused decode step (decode_step.cu): contiguous bulk copies,
-// proxy fences, scoped loads and stores for the grid barrier and the flags, and the mixed-precision
+// proxy fences, scoped loads and stores for the grid barrier and tagged partial sums, and the mixed-precision
 // FMA that takes bf16 operands with an fp32 accumulator.
 #pragma once
 
@@ -73,6 +73,18 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int32_t* p) {
 
 __device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 64-bit relaxed load and store at GPU scope. A naturally aligned 64-bit access is single-copy atomic,
+// so a value stored together with a tag is read either whole or not at all.
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- mixed-precision FMAs

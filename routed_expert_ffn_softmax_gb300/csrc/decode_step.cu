@@ -19,7 +19,7 @@
 //   2. gate+up: the (expert pass, 128-row block, 128-byte reduction slice) tiles of all active
 //      experts are cut into equal contiguous ranges per CTA (stream-K); a unit split between CTAs
 //      is finished by its head, the CTA holding its first tiles, which adds the later pieces'
-//      partial sums in CTA order (published with a flag, gathered while it works on its own part);
+//      partial sums in CTA order (stored with a tag, gathered while it works on its own part);
 //   3. one grid-wide barrier (h complete): while waiting, the producer already streams the CTA's
 //      first down-projection weight tiles, which do not depend on h;
 //   4. down, cut the same way, row-block-major; the CTA that completes the last unit of a 128-row
@@ -31,10 +31,9 @@
 //                tile and the tokens from the slot (INT8 at one token: from shared memory);
 //   warp 16      producer: TMA tensor loads of the weight tiles (and INT8 scale boxes), bulk
 //                copies of the tokens' slices (x for gate+up, h for down) into the same slot;
-//   warp 17      helper: the hand-offs that wait on global memory (publishing a split unit's
-//                later piece, gathering a head's later pieces, counting finished down units, the
-//                grid barrier's arrival), posted to it by the compute warps through a small ring
-//                in shared memory.
+//   warp 17      helper: the hand-offs that wait on global memory (gathering a head's later
+//                pieces, counting finished down units, the grid barrier's arrival), posted to it by
+//                the compute warps through a small ring in shared memory.
 // INT8: the int8 weights enter dp4a as they are; the tokens (x, and h between the phases) are held
 // as records of 24-bit fixed point per 128-element group (three int8 digit planes and a power-of-two
 // scale), so each group's dot product is exact in int32, then scaled in fp32 by the weight group's
@@ -69,13 +68,11 @@ constexpr int kBar1Threads = kComputeThreads + 32;  // barrier 1: the compute wa
 // unit piece (or a phase end) and go on; the helper does the part that waits on global memory.
 constexpr int kItems = 8;
 enum : int {
-  kItemGuPiece = 0,  // a later piece of a split unit: its partial sums are stored, release them to the head
-  kItemDnPiece = 1,
-  kItemGuHead = 2,   // the head piece begins: fetch the unit's later pieces (sum in CTA order) meanwhile
-  kItemDnHead = 3,
-  kItemDnWhole = 4,  // a down unit's Y rows are final: count it toward its row block
-  kItemGuEnd = 5,    // gate+up done: arrive at the grid barrier
-  kItemEnd = 6,
+  kItemGuHead = 0,   // the head piece begins: gather the unit's later pieces (sum in CTA order) meanwhile
+  kItemDnHead = 1,
+  kItemDnWhole = 2,  // a down unit's Y rows are final: count it toward its row block
+  kItemGuEnd = 3,    // gate+up done: arrive at the grid barrier
+  kItemEnd = 4,
 };
 constexpr int kMaxOwed = 128;  // row blocks of the output (H <= 16384)
 // INT8 token record of one 128-element group (x for gate+up, h for down): the group's values as 24-bit
@@ -115,6 +112,7 @@ struct Shared {
   int owed[kMaxOwed];     // complete row blocks, posted by the helper: the compute warps write their combine
   int owed_n;
   int gbar_epoch;         // the barrier's release word as read before arriving
+  uint32_t tag_base;      // twice the release word at entry: partial sums carry tag_base + 1 (gate+up), + 2 (down)
   uint32_t need;          // INT8: tokens this CTA converts (bit t)
   int A;                  // active experts
   int ids[kDecodeMaxP];   // token t's experts at t * k .. t * k + k - 1 (slot order)
@@ -348,6 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the status word starts each call at 0 (a wait gives up only after kWaitLimitNs, long after every
   // CTA of this cooperative launch has passed this point)
   if (cta == 0 && tid == 0) *a.status = 0;
+  // the launch's tags: the release word advances once per launch, at the grid barrier, which no CTA
+  // passes before every CTA has read it here (the predecessor's advance is visible after the wait)
+  if (tid == 0) S.tag_base = 2u * static_cast<uint32_t>(ld_relaxed_gpu(a.gbar + 1));
   __syncthreads();
 
   // ============================ 1. routing (every CTA) ============================
@@ -811,8 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kHelperWarp) {
     // ================================ helper ================================
     // The part of a unit's end that waits on global memory, in the order the compute warps post it:
-    // a later piece of a split unit (the range's first unit) is released to its head with a flag; a
-    // head piece's start makes the helper gather the unit's later pieces, in CTA order, into `pre`;
+    // a head piece's start makes the helper gather the unit's later pieces, in CTA order, into `pre`
+    // (the later pieces publish themselves, as tagged partial sums);
     // a finished down unit is counted toward its row block, and the row block's last unit posts the
     // block's combine to the compute warps; the gate+up phase's end is the arrival at the grid
     // barrier. Each round trip takes microseconds while HBM streams at full rate (measured on GB300,
@@ -863,41 +864,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         count_dn(m.rb);
         continue;
       }
-      if (m.kind == kItemGuPiece || m.kind == kItemDnPiece) {
-        // the compute warps' partial sums are stored (ordered before this by the item's barrier):
-        // release them to the unit's head (the flag is this CTA's; a CTA has one such piece per phase).
-        // The phases keep apart flags: a down head starts gathering before the grid barrier opens, while
-        // a gate+up flag may still wait for its own head.
-        if (lane == 0) st_release_gpu((m.kind == kItemGuPiece ? a.counters : a.dn_flags) + cta, 1);
-        __syncwarp();
-        continue;
-      }
-      // a head piece begins: sum the unit's later pieces, CTAs cta + 1 .. c_last in order, into `pre`
-      // (each flag cleared once taken: the flags are zero again when the phase's heads are done)
+      // a head piece begins: sum the unit's later pieces, CTAs cta + 1 .. c_last in order, into `pre`.
+      // Each later piece's partial sums are 64-bit stores of (tag, value): a value is this phase's once
+      // its tag is, so the loads themselves are the wait (no flag, no fence on either side). A down head
+      // starts gathering before the grid barrier opens, while the slots may still hold gate+up sums:
+      // those carry the gate+up tag.
       const bool gu = m.kind == kItemGuHead;
+      const uint32_t tag = S.tag_base + (gu ? 1u : 2u);
       const int c_last = cta_at(gu ? pos_gu(m.ue - 1) : pos_dn(m.ue - 1), gu ? Cg : Cd, gu ? Ng : Nd);
-      const int nv = m.n * 256;  // floats of a piece (token t, gate/up m at (2 t + m) * 128 + row)
-      int32_t* const flags = gu ? a.counters : a.dn_flags;
+      const int nv = m.n * 256;  // values of a piece (token t, gate/up m at (2 t + m) * 128 + row)
       for (int c = cta + 1; c <= c_last; ++c) {
-        if (lane == 0) {
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire_gpu(flags + c) == 0) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-              atomicExch(a.status, kStatusWaitFullTimeout);
-              break;
-            }
-          }
-          flags[c] = 0;
-        }
-        __syncwarp();
-        __threadfence();
-        const float* src = a.partials + static_cast<int64_t>(c) * 2 * kPartialSlotFloats;
+        const unsigned long long* src =
+            reinterpret_cast<const unsigned long long*>(a.partials + static_cast<int64_t>(c) * 2 * kPartialSlotFloats);
         for (int base = 0; base < nv; base += 256) {  // eight loads in flight per lane
           float v[8];
+          const uint64_t t0 = global_timer_ns();
+          for (;;) {  // until every value of the batch carries the tag (bounded)
+            bool ready = true;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int idx = base + lane + 32 * j;
-            v[j] = (idx < nv && (gu || !(idx & 128))) ? __ldcg(src + idx) : 0.0f;  // down: one sum per token
+            for (int j = 0; j < 8; ++j) {
+              const int idx = base + lane + 32 * j;
+              v[j] = 0.0f;
+              if (idx < nv && (gu || !(idx & 128))) {  // down: one sum per token
+                const unsigned long long w = ld_relaxed_gpu_u64(src + idx);
+                ready = ready && static_cast<uint32_t>(w >> 32) == tag;
+                v[j] = __uint_as_float(static_cast<uint32_t>(w));
+              }
+            }
+            if (__all_sync(0xffffffffu, ready)) break;
+            if (__shfl_sync(0xffffffffu, global_timer_ns() - t0 > kWaitLimitNs ? 1 : 0, 0)) {
+              if (lane == 0) atomicExch(a.status, kStatusWaitFullTimeout);
+              break;
+            }
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -939,15 +937,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // A later piece of a unit split between CTAs (the range's first unit, begun in an earlier CTA):
     // this CTA's partial sums (vals[t][m], m < kM, full in every quarter after the shuffles) into its
-    // partial slot, for the unit's head to gather.
-    auto publish = [&](auto& vals, auto kMc) {
+    // partial slot as (tag, value) pairs, for the unit's head to gather; nothing else to wait for.
+    auto publish = [&](auto& vals, auto kMc, uint32_t tag) {
       constexpr int kM = decltype(kMc)::value;
-      float* mine = a.partials + static_cast<int64_t>(cta) * 2 * kPartialSlotFloats;
+      unsigned long long* mine =
+          reinterpret_cast<unsigned long long*>(a.partials + static_cast<int64_t>(cta) * 2 * kPartialSlotFloats);
       if (q == 0) {
+        const unsigned long long hi = static_cast<unsigned long long>(tag) << 32;
 #pragma unroll
         for (int t = 0; t < kNE; ++t)
 #pragma unroll
-          for (int m = 0; m < kM; ++m) mine[(t * 2 + m) * 128 + r] = vals[t][m];
+          for (int m = 0; m < kM; ++m) st_relaxed_gpu_u64(mine + (t * 2 + m) * 128 + r, hi | __float_as_uint(vals[t][m]));
       }
     };
     // A head piece: add the later pieces' sum the helper gathered (their CTA order after the head's)
@@ -1082,8 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[t][m] += __shfl_xor_sync(0xffffffffu, acc[t][m], 2);
         }
       if (ub < g_beg) {  // a later piece of a unit begun in an earlier CTA: published for its head
-        publish(acc, std::integral_constant<int, 2>{});
-        post(kItemGuPiece, ub, ue, un);
+        publish(acc, std::integral_constant<int, 2>{}, S.tag_base + 1u);
         continue;
       }
       if (head) add_pre(acc, std::integral_constant<int, 2>{});
@@ -1208,8 +1207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[t][0] += __shfl_xor_sync(0xffffffffu, acc[t][0], 2);
       }
       if (ub < d_beg) {  // a later piece of a unit begun in an earlier CTA: published for its head
-        publish(acc, std::integral_constant<int, 1>{});
-        post(kItemDnPiece, ub, ue, un);
+        publish(acc, std::integral_constant<int, 1>{}, S.tag_base + 2u);
       } else {
         if (head) add_pre(acc, std::integral_constant<int, 1>{});
         // the unit's Y rows are final; the helper counts the unit toward its row block

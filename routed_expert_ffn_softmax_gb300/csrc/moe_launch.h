@@ -131,9 +131,7 @@ struct DecodeArgs {
   uint16_t* x16;         // INT8: [T, H / 128] records of 400 bytes, the token rows as digit planes (scratch)
   void* h;               // BF16: [P, I] bf16; INT8: [P, I / 128] records of 400 bytes (scratch)
   float* Y;              // [P, H] (scratch)
-  float* partials;       // stream-K partial slots, [num CTAs][2][kPartialSlotFloats] (slot 0 used)
-  int32_t* counters;     // per CTA: its gate+up split-unit piece is published; zero on entry, left zero
-  int32_t* dn_flags;     // the same for the down phase (apart: a down head may look before gate+up ends)
+  float* partials;       // per CTA: its split-unit piece as (tag, value) pairs, [num CTAs][2][kPartialSlotFloats]
   int32_t* ccount;       // per 128-row block of H: units done, zero on entry, left zero
   int32_t* gbar;         // grid barrier: [0] arrivals (zero on entry, left zero), [1] release word
   int32_t* status;
