@@ -215,10 +215,10 @@ moe_status_t moe_combine(const float* Y, const int32_t* inv_pos, const float* to
  * learns the routing, so the call is free of host synchronisation.
  * It runs the routing, gather, tensor-core expert kernels and combine as separate launches
  * (linked by programmatic dependent launch), except for INT8 weights while the batch has at
- * most one assignment per four experts (4 * T * top_k <= E, about one token per active
- * expert): that step runs as ONE cooperative kernel that routes, streams both projections on
- * CUDA-core integer dot products and combines (measured faster on GB300 there, level or
- * slower at larger batches and for BF16). moe_set_decode_step_policy can force either way for
+ * most one assignment per two experts (2 * T * top_k <= E) and BF16 weights up to two tokens
+ * (T <= 2): that step runs as ONE cooperative kernel that routes, streams both projections on
+ * CUDA-core dot products (INT8: integer) and combines (measured faster on GB300 there, level
+ * or slower at larger batches). moe_set_decode_step_policy can force either way for
  * small decode batches (T <= 32, T * top_k <= 256, H <= 16384, I <= 32768, H and I multiples
  * of 128, for INT8 multiples of 512). Both give results within the same tolerance of the
  * definition; the routing tables in the workspace are the same.
@@ -231,8 +231,8 @@ moe_status_t moe_ffn_forward(const uint16_t* x, const float* logits, const void*
 
 /*
  * Which implementation moe_ffn_forward uses (process-wide; the default is 0):
- *   0  by batch shape (the one-launch step for INT8 weights with 4 * T * top_k <= E, else the
- *      separate launches);
+ *   0  by batch shape (the one-launch step for INT8 weights with 2 * T * top_k <= E and for
+ *      BF16 weights with T <= 2, else the separate launches);
  *   1  never the one-launch decode step;
  *   2  the one-launch decode step whenever the sizes allow it.
  * Returns MOE_ERR_INVALID_ARG for any other value. Affects only later calls.

@@ -173,7 +173,7 @@ def moe_ffn_forward(x, logits, W_gate, W_up, W_down, s_gate, s_up, s_down, top_k
 
 
 def moe_set_decode_step_policy(policy: int) -> None:
-    """0: by batch shape (default: the one-launch decode step for INT8 with 4 * T * top_k <= E only); 1: never; 2: whenever
+    """0: by batch shape (default: the one-launch decode step for INT8 with 2 * T * top_k <= E and BF16 with T <= 2); 1: never; 2: whenever
     the sizes allow."""
     _check("moe_set_decode_step_policy", load().moe_set_decode_step_policy(policy))
 

@@ -137,17 +137,18 @@ std::atomic<unsigned long long> g_grid_wait_ns{2000000000ull};
 std::atomic<unsigned long long> g_expert_wait_ns{0};
 
 // Whether moe_ffn_forward runs the fused one-launch decode step for these sizes: by batch shape
-// (policy 0) INT8 weights while the batch has at most one assignment per four experts (about one
-// token per active expert). Measured on GB300 at Qwen3-235B shapes: 3114 / 4333 / 5072 GB/s at
-// T = 1 / 2 / 4 against 2837 / 4076 / 4919 for the separate launches, level at T = 8, behind at
-// T = 16. BF16 came within 1% of the separate launches up to four tokens (Mixtral, DeepSeek-V3)
-// and behind at eight, so BF16 keeps the separate launches.
+// (policy 0) INT8 weights while the batch has at most one assignment per two experts (T <= 8 at
+// Qwen3-235B shapes), BF16 weights up to two tokens. Measured on GB300 against the separate
+// launches (the same box, GB/s): INT8 3480 vs 2837 at T = 1, 5160 vs 4919 at T = 4, 5720 vs 5689
+// at T = 8, behind at T = 16; BF16 at T = 1 5920 vs 5730 (Mixtral-8x7B), 5754 vs 5611
+// (DeepSeek-V3), 6375 vs 6201 (Mixtral-8x22B), at T = 2 +0.7-2%, level at T = 4, behind at T = 8.
 bool use_decode_step(int T, int H, int I, int E, int top_k, moe_wtype_t wtype, bool residual) {
   const int policy = g_decode_policy.load(std::memory_order_relaxed);
   if (policy == 1 || residual) return false;
   if (!moe::decode_step_supported(T, H, I, E, top_k, wtype == MOE_W_INT8_G128)) return false;
   if (H / 128 > kMaxRowBlocks) return false;
-  return policy == 2 || (wtype == MOE_W_INT8_G128 && static_cast<int64_t>(T) * top_k * 4 <= E);
+  if (policy == 2) return true;
+  return wtype == MOE_W_INT8_G128 ? static_cast<int64_t>(T) * top_k * 2 <= E : T <= 2;
 }
 
 // Residual-split parts of gate and up (INT8 only); all null when the weights are not split.

@@ -204,9 +204,9 @@ def test_residual_entry_points_reject_bad_arguments(lib):
 
 
 def test_decode_step_policy_and_launch_count(lib):
-    """By batch shape the one-launch decode step runs for INT8 weights with at most one assignment per four experts
-    (when the sizes allow it: T <= 32, P <= 256, H <= 16384, I <= 32768, H and I multiples of 128, INT8 of 512);
-    the policy forces either path; host-only queries."""
+    """By batch shape the one-launch decode step runs for INT8 weights with at most one assignment per two experts
+    and for BF16 weights up to two tokens (when the sizes allow it: T <= 32, P <= 256, H <= 16384, I <= 32768, H and
+    I multiples of 128, INT8 of 512); the policy forces either path; host-only queries."""
     lib.moe_set_decode_step_policy.argtypes = [ctypes.c_int]
     lib.moe_set_decode_step_policy.restype = ctypes.c_int
     f = lib.moe_ffn_forward_launches
@@ -218,10 +218,12 @@ def test_decode_step_policy_and_launch_count(lib):
         assert f(512, 7168, 2048, 256, 8, BF16) == 6        # routing in two launches above 64 tokens
         assert f(64, 4096, 1536, 128, 8, INT8) == 6         # staged INT8: + the fp16 copy of h
         assert f(1, 4096, 1536, 128, 8, INT8) == 1          # INT8 at one token: the one-launch step
-        assert f(4, 4096, 1536, 128, 8, INT8) == 1          # 32 assignments over 128 experts
-        assert f(5, 4096, 1536, 128, 8, INT8) == 6          # 40: the separate launches
-        assert f(2, 512, 512, 8, 2, INT8) == 6              # 4 assignments over 8 experts
-        assert f(1, 7168, 2048, 256, 8, BF16) == 5          # BF16 at one token: the separate launches
+        assert f(8, 4096, 1536, 128, 8, INT8) == 1          # 64 assignments over 128 experts
+        assert f(9, 4096, 1536, 128, 8, INT8) == 6          # 72: the separate launches
+        assert f(3, 512, 512, 8, 2, INT8) == 6              # 6 assignments over 8 experts
+        assert f(1, 7168, 2048, 256, 8, BF16) == 1          # BF16 at one and two tokens: the one-launch step
+        assert f(2, 4096, 14336, 8, 2, BF16) == 1
+        assert f(3, 4096, 14336, 8, 2, BF16) == 5           # three tokens: the separate launches
         assert f(16, 4096, 14336, 8, 2, BF16) == 5          # Mixtral-8x7B, 4 tokens per expert
         assert f(0, 256, 512, 8, 2, BF16) == 0
         assert f(1, 256, 512, 8, 9, BF16) == -1
