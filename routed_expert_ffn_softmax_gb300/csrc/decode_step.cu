@@ -140,7 +140,7 @@ struct Shared {
 //
 // Every unit split between CTAs is finished by its head, the CTA that holds its first tiles (at the
 // end of that CTA's range); its later pieces (at the start of later CTAs' ranges, or a later CTA's
-// whole range) publish their partial sums with a flag, and the head's helper gathers them into
+// whole range) publish their partial sums as tagged 64-bit stores, and the head's helper gathers them into
 // `pre` (kNE x 2 x 128 fp32, after Shared) while the head's compute warps work on their part. BF16
 // passes of eight tokens keep five slots to make room for it.
 //
